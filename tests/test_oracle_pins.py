@@ -1,0 +1,16 @@
+"""The oracle against the pages' worked examples, closed forms, invariants and
+independent library routines (CPU only)."""
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return oracle.load()
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
+def test_pin(lib, pin):
+    pin(lib)
