@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 loss-scaled AdamW optimizer step.
+
+One step is one attempted logical update over k micro-batches, the whole hot
+path: k-1 accumulations, the fused last-micro-batch + unscale + overflow check
++ squared-norm pass, the global norm / clip coefficient, clip + AdamW + recast,
+and the scaler update.  The default workload is the ~1.24B-parameter Llama
+tensor list (146 tensors, bf16 parameters and gradients, fp32 master/m/v and
+accumulation buffer, k = 8 micro-batches, synthetic seeded inputs).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  ``value`` is whole-job Gparams/s (parameters
+updated per second, all ranks) with inputs resident in HBM; ``e2e`` is the same
+metric through the Python binding with the micro-batch gradients copied from
+pinned host memory inside the timed region and the step's status read back.
+With N > 1 (torchrun) each rank runs an independent replica on its own GPU: the
+optimizer step has no exchange of its own, so there is no collective.
+``--impl reference`` times the CPU oracle (the reference statement of the step)
+on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused optimizer-step Gparams/s and achieved HBM GB/s as % of GB300 peak"
+UNIT = "Gparams/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama_1b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas; used with gloo on CPU in the tests)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def whole_job_rate(params_per_step: int, steps: int, world: int, seconds_max: float) -> float:
+    """Gparams/s of the whole job: every rank updates params_per_step per step; the job
+    takes the slowest rank's time."""
+    return params_per_step * steps * world / seconds_max / 1e9
+
+
+# ---------------------------------------------------------------------------
+# peaks, traffic summary, clocks
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            v = float(json.load(fh)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("tl_kernels.cu", "tl_internal.cuh"):
+        with open(os.path.join(ROOT, "loss_scaled_adamw_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, if it was taken
+    from the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        line = line.strip()
+        if "=" in line and not line.startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    v = kv.get(kernel_key + ".dram_bytes_per_launch")
+    return float(v) if v else None
+
+
+def gpu_id(local_rank: int) -> str:
+    """nvidia-smi's id of this process's GPU (its UUID, whatever CUDA_VISIBLE_DEVICES says)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local_rank)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu_index)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, a in enumerate(r[3]) if a.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+KERNEL_BYTES = {  # algorithmic bytes per parameter per launch (bf16 grads and params)
+    "accumulate_first": 2 + 4,
+    "accumulate": 2 + 4 + 4,
+    "unscale_check": 2 + 4 + 4,
+    "clip_adamw_step": 16 + 12 + 2,
+}
+
+
+class GpuWorkload:
+    """Device-resident tensor lists of a workload, packed into flat buffers."""
+
+    def __init__(self, wl, device):
+        import torch
+        import loss_scaled_adamw_gb300 as tl
+        from loss_scaled_adamw_gb300 import workloads as W
+        self.wl = wl
+        P = wl.P
+        self.P = P
+        self.device = device
+        offs = np.cumsum([0] + wl.numel[:-1]).tolist()
+        assert all(o % 8 == 0 for o in offs)  # every tensor starts on a 16-byte boundary
+        self.master = W.master_init(wl, device)
+        self.param = W.to_16bit(self.master, wl.param_dtype)
+        self.m = torch.zeros(P, dtype=torch.float32, device=device)
+        self.v = torch.zeros(P, dtype=torch.float32, device=device)
+        self.acc = torch.empty(P, dtype=torch.float32, device=device)
+        self.grads = [W.grad_input(wl, 1, i, device=device) for i in range(wl.k)]
+
+        def plist(t):
+            es, base = t.element_size(), t.data_ptr()
+            p = tl.PtrList([base + o * es for o in offs])
+            p.tensors = [t]
+            return p
+
+        self.plists = {n: plist(getattr(self, n)) for n in ("param", "master", "m", "v", "acc")}
+        self.gplists = [plist(g) for g in self.grads]
+        dt = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32}
+        cfg = tl.make_config(dt[wl.param_dtype], dt[wl.grad_dtype], wl.scaler_enabled,
+                             wl.init_scale if wl.scaler_enabled else 1.0, interval=wl.interval)
+        L = self.plists
+        self.ctx = tl.tl_create(wl.numel, L["param"], L["master"], L["m"], L["v"], L["acc"], cfg)
+        self.counts = wl.counts(1)
+        self.N = sum(self.counts)
+        self.hp = tl.tl_adamw_hp(1e-3, 0.9, 0.95, 1e-8, 0.1)
+
+    def step(self, events=None):
+        """One logical update; with `events`, a pair of CUDA events around every call."""
+        import loss_scaled_adamw_gb300 as tl
+        k = self.wl.k
+        calls = []
+        for i in range(k - 1):
+            calls.append(("accumulate_first" if i == 0 else "accumulate",
+                          lambda i=i: tl.tl_accumulate(self.ctx, self.gplists[i], self.counts[i], self.N, 1 if i == 0 else 0)))
+        calls.append(("unscale_check", lambda: tl.tl_unscale_check(self.ctx, self.gplists[k - 1], self.counts[k - 1], self.N)))
+        calls.append(("grad_norm", lambda: tl.tl_grad_norm(self.ctx, self.wl.max_norm)))
+        calls.append(("clip_adamw_step", lambda: tl.tl_clip_adamw_step(self.ctx, self.hp)))
+        calls.append(("scaler_update", lambda: tl.tl_scaler_update(self.ctx)))
+        for name, fn in calls:
+            if events is None:
+                fn()
+            else:
+                import torch
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                events.append((name, a, b))
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import loss_scaled_adamw_gb300 as tl
+    from loss_scaled_adamw_gb300 import workloads as W
+    from loss_scaled_adamw_gb300 import _build
+    _build.build()
+    tl.load_library()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    wl = W.make(args.workload)
+    gw = GpuWorkload(wl, device)
+    P, k = wl.P, wl.k
+    step_bytes = P * (KERNEL_BYTES["accumulate_first"] + (k - 2) * KERNEL_BYTES["accumulate"]
+                      + KERNEL_BYTES["unscale_check"] + KERNEL_BYTES["clip_adamw_step"]) if k > 1 else \
+        P * (6 + KERNEL_BYTES["clip_adamw_step"])
+    for _ in range(args.warmup):
+        gw.step()
+    torch.cuda.synchronize()
+    barrier()
+
+    # ---- device-resident timed region ----
+    events = []
+    launches0 = tl.tl_launch_count(gw.ctx)
+    with ClockSampler(gpu_id(local_rank)) as clk:
+        torch.cuda.synchronize()
+        barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            gw.step(events)
+        t1.record()
+        torch.cuda.synchronize()
+        barrier()
+        elapsed = t0.elapsed_time(t1) / 1e3
+        launches = tl.tl_launch_count(gw.ctx) - launches0
+
+        # ---- end-to-end through host buffers ----
+        e2e = None
+        if not args.no_e2e:
+            e2e = run_e2e(args, gw, world)
+    elapsed_max = max_over_ranks(elapsed, device)
+    st = tl.tl_read_status(gw.ctx)
+
+    per = {}
+    for name, a, b in events:
+        per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    peak, peak_kind = hbm_peak()
+    kernels = {}
+    for name, ts in per.items():
+        avg = sum(ts) / len(ts)
+        entry = {"launches": len(ts), "avg_ms": avg * 1e3, "share": sum(ts) / elapsed}
+        if name in KERNEL_BYTES:
+            gbs = KERNEL_BYTES[name] * P / avg / 1e9
+            entry.update({"bytes_per_launch": KERNEL_BYTES[name] * P, "achieved_gbs": gbs, "frac": gbs / peak})
+        kernels[name] = entry
+    dom = max((n for n in kernels if n in KERNEL_BYTES), key=lambda n: kernels[n]["share"] * 1.0)
+    value = whole_job_rate(P, args.steps, world, elapsed_max)
+    clocks = clk.summary()
+    traffic_key = {"accumulate": "k_accumulate_bf16", "clip_adamw_step": "k_adamw_bf16",
+                   "unscale_check": "k_unscale_bf16_acc_grad", "accumulate_first": "k_accumulate_first_bf16"}[dom]
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; random-init masters, N(0,1e-3) bf16 grads)",
+        "config": {"workload": f"{wl.name}: ~1.24B-param Llama tensor list, {len(wl.numel)} tensors, P={P}, "
+                               f"bf16 params/grads, fp32 master/m/v/acc, k={k} micro-batches"
+                               if wl.name == "llama_1b" else f"{wl.name}: {len(wl.numel)} tensors, P={P}, k={k}",
+                   "P": P, "k": k, "tensors": len(wl.numel), "counts": gw.counts,
+                   "l2": "no flush: every launch streams >= 7.4 GB, far above the 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm": {"algorithmic_bytes_per_step": step_bytes, "bytes_per_param": step_bytes / P,
+                "achieved_gbs_per_gpu": step_bytes * args.steps / elapsed_max / 1e9,
+                "peak_gbs": peak, "peak_kind": peak_kind,
+                "frac": step_bytes * args.steps / elapsed_max / 1e9 / peak},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
+                     "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(traffic_key)},
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "status": {"S": st.S, "t": st.t, "skipped": st.skipped, "norm": st.norm},
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    return out
+
+
+def run_e2e(args, gw, world):
+    """Same metric through the binding with the k micro-batch gradients copied from pinned
+    host memory every step (on a copy stream, overlapped with the accumulations) and the
+    status read back to the host."""
+    import torch
+    import loss_scaled_adamw_gb300 as tl
+    k = gw.wl.k
+    host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gw.grads]
+    for h, g in zip(host, gw.grads):
+        h.copy_(g)
+    torch.cuda.synchronize()
+    copy_stream = torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    status_bytes = 64  # sizeof(tl_status)
+
+    def one():
+        evs = []
+        with torch.cuda.stream(copy_stream):
+            for i in range(k):
+                gw.grads[i].copy_(host[i], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy_stream)
+                evs.append(e)
+        for i in range(k - 1):
+            compute.wait_event(evs[i])
+            tl.tl_accumulate(gw.ctx, gw.gplists[i], gw.counts[i], gw.N, 1 if i == 0 else 0)
+        compute.wait_event(evs[k - 1])
+        tl.tl_unscale_check(gw.ctx, gw.gplists[k - 1], gw.counts[k - 1], gw.N)
+        tl.tl_grad_norm(gw.ctx, gw.wl.max_norm)
+        tl.tl_clip_adamw_step(gw.ctx, gw.hp)
+        tl.tl_scaler_update(gw.ctx)
+        copy_stream.wait_stream(compute)  # the next step's copies overwrite the device grads
+        return tl.tl_read_status(gw.ctx)  # device -> host read of the step's result
+
+    one()
+    torch.cuda.synchronize()
+    barrier()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    torch.cuda.synchronize()
+    el = max_over_ranks(time.perf_counter() - t, gw.device)
+    return {"value": whole_job_rate(gw.P, args.steps, world, el), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": status_bytes, "ms_per_step": el / args.steps * 1e3,
+            "how": "grads copied from pinned host memory each step on a copy stream overlapped with the "
+                   "accumulations; status read back each step"}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, n_params: int):
+    """A contiguous slice of the workload's flat tensor list: masters and k gradients."""
+    import torch
+    from loss_scaled_adamw_gb300 import workloads as W
+    n = min(n_params, wl.P)
+    g = torch.Generator().manual_seed(W.SEED)
+    master = (torch.randn(n, generator=g) * wl.master_std).numpy().astype(np.float32)
+    grads = [W.to_16bit(torch.randn(n, generator=g) * wl.grad_std, wl.grad_dtype).view(torch.int16).numpy()
+             .view(np.uint16) for _ in range(wl.k)]
+    p0 = W.to_16bit(torch.from_numpy(master), wl.param_dtype).view(torch.int16).numpy().view(np.uint16)
+    return master, p0, grads
+
+
+def time_oracle(wl, seconds: float, steps: int = 1):
+    """Time the oracle's logical update on a sample sized for about `seconds` of CPU time."""
+    import oracle
+    n = 1 << 20
+    master, p0, grads = oracle_sample(wl, n)
+    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype)
+    t = time.perf_counter()
+    o.step(grads, wl.counts(1), wl.max_norm)
+    per_param = (time.perf_counter() - t) / n
+    n = int(min(max(seconds / max(steps, 1) / per_param, 1 << 20), 1 << 27, wl.P))
+    master, p0, grads = oracle_sample(wl, n)
+    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype)
+    t = time.perf_counter()
+    for s in range(steps):
+        o.step(grads, wl.counts(s + 1), wl.max_norm)
+    el = time.perf_counter() - t
+    return {"value": n * steps / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} parameters (a contiguous slice of the {wl.name} tensor list), k={wl.k}, "
+                      f"{steps} logical update(s), {el:.1f} s, single-threaded C oracle"}
+
+
+def run_reference(args, rank, world):
+    from loss_scaled_adamw_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    wl = W.make(args.workload)
+    per_step = max(args.cpu_seconds / max(args.steps, 1), 1.0)
+    for _ in range(min(args.warmup, 1)):
+        time_oracle(wl, 0.5)
+    t = time.perf_counter()
+    res = time_oracle(wl, per_step * args.steps, steps=args.steps)
+    el = time.perf_counter() - t
+    return {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": f"{wl.name}: sample of the tensor list on the host cores", "P": wl.P, "k": wl.k},
+            "cpu_baseline": res, "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        # rank 0 alone times the oracle on the host cores; other ranks exit without work
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    if True:
+        out = run_gpu(args, rank, world, local_rank)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                from loss_scaled_adamw_gb300 import workloads as W
+                import oracle
+                oracle.build()
+                out["cpu_baseline"] = time_oracle(W.make(args.workload), args.cpu_seconds)
+            print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+/*
+ * tl.h - C ABI of the GB300 loss-scaled AdamW optimizer step.
+ *
+ * One attempted logical update over k micro-batches is the call sequence
+ *
+ *     tl_accumulate(first=1) ; tl_accumulate(first=0) x (k-2) ;
+ *     tl_unscale_check ; tl_grad_norm ; tl_clip_adamw_step ; tl_scaler_update
+ *
+ * (with k = 1: tl_unscale_check alone takes the only micro-batch), in the
+ * order the Megatron page fixes ("Megatron Internals III: Mixed Precision,
+ * Loss Scaling, and Grad Clipping", section 9 "The order matters": detect
+ * overflow, copy gradients to fp32 main buffers, unscale, global norm, clip,
+ * step fp32 masters, copy back).  Every call is asynchronous on the stream it
+ * is given and never waits for the device, except tl_read_status,
+ * tl_get_state and tl_set_state, which synchronise that stream.  The skip
+ * decision, the loss scale and the optimizer step count live on the device:
+ * no call reads a device value back to decide anything, so the whole
+ * sequence can be enqueued (or captured) without a host synchronisation.
+ *
+ * Memory ownership.  The caller owns every tensor: the 16-bit model
+ * parameters, the micro-batch gradients and the fp32 master weights, first
+ * and second moments and accumulation buffer.  Pointers are device pointers
+ * (or any address the device can load and store).  The library owns only
+ * the opaque context: its chunk table, per-chunk norm partials, a cache of
+ * gradient-pointer tables, and the device scalars (loss scale, good-step
+ * count, optimizer step, beta powers, overflow flag, norm, clip coefficient).
+ *
+ * Tensor lists.  A tensor list is an array of ntensors pointers, tensor i
+ * holding numel[i] contiguous elements.  Every list given to one context
+ * uses the same ntensors and numel[].  Distinct tensors must not overlap,
+ * in any list (a tensor passed twice would be counted twice in the global
+ * norm; the tied input/output table appears once).  A pointer must be
+ * aligned to its element size; 16-byte alignment takes the vector path,
+ * anything else a scalar path.
+ *
+ * Errors.  Every function returns a status code; nothing is thrown across
+ * this boundary.  A call that returns an error has enqueued no work.
+ * Non-finite gradients are NOT an error: they set the device overflow flag
+ * and the update is skipped on the device.
+ *
+ * Pages cited (by title):
+ *   [MP]  "Mixed precision, loss scaling, gradient accumulation, and
+ *         activation checkpointing" (tinyllm module L11.1)
+ *   [MEG] "Megatron Internals III: Mixed Precision, Loss Scaling, and Grad
+ *         Clipping"
+ *   [ZRO] "Your weights fit on one device but Adam's moments do not - how do
+ *         you shard the optimizer state?"
+ *   [RST] "Practical LLM in Rust", chapter 13 "Accumulate gradients and
+ *         recompute activations"
+ */
+#ifndef TL_H
+#define TL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define TL_OK 0
+#define TL_EINVAL 1   /* bad argument: count, size, dtype, pointer, overlap, scaler setting */
+#define TL_ECUDA 2    /* a CUDA runtime call or kernel launch failed */
+#define TL_ESTATE 3   /* call out of order in the update sequence, or not allowed now */
+#define TL_ENOMEM 4   /* the context could not allocate its own device/host memory */
+
+/* Element types. */
+#define TL_F32 0
+#define TL_BF16 1
+#define TL_F16 2
+
+typedef struct tl_ctx tl_ctx;
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef void* tl_stream;
+
+/* Static configuration, fixed at tl_create.
+ * [MP] section 4 "The interface": DynamicLossScaler(init=2^16, growth=2,
+ * backoff=0.5, interval=2000); [MEG] section 5: the controller and its
+ * min_loss_scale floor.  All five scale values must be powers of two so that
+ * unscaling only changes exponents ([MP] section 2 "Loss scaling").  With
+ * scaler_enabled = 0 (bf16 training, [MP] "Dynamic scaling": bf16 needs no
+ * scaler) S stays 1, the good-step count stays 0, and the finite check still
+ * gates every update. */
+typedef struct {
+    int32_t param_dtype;    /* TL_BF16 or TL_F16: the model copy */
+    int32_t grad_dtype;     /* TL_BF16, TL_F16 or TL_F32: the micro-batch gradients */
+    int32_t scaler_enabled; /* 1: dynamic loss scaling; 0: S = 1 fixed */
+    float init_scale;       /* S0 > 0, a power of two (e.g. 65536) */
+    float growth;           /* > 1, a power of two (2) */
+    float backoff;          /* in (0,1), a power of two (0.5) */
+    int32_t interval;       /* >= 1 good steps between growths (2000) */
+    float min_scale;        /* > 0, a power of two; S never goes below it (1) */
+    float max_scale;        /* >= min_scale, a power of two; S never exceeds it (2^127) */
+} tl_config;
+
+/* AdamW hyper-parameters of one update (may change between updates, e.g.
+ * under a learning-rate schedule).  beta1, beta2 in [0.5, 1), eps > 0,
+ * lr >= 0, weight_decay >= 0. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} tl_adamw_hp;
+
+/* The resumable scaler/optimizer scalars ([MP] section 4: state_dict keeps S
+ * and the count; [RST] ch. 13: the optimizer state includes the beta powers
+ * and the step).  b1p = beta1^t and b2p = beta2^t as products of the betas
+ * actually used. */
+typedef struct {
+    float S;
+    int32_t count;
+    int64_t t;
+    double b1p, b2p;
+} tl_state;
+
+/* Diagnostic snapshot (tests and logging). */
+typedef struct {
+    float S;            /* current loss scale */
+    int32_t count;      /* good steps since the last overflow or growth */
+    int64_t t;          /* committed optimizer steps */
+    int32_t skipped;    /* 1 if the last finished update was skipped */
+    int32_t found_inf;  /* overflow flag of the update in flight (0 after tl_scaler_update) */
+    float norm;         /* global L2 norm of the last update's unscaled gradient */
+    float coef;         /* clip coefficient applied by the last update (<= 1) */
+    double sumsq;       /* squared norm in fp64 */
+    double b1p, b2p;
+} tl_status;
+
+/* Create a context for one tensor list.
+ * ntensors >= 0; numel[i] >= 0.  param[i]: ntensors 16-bit model tensors of
+ * param_dtype; master/m/v/acc[i]: fp32 tensors of the same sizes ([MEG]
+ * section 1: fp16/bf16 param, fp32 master, fp32 Adam m and v; [MEG] section
+ * 8: the fp32 master-gradient buffer).  The caller initialises master,
+ * param, m and v; acc needs no initialisation.  Host arrays are copied
+ * before return.  The context's device scalars start at S = init_scale
+ * (1 when disabled), count 0, t 0, b1p = b2p = 1.  stream orders the
+ * initial uploads; tl_create returns after they are complete.
+ * Errors: TL_EINVAL (NULL/misaligned/overlapping pointers, bad sizes or
+ * configuration), TL_ENOMEM, TL_ECUDA. */
+int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const* param,
+              float* const* master, float* const* m, float* const* v, float* const* acc,
+              const tl_config* cfg, tl_stream stream);
+
+/* Release the context (waits for the device first).  NULL is accepted. */
+int tl_destroy(tl_ctx* ctx);
+
+/* Accumulate micro-batch i into the fp32 buffer (step a2).
+ * [RST] ch. 13 "Weight each mean by the targets it represents": N = sum n_i,
+ * the gradient of the mean over N targets is sum_i (n_i/N) grad L_i; [MP]
+ * section 2 "Gradient accumulation": no zeroing in between.
+ * grads: ntensors device pointers of grad_dtype, the gradient of micro-batch
+ * i's MEAN loss times S.  n_i > 0 valid targets of this micro-batch, N the
+ * total of the logical update (N <= 2^53, same N for every call of one
+ * update).  w_i = fl32(n_i / N) computed in fp64 on the host.
+ * first = 1: acc = w_i * g (starts an update, discarding any partial one);
+ * first = 0: acc = fma(w_i, g, acc).
+ * Errors: TL_EINVAL (counts, NULL pointer), TL_ESTATE (first = 0 with no
+ * update open, or after tl_unscale_check). */
+int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N, int first,
+                  tl_stream stream);
+
+/* Last micro-batch + unscale + overflow check + squared-norm partials (a3).
+ * [MEG] section 8: cast, divide by the loss scale, place in the flattened
+ * master-gradient buffer; [MEG] section 6: the overflow flag; [MP] "Loss
+ * scaling": S a power of two makes unscaling exact.
+ * u = (fma(w_k, g_k, acc), or w_k * g_k if no micro-batch was accumulated
+ * before) * (1/S), stored into acc; the device overflow flag is raised if any
+ * u is not finite; one fp64 partial sum of fl32(u*u) is written per chunk.
+ * grads = NULL: all micro-batches were accumulated already (n_k ignored),
+ * u = acc * (1/S).  The n_i of the update must total N by this call.
+ * Errors: TL_EINVAL (counts do not add up to N), TL_ESTATE (out of order). */
+int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t N,
+                     tl_stream stream);
+
+/* Global L2 norm and clip coefficient (a4).  [MEG] section 9: global_norm =
+ * sqrt(sum ||grad||^2), clip_coef = max_norm / (global_norm + eps); the
+ * coefficient is applied only when below 1 (eps = 1e-6); max_norm <= 0
+ * disables clipping (coef = 1, the norm is still computed).  The partials
+ * are reduced in a fixed order, so the norm is deterministic.  A non-finite
+ * squared norm raises the overflow flag.  Errors: TL_ESTATE. */
+int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream);
+
+/* Clip + AdamW on the fp32 masters + recast to the model dtype (a5).
+ * [MEG] sections 7 and 9 (clip with the global coefficient, step the fp32
+ * masters, copy back to model precision); [ZRO] "Why the optimizer state is
+ * the thing that overflows" (bias-corrected first moment over the root of
+ * the bias-corrected second moment plus a small constant); [RST] ch. 13
+ * (decoupled weight decay; beta powers as state).  Per element, in fp32 with
+ * each operation rounded to nearest:
+ *   g = u*coef; m = b1*m + (1-b1)*g; v = b2*v + (1-b2)*(g*g);
+ *   w = w - (lr*wd)*w; w = w - (lr/(1-b1^(t+1))) * (m / (sqrt(v)/sqrt(1-b2^(t+1)) + eps));
+ *   param = round-to-nearest-even(w).
+ * If the overflow flag is set the kernel exits without touching any tensor.
+ * Errors: TL_EINVAL (hp), TL_ESTATE. */
+int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream);
+
+/* Scaler state machine and optimizer scalars (a6).  [MEG] section 5; [MP]
+ * "Dynamic scaling" and the five-step trace of section 3; [RST] ch. 13
+ * "Discard a failed partial logical update".
+ * Overflow: S = max(S*backoff, min_scale), count = 0, t and the beta powers
+ * unchanged, skipped = 1.  Clean: t += 1, beta powers advanced, count += 1,
+ * and when count reaches interval S = min(S*growth, max_scale), count = 0.
+ * Clears the overflow flag and closes the update.  Errors: TL_ESTATE. */
+int tl_scaler_update(tl_ctx* ctx, tl_stream stream);
+
+/* Synchronous reads and writes of the device scalars (these wait for the
+ * stream).  tl_set_state is allowed only between updates and checks S
+ * (power of two within [min_scale, max_scale], or 1 when disabled), count
+ * (0 <= count < interval) and t >= 0 ([MP] section 4 catalogue: a resume
+ * keeps S and the count; bad arguments raise).  Errors: TL_EINVAL,
+ * TL_ESTATE, TL_ECUDA. */
+int tl_read_status(tl_ctx* ctx, tl_status* out, tl_stream stream);
+int tl_get_state(tl_ctx* ctx, tl_state* out, tl_stream stream);
+int tl_set_state(tl_ctx* ctx, const tl_state* in, tl_stream stream);
+
+/* Device address of the current loss scale S (fp32), for scaling the loss
+ * on the device without a host read ([MP] section 4: scale(loss) = loss*S).
+ * Valid until tl_destroy. */
+const float* tl_scale_ptr(const tl_ctx* ctx);
+
+/* Sizes of the context: total elements and work chunks. */
+int64_t tl_num_params(const tl_ctx* ctx);
+int64_t tl_num_chunks(const tl_ctx* ctx);
+
+/* Number of kernels this context has launched so far. */
+int64_t tl_launch_count(const tl_ctx* ctx);
+
+/* Human-readable text of a status code, and of the last error a context saw. */
+const char* tl_status_string(int status);
+const char* tl_last_error(const tl_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TL_H */

@@ -1,0 +1,576 @@
+// tl_api.cu - host side of the C ABI declared in include/tl.h.
+//
+// Holds the opaque context: argument validation (all of it before any work is
+// enqueued), the chunk table of the multi-tensor-apply launcher (built once per
+// tensor list and kept on the device), the per-chunk norm partials, the device
+// scalars, a cache of device-resident gradient pointer tables for lists too
+// long to pass by value, and the order of the calls of one logical update.
+#include "tl_internal.cuh"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/tl.h"
+
+using namespace tl;
+
+namespace {
+
+enum Phase { kIdle = 0, kAccum = 1, kUnscaled = 2, kNormed = 3, kStepped = 4 };
+
+int elem_size(int dt) { return dt == TL_F32 ? 4 : 2; }
+
+bool is_pow2(float x) {
+    if (!(x > 0.0f) || !std::isfinite(x)) return false;
+    int e = 0;
+    return std::frexp(x, &e) == 0.5f;
+}
+
+struct Interval {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+// A device-resident gradient pointer table keyed by the host pointer array.
+struct GradSlot {
+    std::vector<const void*> key;
+    uint64_t hash = 0;
+    const void** d_tab = nullptr;   // ntensors device pointers
+    const void** h_stage = nullptr; // pinned staging copy
+    cudaEvent_t last_use = nullptr;
+    uint64_t stamp = 0;
+    bool valid = false;
+};
+
+constexpr int kGradSlots = 16;
+
+uint64_t hash_ptrs(const void* const* p, int64_t n) {
+    uint64_t h = 1469598103934665603ull;
+    for (int64_t i = 0; i < n; ++i) {
+        h ^= reinterpret_cast<uintptr_t>(p[i]);
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+}  // namespace
+
+struct tl_ctx {
+    int device = 0;
+    int sm_count = 0;
+    tl_config cfg{};
+    int64_t ntensors = 0;
+    int64_t P = 0;
+    int64_t nchunks = 0;
+    std::vector<int64_t> numel;
+    std::vector<Interval> state_iv;  // sorted intervals of every state tensor
+    Chunk* d_chunks = nullptr;
+    TensorPtrs* d_tp = nullptr;
+    double* d_partials = nullptr;
+    DevState* d_state = nullptr;
+    GradSlot slots[kGradSlots];
+    uint64_t clock = 0;
+    int grid_acc[3][2] = {{0}};
+    int grid_uns[3][3] = {{0}};
+    int grid_adam[3] = {0};
+    // the update in flight
+    int phase = kIdle;
+    int64_t n_sum = 0;
+    int64_t N_update = 0;
+    bool accumulated = false;
+    int64_t launches = 0;
+    std::string last_error;
+};
+
+namespace {
+
+int fail(tl_ctx* ctx, int code, const std::string& msg) {
+    if (ctx != nullptr) ctx->last_error = msg;
+    return code;
+}
+
+int cuda_fail(tl_ctx* ctx, cudaError_t e, const char* what) {
+    std::string msg = std::string(what) + ": " + cudaGetErrorString(e);
+    return fail(ctx, TL_ECUDA, msg);
+}
+
+bool overlaps_any(const std::vector<Interval>& sorted, uintptr_t lo, uintptr_t hi) {
+    // sorted by lo and pairwise disjoint: only the last interval starting before hi can overlap
+    auto it = std::lower_bound(sorted.begin(), sorted.end(), hi,
+                               [](const Interval& a, uintptr_t v) { return a.lo < v; });
+    if (it == sorted.begin()) return false;
+    --it;
+    return it->hi > lo;
+}
+
+int check_config(const tl_config* c, std::string& why) {
+    if (c->param_dtype != TL_BF16 && c->param_dtype != TL_F16) { why = "param_dtype must be TL_BF16 or TL_F16"; return TL_EINVAL; }
+    if (c->grad_dtype != TL_BF16 && c->grad_dtype != TL_F16 && c->grad_dtype != TL_F32) { why = "grad_dtype must be TL_BF16, TL_F16 or TL_F32"; return TL_EINVAL; }
+    if (c->scaler_enabled != 0 && c->scaler_enabled != 1) { why = "scaler_enabled must be 0 or 1"; return TL_EINVAL; }
+    if (c->scaler_enabled) {
+        if (!is_pow2(c->init_scale)) { why = "init_scale must be a positive power of two"; return TL_EINVAL; }
+        if (!is_pow2(c->growth) || !(c->growth > 1.0f)) { why = "growth must be a power of two > 1"; return TL_EINVAL; }
+        if (!is_pow2(c->backoff) || !(c->backoff < 1.0f)) { why = "backoff must be a power of two < 1"; return TL_EINVAL; }
+        if (c->interval < 1) { why = "interval must be >= 1"; return TL_EINVAL; }
+        if (!is_pow2(c->min_scale) || !is_pow2(c->max_scale) || c->min_scale > c->max_scale) {
+            why = "min_scale and max_scale must be powers of two with min_scale <= max_scale"; return TL_EINVAL;
+        }
+        if (c->init_scale < c->min_scale || c->init_scale > c->max_scale) { why = "init_scale must lie in [min_scale, max_scale]"; return TL_EINVAL; }
+    }
+    return TL_OK;
+}
+
+int check_counts(tl_ctx* ctx, int64_t n_i, int64_t N) {
+    if (N <= 0 || N > (int64_t(1) << 53)) return fail(ctx, TL_EINVAL, "N must be in [1, 2^53]");
+    if (n_i <= 0 || n_i > N) return fail(ctx, TL_EINVAL, "n_i must be in [1, N]");
+    return TL_OK;
+}
+
+int check_device(tl_ctx* ctx) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDevice");
+    if (dev != ctx->device) return fail(ctx, TL_ESTATE, "the current CUDA device is not the context's device");
+    return TL_OK;
+}
+
+// Validate a gradient list against the context (sizes implied, alignment, no
+// overlap with anything the kernels write).
+int check_grads(tl_ctx* ctx, const void* const* grads) {
+    const int es = elem_size(ctx->cfg.grad_dtype);
+    for (int64_t i = 0; i < ctx->ntensors; ++i) {
+        if (ctx->numel[i] == 0) continue;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(grads[i]);
+        if (a == 0) return fail(ctx, TL_EINVAL, "NULL gradient pointer for tensor " + std::to_string(i));
+        if (a % es != 0) return fail(ctx, TL_EINVAL, "misaligned gradient pointer for tensor " + std::to_string(i));
+        if (overlaps_any(ctx->state_iv, a, a + uintptr_t(ctx->numel[i]) * es))
+            return fail(ctx, TL_EINVAL, "gradient tensor " + std::to_string(i) + " overlaps a state tensor");
+    }
+    return TL_OK;
+}
+
+// Resolve the gradient table for one call: by value when short, else a cached
+// device table (uploaded on first use of this exact pointer list).
+int resolve_grads(tl_ctx* ctx, const void* const* grads, cudaStream_t s, GradTable* inl,
+                  const void* const** dtab, GradSlot** used) {
+    *dtab = nullptr;
+    *used = nullptr;
+    if (ctx->ntensors <= kInlineGrads) {
+        int rc = check_grads(ctx, grads);
+        if (rc != TL_OK) return rc;
+        for (int64_t i = 0; i < ctx->ntensors; ++i) inl->p[i] = grads[i];
+        return TL_OK;
+    }
+    const uint64_t h = hash_ptrs(grads, ctx->ntensors);
+    ctx->clock += 1;
+    for (GradSlot& sl : ctx->slots) {
+        if (sl.valid && sl.hash == h && std::equal(sl.key.begin(), sl.key.end(), grads)) {
+            sl.stamp = ctx->clock;
+            *dtab = sl.d_tab;
+            *used = &sl;
+            return TL_OK;
+        }
+    }
+    int rc = check_grads(ctx, grads);
+    if (rc != TL_OK) return rc;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+        return fail(ctx, TL_ESTATE, "a new gradient list cannot be uploaded during stream capture; use it once before capturing");
+    GradSlot* victim = &ctx->slots[0];
+    for (GradSlot& sl : ctx->slots) {
+        if (!sl.valid) { victim = &sl; break; }
+        if (sl.stamp < victim->stamp) victim = &sl;
+    }
+    if (victim->valid && victim->last_use != nullptr) {
+        cudaError_t e = cudaEventSynchronize(victim->last_use);  // its previous users are done
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaEventSynchronize");
+    }
+    std::memcpy(victim->h_stage, grads, sizeof(void*) * size_t(ctx->ntensors));
+    cudaError_t e = cudaMemcpyAsync(victim->d_tab, victim->h_stage, sizeof(void*) * size_t(ctx->ntensors),
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemcpyAsync(gradient table)");
+    victim->key.assign(grads, grads + ctx->ntensors);
+    victim->hash = h;
+    victim->stamp = ctx->clock;
+    victim->valid = true;
+    *dtab = victim->d_tab;
+    *used = victim;
+    return TL_OK;
+}
+
+void mark_used(GradSlot* sl, cudaStream_t s) {
+    if (sl == nullptr || sl->last_use == nullptr) return;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone)
+        cudaEventRecord(sl->last_use, s);
+}
+
+int grid_for(tl_ctx* ctx, int per_sm) {
+    int64_t g = int64_t(ctx->sm_count) * per_sm;
+    if (g > ctx->nchunks) g = ctx->nchunks;
+    if (g < 1) g = 1;
+    return int(g);
+}
+
+void free_ctx(tl_ctx* ctx) {
+    if (ctx == nullptr) return;
+    cudaFree(ctx->d_chunks);
+    cudaFree(ctx->d_tp);
+    cudaFree(ctx->d_partials);
+    cudaFree(ctx->d_state);
+    for (GradSlot& sl : ctx->slots) {
+        cudaFree(sl.d_tab);
+        cudaFreeHost(sl.h_stage);
+        if (sl.last_use != nullptr) cudaEventDestroy(sl.last_use);
+    }
+    delete ctx;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tl_status_string(int status) {
+    switch (status) {
+        case TL_OK: return "ok";
+        case TL_EINVAL: return "invalid argument";
+        case TL_ECUDA: return "CUDA error";
+        case TL_ESTATE: return "call not allowed in the current state";
+        case TL_ENOMEM: return "out of memory";
+        default: return "unknown status";
+    }
+}
+
+const char* tl_last_error(const tl_ctx* ctx) {
+    return ctx == nullptr ? "" : ctx->last_error.c_str();
+}
+
+int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const* param, float* const* master,
+              float* const* m, float* const* v, float* const* acc, const tl_config* cfg, tl_stream stream) {
+    if (out == nullptr || cfg == nullptr) return TL_EINVAL;
+    *out = nullptr;
+    if (ntensors < 0 || ntensors > (int64_t(1) << 31) - 1) return TL_EINVAL;
+    if (ntensors > 0 && (numel == nullptr || param == nullptr || master == nullptr || m == nullptr ||
+                         v == nullptr || acc == nullptr))
+        return TL_EINVAL;
+    std::string why;
+    if (check_config(cfg, why) != TL_OK) return TL_EINVAL;
+    const int pes = elem_size(cfg->param_dtype);
+
+    // Sizes, pointers, alignment and overlap: everything before any allocation.
+    std::vector<Interval> iv;
+    iv.reserve(size_t(ntensors) * 5);
+    int64_t P = 0, nchunks = 0;
+    for (int64_t i = 0; i < ntensors; ++i) {
+        if (numel[i] < 0) return TL_EINVAL;
+        if (numel[i] == 0) continue;
+        if (numel[i] > (int64_t(1) << 62) / 4 - P) return TL_EINVAL;
+        P += numel[i];
+        nchunks += (numel[i] + kChunk - 1) / kChunk;
+        const void* ptrs[5] = {param[i], master[i], m[i], v[i], acc[i]};
+        for (int l = 0; l < 5; ++l) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(ptrs[l]);
+            const int es = l == 0 ? pes : 4;
+            if (a == 0 || a % es != 0) return TL_EINVAL;
+            iv.push_back({a, a + uintptr_t(numel[i]) * es});
+        }
+    }
+    std::sort(iv.begin(), iv.end(), [](const Interval& a, const Interval& b) { return a.lo < b.lo; });
+    for (size_t k = 1; k < iv.size(); ++k)
+        if (iv[k].lo < iv[k - 1].hi) return TL_EINVAL;  // two tensors share memory
+
+    tl_ctx* ctx = new (std::nothrow) tl_ctx();
+    if (ctx == nullptr) return TL_ENOMEM;
+    ctx->cfg = *cfg;
+    ctx->ntensors = ntensors;
+    ctx->P = P;
+    ctx->nchunks = nchunks;
+    ctx->numel.assign(numel, numel + ntensors);
+    ctx->state_iv = std::move(iv);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    cudaError_t e = cudaGetDevice(&ctx->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
+    if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
+
+    // Chunk table and per-tensor pointers.
+    std::vector<Chunk> chunks;
+    chunks.reserve(size_t(nchunks));
+    std::vector<TensorPtrs> tp(size_t(std::max<int64_t>(ntensors, 1)));
+    for (int64_t i = 0; i < ntensors; ++i) {
+        tp[i] = TensorPtrs{master[i], m[i], v[i], acc[i], param[i], numel[i]};
+        for (int64_t st = 0; st < numel[i]; st += kChunk)
+            chunks.push_back(Chunk{int32_t(i), int32_t(std::min<int64_t>(kChunk, numel[i] - st)), st});
+    }
+    const size_t nc_alloc = size_t(std::max<int64_t>(nchunks, 1));
+    if (cudaMalloc(&ctx->d_chunks, sizeof(Chunk) * nc_alloc) != cudaSuccess ||
+        cudaMalloc(&ctx->d_tp, sizeof(TensorPtrs) * tp.size()) != cudaSuccess ||
+        cudaMalloc(&ctx->d_partials, sizeof(double) * nc_alloc) != cudaSuccess ||
+        cudaMalloc(&ctx->d_state, sizeof(DevState)) != cudaSuccess) {
+        cudaGetLastError();
+        free_ctx(ctx);
+        return TL_ENOMEM;
+    }
+    if (ntensors > kInlineGrads) {
+        for (GradSlot& sl : ctx->slots) {
+            if (cudaMalloc(reinterpret_cast<void**>(&sl.d_tab), sizeof(void*) * size_t(ntensors)) != cudaSuccess ||
+                cudaMallocHost(reinterpret_cast<void**>(&sl.h_stage), sizeof(void*) * size_t(ntensors)) != cudaSuccess ||
+                cudaEventCreateWithFlags(&sl.last_use, cudaEventDisableTiming) != cudaSuccess) {
+                cudaGetLastError();
+                free_ctx(ctx);
+                return TL_ENOMEM;
+            }
+        }
+    }
+    DevState ds{};
+    ds.S = cfg->scaler_enabled ? cfg->init_scale : 1.0f;
+    ds.count = 0;
+    ds.t = 0;
+    ds.b1p = 1.0;
+    ds.b2p = 1.0;
+    ds.found_inf = 0;
+    ds.skipped = 0;
+    ds.norm = 0.0f;
+    ds.coef = 1.0f;
+    ds.sumsq = 0.0;
+    ds.b1p_next = 1.0;
+    ds.b2p_next = 1.0;
+    e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && nchunks > 0)
+        e = cudaMemcpyAsync(ctx->d_chunks, chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && ntensors > 0)
+        e = cudaMemcpyAsync(ctx->d_tp, tp.data(), sizeof(TensorPtrs) * size_t(ntensors), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
+
+    // Persistent grid sizes from the occupancy of each kernel variant.
+    for (int dt = 0; dt < 3; ++dt) {
+        for (int f = 0; f < 2; ++f) ctx->grid_acc[dt][f] = grid_for(ctx, blocks_per_sm(0, dt, f));
+        for (int md = 0; md < 3; ++md) ctx->grid_uns[dt][md] = grid_for(ctx, blocks_per_sm(1, dt, md));
+        ctx->grid_adam[dt] = dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(2, dt, 0));
+    }
+    *out = ctx;
+    return TL_OK;
+}
+
+int tl_destroy(tl_ctx* ctx) {
+    if (ctx == nullptr) return TL_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    free_ctx(ctx);
+    return e == cudaSuccess ? TL_OK : TL_ECUDA;
+}
+
+int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N, int first, tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (grads == nullptr && ctx->ntensors > 0) return fail(ctx, TL_EINVAL, "grads must not be NULL");
+    if (first != 0 && first != 1) return fail(ctx, TL_EINVAL, "first must be 0 or 1");
+    int rc = check_counts(ctx, n_i, N);
+    if (rc != TL_OK) return rc;
+    if (first) {
+        if (ctx->phase != kIdle && ctx->phase != kAccum)
+            return fail(ctx, TL_ESTATE, "an update is past its accumulation phase; finish it with tl_scaler_update");
+    } else {
+        if (ctx->phase != kAccum) return fail(ctx, TL_ESTATE, "first=0 with no update open");
+        if (N != ctx->N_update) return fail(ctx, TL_EINVAL, "N differs from the N of the open update");
+        if (n_i > N - ctx->n_sum) return fail(ctx, TL_EINVAL, "the counts exceed N");
+    }
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    static thread_local GradTable inl;
+    const void* const* dtab = nullptr;
+    GradSlot* used = nullptr;
+    if (ctx->ntensors > 0 && (rc = resolve_grads(ctx, grads, s, &inl, &dtab, &used)) != TL_OK) return rc;
+    const float w = static_cast<float>(static_cast<double>(n_i) / static_cast<double>(N));
+    if (ctx->nchunks > 0) {
+        cudaError_t e = launch_accumulate(ctx->cfg.grad_dtype, first != 0, ctx->d_chunks, ctx->nchunks, ctx->d_tp,
+                                          inl, dtab, w, ctx->grid_acc[ctx->cfg.grad_dtype][first], s);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "accumulate launch");
+        ctx->launches += 1;
+        mark_used(used, s);
+    }
+    if (first) {
+        ctx->N_update = N;
+        ctx->n_sum = 0;
+    }
+    ctx->n_sum += n_i;
+    ctx->accumulated = true;
+    ctx->phase = kAccum;
+    return TL_OK;
+}
+
+int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t N, tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    int mode;
+    int rc;
+    if (grads == nullptr) {
+        if (ctx->phase != kAccum) return fail(ctx, TL_ESTATE, "no accumulated micro-batch to unscale");
+        if (ctx->n_sum != ctx->N_update) return fail(ctx, TL_EINVAL, "the accumulated counts do not add up to N");
+        mode = kAccOnly;
+    } else {
+        if ((rc = check_counts(ctx, n_k, N)) != TL_OK) return rc;
+        if (ctx->phase == kIdle) {
+            if (n_k != N) return fail(ctx, TL_EINVAL, "the only micro-batch must have n_k == N");
+            mode = kFirstOnly;
+        } else if (ctx->phase == kAccum) {
+            if (N != ctx->N_update) return fail(ctx, TL_EINVAL, "N differs from the N of the open update");
+            if (ctx->n_sum + n_k != N) return fail(ctx, TL_EINVAL, "the counts do not add up to N");
+            mode = kAccAndGrad;
+        } else {
+            return fail(ctx, TL_ESTATE, "tl_unscale_check called twice in one update");
+        }
+    }
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    static thread_local GradTable inl;
+    const void* const* dtab = nullptr;
+    GradSlot* used = nullptr;
+    if (grads != nullptr && ctx->ntensors > 0 && (rc = resolve_grads(ctx, grads, s, &inl, &dtab, &used)) != TL_OK)
+        return rc;
+    const float w = grads == nullptr ? 1.0f : static_cast<float>(static_cast<double>(n_k) / static_cast<double>(N));
+    if (ctx->nchunks > 0) {
+        cudaError_t e = launch_unscale(ctx->cfg.grad_dtype, mode, ctx->d_chunks, ctx->nchunks, ctx->d_tp, inl, dtab, w,
+                                       ctx->d_state, ctx->d_partials, ctx->grid_uns[ctx->cfg.grad_dtype][mode], s);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "unscale launch");
+        ctx->launches += 1;
+        mark_used(used, s);
+    }
+    if (grads != nullptr) {
+        if (ctx->phase == kIdle) ctx->N_update = N;
+        ctx->n_sum = ctx->phase == kIdle ? n_k : ctx->n_sum + n_k;
+    }
+    ctx->phase = kUnscaled;
+    return TL_OK;
+}
+
+int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (ctx->phase != kUnscaled) return fail(ctx, TL_ESTATE, "tl_grad_norm must follow tl_unscale_check");
+    if (std::isnan(max_norm)) return fail(ctx, TL_EINVAL, "max_norm is NaN");
+    int rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaError_t e = launch_norm(ctx->d_partials, ctx->nchunks, ctx->d_state, max_norm, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "norm launch");
+    ctx->launches += 1;
+    ctx->phase = kNormed;
+    return TL_OK;
+}
+
+int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
+    if (ctx == nullptr || hp == nullptr) return TL_EINVAL;
+    if (ctx->phase != kNormed) return fail(ctx, TL_ESTATE, "tl_clip_adamw_step must follow tl_grad_norm");
+    if (!(hp->lr >= 0.0f) || !std::isfinite(hp->lr) || !(hp->beta1 >= 0.5f && hp->beta1 < 1.0f) ||
+        !(hp->beta2 >= 0.5f && hp->beta2 < 1.0f) || !(hp->eps > 0.0f) || !std::isfinite(hp->eps) ||
+        !(hp->weight_decay >= 0.0f) || !std::isfinite(hp->weight_decay))
+        return fail(ctx, TL_EINVAL, "AdamW hyper-parameters out of range");
+    int rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    AdamHP h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+    // Launched even with no elements: its first CTA also computes the beta
+    // powers the scaler kernel commits.
+    cudaError_t e = launch_adamw(ctx->cfg.param_dtype, ctx->d_chunks, ctx->nchunks, ctx->d_tp, ctx->d_state, h,
+                                 ctx->grid_adam[ctx->cfg.param_dtype], static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "adamw launch");
+    ctx->launches += 1;
+    ctx->phase = kStepped;
+    return TL_OK;
+}
+
+int tl_scaler_update(tl_ctx* ctx, tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (ctx->phase != kStepped) return fail(ctx, TL_ESTATE, "tl_scaler_update must follow tl_clip_adamw_step");
+    int rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    ScalerParams sp{ctx->cfg.scaler_enabled, ctx->cfg.growth, ctx->cfg.backoff, ctx->cfg.interval,
+                    ctx->cfg.min_scale, ctx->cfg.max_scale};
+    cudaError_t e = launch_scaler(ctx->d_state, sp, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "scaler launch");
+    ctx->launches += 1;
+    ctx->phase = kIdle;
+    ctx->n_sum = 0;
+    ctx->N_update = 0;
+    ctx->accumulated = false;
+    return TL_OK;
+}
+
+static int read_dev_state(tl_ctx* ctx, DevState* ds, cudaStream_t s) {
+    int rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaError_t e = cudaMemcpyAsync(ds, ctx->d_state, sizeof(DevState), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "reading the device scalars");
+    return TL_OK;
+}
+
+int tl_read_status(tl_ctx* ctx, tl_status* out, tl_stream stream) {
+    if (ctx == nullptr || out == nullptr) return TL_EINVAL;
+    DevState ds;
+    int rc = read_dev_state(ctx, &ds, static_cast<cudaStream_t>(stream));
+    if (rc != TL_OK) return rc;
+    out->S = ds.S;
+    out->count = ds.count;
+    out->t = ds.t;
+    out->skipped = ds.skipped;
+    out->found_inf = ds.found_inf;
+    out->norm = ds.norm;
+    out->coef = ds.coef;
+    out->sumsq = ds.sumsq;
+    out->b1p = ds.b1p;
+    out->b2p = ds.b2p;
+    return TL_OK;
+}
+
+int tl_get_state(tl_ctx* ctx, tl_state* out, tl_stream stream) {
+    if (ctx == nullptr || out == nullptr) return TL_EINVAL;
+    DevState ds;
+    int rc = read_dev_state(ctx, &ds, static_cast<cudaStream_t>(stream));
+    if (rc != TL_OK) return rc;
+    out->S = ds.S;
+    out->count = ds.count;
+    out->t = ds.t;
+    out->b1p = ds.b1p;
+    out->b2p = ds.b2p;
+    return TL_OK;
+}
+
+int tl_set_state(tl_ctx* ctx, const tl_state* in, tl_stream stream) {
+    if (ctx == nullptr || in == nullptr) return TL_EINVAL;
+    if (ctx->phase != kIdle) return fail(ctx, TL_ESTATE, "tl_set_state is allowed only between updates");
+    const tl_config& c = ctx->cfg;
+    if (c.scaler_enabled) {
+        if (!is_pow2(in->S) || in->S < c.min_scale || in->S > c.max_scale)
+            return fail(ctx, TL_EINVAL, "S must be a power of two in [min_scale, max_scale]");
+        if (in->count < 0 || in->count >= c.interval) return fail(ctx, TL_EINVAL, "count must be in [0, interval)");
+    } else {
+        if (in->S != 1.0f || in->count != 0) return fail(ctx, TL_EINVAL, "with the scaler disabled S must be 1 and count 0");
+    }
+    if (in->t < 0) return fail(ctx, TL_EINVAL, "t must be >= 0");
+    if (!(in->b1p > 0.0 && in->b1p <= 1.0) || !(in->b2p > 0.0 && in->b2p <= 1.0))
+        return fail(ctx, TL_EINVAL, "beta powers must lie in (0, 1]");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DevState ds;
+    int rc = read_dev_state(ctx, &ds, s);
+    if (rc != TL_OK) return rc;
+    ds.S = in->S;
+    ds.count = in->count;
+    ds.t = in->t;
+    ds.b1p = in->b1p;
+    ds.b2p = in->b2p;
+    ds.found_inf = 0;
+    cudaError_t e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(DevState), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "writing the device scalars");
+    return TL_OK;
+}
+
+const float* tl_scale_ptr(const tl_ctx* ctx) {
+    return ctx == nullptr ? nullptr : &ctx->d_state->S;
+}
+
+int64_t tl_num_params(const tl_ctx* ctx) { return ctx == nullptr ? 0 : ctx->P; }
+int64_t tl_num_chunks(const tl_ctx* ctx) { return ctx == nullptr ? 0 : ctx->nchunks; }
+int64_t tl_launch_count(const tl_ctx* ctx) { return ctx == nullptr ? 0 : ctx->launches; }
+
+}  // extern "C"

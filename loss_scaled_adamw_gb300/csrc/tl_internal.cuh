@@ -1,0 +1,101 @@
+// tl_internal.cuh - types shared by the kernels (tl_kernels.cu) and the host
+// C ABI (tl_api.cu) of the GB300 loss-scaled AdamW library.  Not installed;
+// the public interface is include/tl.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tl {
+
+// Work decomposition (multi-tensor apply).  Every tensor is cut into chunks of
+// at most kChunk elements; a chunk never spans two tensors, so a chunk has one
+// base pointer per list.  CTAs of a persistent grid walk the chunk table with
+// a fixed stride, and every chunk writes its own squared-norm partial, so the
+// reduction order (and the norm) does not depend on the grid size.
+constexpr int kChunk = 16384;
+constexpr int kThreads = 256;        // streaming kernels: 8 warps per CTA
+constexpr int kNormThreads = 1024;   // the single-CTA second-stage reduce
+constexpr int kInlineGrads = 512;    // gradient pointer tables up to this size travel in the kernel parameters
+
+// Element types (values of TL_F32 / TL_BF16 / TL_F16 in include/tl.h).
+constexpr int kF32 = 0;
+constexpr int kBF16 = 1;
+constexpr int kF16 = 2;
+
+// Per-tensor base pointers of the state lists (48 bytes).
+struct TensorPtrs {
+    float* master;
+    float* m;
+    float* v;
+    float* acc;
+    void* param;
+    int64_t numel;
+};
+
+// One work chunk: elements [start, start + len) of tensor `tensor` (16 bytes).
+struct Chunk {
+    int32_t tensor;
+    int32_t len;
+    int64_t start;
+};
+
+// Device-resident scalars of one context.
+struct DevState {
+    float S;              // loss scale
+    int32_t count;        // good steps since the last overflow or growth
+    int64_t t;            // committed optimizer steps
+    double b1p, b2p;      // beta1^t, beta2^t
+    int32_t found_inf;    // overflow flag of the update in flight
+    int32_t skipped;      // 1 if the last finished update was skipped
+    float norm;           // global L2 norm of the unscaled gradient
+    float coef;           // clip coefficient
+    double sumsq;         // squared norm (fp64)
+    double b1p_next;      // beta powers of the update in flight (committed by the scaler kernel)
+    double b2p_next;
+};
+
+// Gradient pointers passed by value (kernel parameter space).
+struct GradTable {
+    const void* p[kInlineGrads];
+};
+
+struct ScalerParams {
+    int32_t enabled;
+    float growth;
+    float backoff;
+    int32_t interval;
+    float min_scale;
+    float max_scale;
+};
+
+struct AdamHP {
+    float lr, beta1, beta2, eps, wd;
+};
+
+// What the a3 kernel reads besides the accumulation buffer.
+enum UnscaleMode : int {
+    kAccOnly = 0,   // u = acc / S
+    kFirstOnly = 1, // u = (w * g) / S: the only micro-batch
+    kAccAndGrad = 2 // u = fma(w, g, acc) / S: the last of several micro-batches
+};
+
+// Launchers (tl_kernels.cu).  `grid` is the persistent grid size; a gtab of
+// nullptr means the pointers are in `inl`.
+cudaError_t launch_accumulate(int gdt, bool first, const Chunk* chunks, int64_t nchunks,
+                              const TensorPtrs* tp, const GradTable& inl, const void* const* gtab,
+                              float w, int grid, cudaStream_t s);
+cudaError_t launch_unscale(int gdt, int mode, const Chunk* chunks, int64_t nchunks,
+                           const TensorPtrs* tp, const GradTable& inl, const void* const* gtab,
+                           float w, DevState* st, double* partials, int grid, cudaStream_t s);
+cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm,
+                        cudaStream_t s);
+cudaError_t launch_adamw(int pdt, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp,
+                         DevState* st, AdamHP hp, int grid, cudaStream_t s);
+cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);
+
+// Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
+// kind: 0 accumulate, 1 unscale, 2 adamw.
+int blocks_per_sm(int kind, int dt, int variant);
+
+}  // namespace tl

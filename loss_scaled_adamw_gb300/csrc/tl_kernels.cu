@@ -1,0 +1,573 @@
+// tl_kernels.cu - sm_103a kernels of the loss-scaled AdamW optimizer step.
+//
+// The step is bound by HBM bandwidth (well under one flop per byte), so the
+// kernels are streaming kernels, not tensor-core kernels: a persistent grid
+// walks a device-resident chunk table (multi-tensor apply), each thread moves
+// 8 elements per access with 128-bit loads and stores and keeps several such
+// vectors in flight, and a chunk whose pointers are not 16-byte aligned, or
+// the tail of a tensor, takes a coalesced scalar path.
+//
+// Floating point.  Every element-wise operation is written as an explicit
+// round-to-nearest intrinsic (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn,
+// __fsqrt_rn, __fmaf_rn and the fp64 forms), and this file is compiled with
+// -fmad=false, so nothing is contracted or reassociated: each output element is
+// the correctly rounded result of one declared sequence of operations.
+//
+// Pages cited (by title):
+//   [MP]  "Mixed precision, loss scaling, gradient accumulation, and activation
+//         checkpointing" (tinyllm module L11.1)
+//   [MEG] "Megatron Internals III: Mixed Precision, Loss Scaling, and Grad Clipping"
+//   [ZRO] "Your weights fit on one device but Adam's moments do not - how do you
+//         shard the optimizer state?"
+//   [RST] "Practical LLM in Rust", ch. 13 "Accumulate gradients and recompute activations"
+#include "tl_internal.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace tl {
+namespace {
+
+constexpr int kVec = 8;     // elements per vector access (16 B of a 16-bit stream)
+constexpr int kUnroll = 4;  // vectors in flight per thread in the accumulate/unscale kernels
+constexpr int kUnrollAdam = 2;
+
+// ---------------------------------------------------------------------------
+// 8-element vector access
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void ld8_f32(const float* __restrict__ p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void st8_f32(float* __restrict__ p, const float (&x)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+__device__ __forceinline__ void unpack_bf16x2(uint32_t r, float& lo, float& hi) {
+    lo = __uint_as_float(r << 16);          // bf16 -> fp32 is exact: the upper half of the word
+    hi = __uint_as_float(r & 0xffff0000u);
+}
+
+__device__ __forceinline__ void unpack_f16x2(uint32_t r, float& lo, float& hi) {
+    __half2 h;
+    *reinterpret_cast<uint32_t*>(&h) = r;
+    const float2 f = __half22float2(h);     // fp16 -> fp32 is exact
+    lo = f.x;
+    hi = f.y;
+}
+
+// Micro-batch gradient streams: read once per kernel, through the read-only path.
+template <int DT> struct Grad;
+
+template <> struct Grad<kBF16> {
+    static constexpr int kBytes = 2;
+    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8]) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
+        unpack_bf16x2(r.x, x[0], x[1]); unpack_bf16x2(r.y, x[2], x[3]);
+        unpack_bf16x2(r.z, x[4], x[5]); unpack_bf16x2(r.w, x[6], x[7]);
+    }
+    __device__ static __forceinline__ float ld1(const void* base, int64_t i) {
+        return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(base) + i)) << 16);
+    }
+};
+
+template <> struct Grad<kF16> {
+    static constexpr int kBytes = 2;
+    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8]) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
+        unpack_f16x2(r.x, x[0], x[1]); unpack_f16x2(r.y, x[2], x[3]);
+        unpack_f16x2(r.z, x[4], x[5]); unpack_f16x2(r.w, x[6], x[7]);
+    }
+    __device__ static __forceinline__ float ld1(const void* base, int64_t i) {
+        const unsigned short b = __ldg(static_cast<const unsigned short*>(base) + i);
+        return __half2float(__ushort_as_half(b));
+    }
+};
+
+template <> struct Grad<kF32> {
+    static constexpr int kBytes = 4;
+    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8]) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+    __device__ static __forceinline__ float ld1(const void* base, int64_t i) {
+        return __ldg(static_cast<const float*>(base) + i);
+    }
+};
+
+// Model-precision parameter stores: round to nearest even ([MP] section 2, rd16).
+template <int DT> struct Param;
+
+template <> struct Param<kBF16> {
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&b);
+    }
+    __device__ static __forceinline__ void st1(void* base, int64_t i, float x) {
+        static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+    }
+};
+
+template <> struct Param<kF16> {
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    __device__ static __forceinline__ void st1(void* base, int64_t i, float x) {
+        static_cast<__half*>(base)[i] = __float2half_rn(x);
+    }
+};
+
+template <int DT>
+__device__ __forceinline__ void st8_param(void* base, int64_t i, const float (&x)[8]) {
+    uint4 r;
+    r.x = Param<DT>::pack2(x[0], x[1]);
+    r.y = Param<DT>::pack2(x[2], x[3]);
+    r.z = Param<DT>::pack2(x[4], x[5]);
+    r.w = Param<DT>::pack2(x[6], x[7]);
+    *reinterpret_cast<uint4*>(static_cast<unsigned short*>(base) + i) = r;
+}
+
+__device__ __forceinline__ bool aligned16(const void* p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// ---------------------------------------------------------------------------
+// a2: accumulate micro-batch i.  [RST] ch. 13 "Weight each mean by the targets
+// it represents"; [MP] section 2 "Gradient accumulation" (no zeroing between
+// micro-batches).  acc = w*g (first) or fma(w, g, acc).
+// ---------------------------------------------------------------------------
+template <int GDT, bool FIRST>
+__global__ void __launch_bounds__(kThreads)
+k_accumulate(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
+             const __grid_constant__ GradTable inl, const void* const* __restrict__ gtab, float w) {
+    const void* const* gp = gtab != nullptr ? gtab : inl.p;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
+        const void* g = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
+        const int len = ch.len;
+        int done = 0;
+        if (aligned16(acc) && aligned16(g)) {
+            const int nv = len / kVec;
+            int i = threadIdx.x;
+            for (; i + (kUnroll - 1) * kThreads < nv; i += kUnroll * kThreads) {
+                float gx[kUnroll][8], ax[kUnroll][8];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * kThreads) * kVec, gx[u]);
+                if (!FIRST) {
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        ax[u][e] = FIRST ? __fmul_rn(w, gx[u][e]) : __fmaf_rn(w, gx[u][e], ax[u][e]);
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+            }
+            for (; i < nv; i += kThreads) {
+                float gx[8], ax[8];
+                Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
+                if (!FIRST) ld8_f32(acc + i * kVec, ax);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ax[e] = FIRST ? __fmul_rn(w, gx[e]) : __fmaf_rn(w, gx[e], ax[e]);
+                st8_f32(acc + i * kVec, ax);
+            }
+            done = nv * kVec;
+        }
+        for (int j = done + threadIdx.x; j < len; j += kThreads) {
+            const float gj = Grad<GDT>::ld1(g, j);
+            acc[j] = FIRST ? __fmul_rn(w, gj) : __fmaf_rn(w, gj, acc[j]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a3: last micro-batch + unscale + overflow check + squared-norm partial.
+// [MEG] section 8 (cast, divide by the loss scale, place in the fp32 buffer),
+// section 6 (overflow flag), section 9 (sum of squares); [MP] section 2 "Loss
+// scaling" (S a power of two: exact).  Squares are fp32 products summed in
+// fp32 over 8 elements, then in fp64 per thread; a group whose fp32 sum
+// overflowed is re-summed in fp64, so the squared norm is infinite exactly
+// when some fp32 square is.  One fp64 partial per chunk, no atomics.
+// ---------------------------------------------------------------------------
+template <int MODE>
+__device__ __forceinline__ float unscale1(float a, float gj, float w, float inv_s) {
+    if (MODE == kAccOnly) return __fmul_rn(a, inv_s);
+    if (MODE == kFirstOnly) return __fmul_rn(__fmul_rn(w, gj), inv_s);
+    return __fmul_rn(__fmaf_rn(w, gj, a), inv_s);
+}
+
+__device__ __forceinline__ double sumsq8(const float (&u)[8]) {
+    float q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = __fmul_rn(u[e], u[e]);
+    const float s = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                              __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+    if (!isinf(s)) return static_cast<double>(s);
+    double d = 0.0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) d = __dadd_rn(d, static_cast<double>(q[e]));
+    return d;
+}
+
+template <int GDT, int MODE>
+__global__ void __launch_bounds__(kThreads)
+k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
+          const __grid_constant__ GradTable inl, const void* const* __restrict__ gtab, float w,
+          DevState* __restrict__ st, double* __restrict__ partials) {
+    __shared__ double red[kThreads / 32];
+    const void* const* gp = gtab != nullptr ? gtab : inl.p;
+    const float inv_s = __fdiv_rn(1.0f, st->S);
+    constexpr bool kReadG = MODE != kAccOnly;
+    constexpr bool kReadAcc = MODE != kFirstOnly;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
+        const void* g = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
+        const int len = ch.len;
+        double tsum = 0.0;
+        bool bad = false;
+        int done = 0;
+        if (aligned16(acc) && (!kReadG || aligned16(g))) {
+            const int nv = len / kVec;
+            int i = threadIdx.x;
+            for (; i + (kUnroll - 1) * kThreads < nv; i += kUnroll * kThreads) {
+                float gx[kUnroll][8], ax[kUnroll][8];
+                if (kReadG) {
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * kThreads) * kVec, gx[u]);
+                }
+                if (kReadAcc) {
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        ax[u][e] = unscale1<MODE>(kReadAcc ? ax[u][e] : 0.0f, kReadG ? gx[u][e] : 0.0f, w, inv_s);
+                        bad |= !isfinite(ax[u][e]);
+                    }
+                    tsum = __dadd_rn(tsum, sumsq8(ax[u]));
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+            }
+            for (; i < nv; i += kThreads) {
+                float gx[8], ax[8];
+                if (kReadG) Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
+                if (kReadAcc) ld8_f32(acc + i * kVec, ax);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    ax[e] = unscale1<MODE>(kReadAcc ? ax[e] : 0.0f, kReadG ? gx[e] : 0.0f, w, inv_s);
+                    bad |= !isfinite(ax[e]);
+                }
+                tsum = __dadd_rn(tsum, sumsq8(ax));
+                st8_f32(acc + i * kVec, ax);
+            }
+            done = nv * kVec;
+        }
+        for (int j = done + threadIdx.x; j < len; j += kThreads) {
+            const float u = unscale1<MODE>(kReadAcc ? acc[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g, j) : 0.0f, w, inv_s);
+            acc[j] = u;
+            bad |= !isfinite(u);
+            tsum = __dadd_rn(tsum, static_cast<double>(__fmul_rn(u, u)));
+        }
+        // Fixed-order block reduction: butterfly within each warp, then warp 0's
+        // sums added in warp order by thread 0.
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tsum = __dadd_rn(tsum, __shfl_xor_sync(0xffffffffu, tsum, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = tsum;
+        const int any_bad = __syncthreads_or(bad);
+        if (threadIdx.x == 0) {
+            double s = 0.0;
+#pragma unroll
+            for (int k = 0; k < kThreads / 32; ++k) s = __dadd_rn(s, red[k]);
+            partials[c] = s;
+            if (any_bad) st->found_inf = 1;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a4: deterministic second stage.  [MEG] section 9: global_norm =
+// sqrt(sum ||g||^2), clip_coef = max_norm / (global_norm + eps), applied only
+// below 1 (eps = 1e-6).  One CTA: thread t adds partials t, t+1024, ... in
+// order, then a fixed butterfly and a fixed warp-order sum.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kNormThreads)
+k_norm(const double* __restrict__ partials, int64_t n, DevState* __restrict__ st, float max_norm) {
+    __shared__ double red[kNormThreads / 32];
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < n; i += kNormThreads) s = __dadd_rn(s, partials[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        double v = red[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (threadIdx.x == 0) {
+            st->sumsq = v;
+            if (!isfinite(v)) st->found_inf = 1;   // an fp32 square overflowed: treated as an overflow
+            const float norm = __double2float_rn(__dsqrt_rn(v));
+            st->norm = norm;
+            float coef = 1.0f;
+            if (max_norm > 0.0f) {
+                const float cc = __fdiv_rn(max_norm, __fadd_rn(norm, 1e-6f));
+                if (cc < 1.0f) coef = cc;
+            }
+            st->coef = coef;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a5: clip + AdamW + recast.  [MEG] sections 7 and 9; [ZRO] "Why the optimizer
+// state is the thing that overflows" (bias-corrected moments, eps outside the
+// root); [RST] ch. 13 (decoupled weight decay, beta powers as state); [MP]
+// section 2 "Why the weights stay float32" (only the model copy is rounded).
+// A set overflow flag makes every CTA return before touching memory.
+// ---------------------------------------------------------------------------
+struct AdamConsts {
+    float step, bc2s, lrwd, b1, omb1, b2, omb2, eps, coef;
+};
+
+__device__ __forceinline__ void adamw1(float u, float& w, float& m, float& v, const AdamConsts& k) {
+    const float g = __fmul_rn(u, k.coef);
+    m = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.omb1, g));
+    v = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.omb2, __fmul_rn(g, g)));
+    const float wd = __fsub_rn(w, __fmul_rn(k.lrwd, w));
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), k.bc2s), k.eps);
+    w = __fsub_rn(wd, __fmul_rn(k.step, __fdiv_rn(m, denom)));
+}
+
+template <int PDT>
+__global__ void __launch_bounds__(kThreads)
+k_adamw(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
+        DevState* __restrict__ st, AdamHP hp) {
+    __shared__ AdamConsts sk;
+    __shared__ int skip;
+    if (threadIdx.x == 0) {
+        const int f = st->found_inf;
+        skip = f;
+        const double b1n = __dmul_rn(st->b1p, static_cast<double>(hp.beta1));
+        const double b2n = __dmul_rn(st->b2p, static_cast<double>(hp.beta2));
+        AdamConsts k;
+        k.step = __double2float_rn(__ddiv_rn(static_cast<double>(hp.lr), __dadd_rn(1.0, -b1n)));
+        k.bc2s = __double2float_rn(__dsqrt_rn(__dadd_rn(1.0, -b2n)));
+        k.lrwd = __double2float_rn(__dmul_rn(static_cast<double>(hp.lr), static_cast<double>(hp.wd)));
+        k.b1 = hp.beta1;
+        k.omb1 = __fsub_rn(1.0f, hp.beta1);
+        k.b2 = hp.beta2;
+        k.omb2 = __fsub_rn(1.0f, hp.beta2);
+        k.eps = hp.eps;
+        k.coef = st->coef;
+        sk = k;
+        if (blockIdx.x == 0 && !f) {
+            st->b1p_next = b1n;
+            st->b2p_next = b2n;
+        }
+    }
+    __syncthreads();
+    if (skip) return;
+    const AdamConsts k = sk;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        const TensorPtrs t = tp[ch.tensor];
+        const float* __restrict__ u = t.acc + ch.start;
+        float* __restrict__ w = t.master + ch.start;
+        float* __restrict__ m = t.m + ch.start;
+        float* __restrict__ v = t.v + ch.start;
+        void* p = static_cast<unsigned short*>(t.param) + ch.start;
+        const int len = ch.len;
+        int done = 0;
+        if (aligned16(u) && aligned16(w) && aligned16(m) && aligned16(v) && aligned16(p)) {
+            const int nv = len / kVec;
+            int i = threadIdx.x;
+            for (; i + (kUnrollAdam - 1) * kThreads < nv; i += kUnrollAdam * kThreads) {
+                float ux[kUnrollAdam][8], wx[kUnrollAdam][8], mx[kUnrollAdam][8], vx[kUnrollAdam][8];
+#pragma unroll
+                for (int q = 0; q < kUnrollAdam; ++q) {
+                    const int o = (i + q * kThreads) * kVec;
+                    ld8_f32(u + o, ux[q]);
+                    ld8_f32(w + o, wx[q]);
+                    ld8_f32(m + o, mx[q]);
+                    ld8_f32(v + o, vx[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < kUnrollAdam; ++q) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) adamw1(ux[q][e], wx[q][e], mx[q][e], vx[q][e], k);
+                    const int o = (i + q * kThreads) * kVec;
+                    st8_f32(w + o, wx[q]);
+                    st8_f32(m + o, mx[q]);
+                    st8_f32(v + o, vx[q]);
+                    st8_param<PDT>(p, o, wx[q]);
+                }
+            }
+            for (; i < nv; i += kThreads) {
+                float ux[8], wx[8], mx[8], vx[8];
+                const int o = i * kVec;
+                ld8_f32(u + o, ux);
+                ld8_f32(w + o, wx);
+                ld8_f32(m + o, mx);
+                ld8_f32(v + o, vx);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) adamw1(ux[e], wx[e], mx[e], vx[e], k);
+                st8_f32(w + o, wx);
+                st8_f32(m + o, mx);
+                st8_f32(v + o, vx);
+                st8_param<PDT>(p, o, wx);
+            }
+            done = nv * kVec;
+        }
+        for (int j = done + threadIdx.x; j < len; j += kThreads) {
+            float wj = w[j], mj = m[j], vj = v[j];
+            adamw1(u[j], wj, mj, vj, k);
+            w[j] = wj;
+            m[j] = mj;
+            v[j] = vj;
+            Param<PDT>::st1(p, j, wj);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a6: the scaler state machine.  [MEG] section 5 (skip, back off to at least
+// min_loss_scale, reset the tracker; or count a good step and grow after
+// `interval` of them); [MP] "Dynamic scaling" (the count restarts after every
+// overflow and every growth); [RST] ch. 13 "Discard a failed partial logical
+// update" (a skipped attempt keeps t and the beta powers).  One thread.
+// ---------------------------------------------------------------------------
+__global__ void k_scaler(DevState* __restrict__ st, ScalerParams sp) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    if (st->found_inf) {
+        if (sp.enabled) {
+            const float s = __fmul_rn(st->S, sp.backoff);
+            st->S = s > sp.min_scale ? s : sp.min_scale;
+        }
+        st->count = 0;
+        st->skipped = 1;
+    } else {
+        st->t += 1;
+        st->b1p = st->b1p_next;
+        st->b2p = st->b2p_next;
+        if (sp.enabled) {
+            st->count += 1;
+            if (st->count == sp.interval) {
+                const float s = __fmul_rn(st->S, sp.growth);
+                st->S = s < sp.max_scale ? s : sp.max_scale;
+                st->count = 0;
+            }
+        }
+        st->skipped = 0;
+    }
+    st->found_inf = 0;
+}
+
+// ---------------------------------------------------------------------------
+// dispatch tables
+// ---------------------------------------------------------------------------
+using AccFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, const GradTable, const void* const*, float);
+using UnsFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, const GradTable, const void* const*, float,
+                       DevState*, double*);
+using AdamFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, DevState*, AdamHP);
+
+AccFn acc_fn(int gdt, bool first) {
+    switch (gdt) {
+        case kBF16: return first ? k_accumulate<kBF16, true> : k_accumulate<kBF16, false>;
+        case kF16: return first ? k_accumulate<kF16, true> : k_accumulate<kF16, false>;
+        case kF32: return first ? k_accumulate<kF32, true> : k_accumulate<kF32, false>;
+        default: return nullptr;
+    }
+}
+
+template <int GDT>
+UnsFn uns_fn_dt(int mode) {
+    switch (mode) {
+        case kAccOnly: return k_unscale<GDT, kAccOnly>;
+        case kFirstOnly: return k_unscale<GDT, kFirstOnly>;
+        case kAccAndGrad: return k_unscale<GDT, kAccAndGrad>;
+        default: return nullptr;
+    }
+}
+
+UnsFn uns_fn(int gdt, int mode) {
+    switch (gdt) {
+        case kBF16: return uns_fn_dt<kBF16>(mode);
+        case kF16: return uns_fn_dt<kF16>(mode);
+        case kF32: return uns_fn_dt<kF32>(mode);
+        default: return nullptr;
+    }
+}
+
+AdamFn adam_fn(int pdt) {
+    switch (pdt) {
+        case kBF16: return k_adamw<kBF16>;
+        case kF16: return k_adamw<kF16>;
+        default: return nullptr;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_accumulate(int gdt, bool first, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp,
+                              const GradTable& inl, const void* const* gtab, float w, int grid, cudaStream_t s) {
+    AccFn f = acc_fn(gdt, first);
+    if (f == nullptr) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, inl, gtab, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unscale(int gdt, int mode, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp,
+                           const GradTable& inl, const void* const* gtab, float w, DevState* st,
+                           double* partials, int grid, cudaStream_t s) {
+    UnsFn f = uns_fn(gdt, mode);
+    if (f == nullptr) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, inl, gtab, w, st, partials);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm, cudaStream_t s) {
+    k_norm<<<1, kNormThreads, 0, s>>>(partials, nchunks, st, max_norm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(int pdt, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp, DevState* st,
+                         AdamHP hp, int grid, cudaStream_t s) {
+    AdamFn f = adam_fn(pdt);
+    if (f == nullptr) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, st, hp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s) {
+    k_scaler<<<1, 32, 0, s>>>(st, sp);
+    return cudaGetLastError();
+}
+
+int blocks_per_sm(int kind, int dt, int variant) {
+    const void* f = nullptr;
+    if (kind == 0) f = reinterpret_cast<const void*>(acc_fn(dt, variant != 0));
+    else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn(dt, variant));
+    else if (kind == 2) f = reinterpret_cast<const void*>(adam_fn(dt));
+    if (f == nullptr) return 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+}  // namespace tl

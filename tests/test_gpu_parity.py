@@ -1,0 +1,405 @@
+"""GPU parity: the CUDA library (through its C ABI) against the oracle on the same
+seeded inputs.
+
+Tolerances (fixed by the method's statement of what must agree):
+  overflow flags, skip decisions, the loss-scale sequence, the good-step count, t and
+  the beta powers: bit-exact;
+  fp32 master, m, v: at most 2 units in the last place per element;
+  bf16/fp16 parameters: at most 1 unit in the last place;
+  the global gradient norm: 1e-6 relative.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import loss_scaled_adamw_gb300 as tl
+from loss_scaled_adamw_gb300 import workloads as W
+from harness import (DT, GpuOptimizer, assert_ulps16, assert_ulps32, compare_scalars, compare_state,
+                     grad_bits, oracle_for, run_parity)
+from oracle_pins import read_golden
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from loss_scaled_adamw_gb300 import _build
+    _build.build()
+    tl.load_library()
+
+
+def custom(numel, pdtype="bf16", gdtype="bf16", k=2, steps=2, scaler=False, init_scale=1.0, interval=2000,
+           grad_std=1e-2, counts=None, injections=None, name="custom"):
+    return W.Workload(name, list(numel), pdtype, gdtype, steps=steps, k=k, grad_std=grad_std, scaler_enabled=scaler,
+                      init_scale=init_scale, interval=interval, fixed_counts=counts,
+                      grads_prescaled=scaler, injections=injections or {})
+
+
+# ---------------------------------------------------------------------------
+# the workloads at their stated sizes
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("gaps", [False, True], ids=["packed", "misaligned"])
+def test_bf16_small(gaps):
+    """12 x 4,096 bf16, k=2 with 6 and 3 targets, clip active, 3 steps."""
+    _, _, log = run_parity(W.make("bf16_small"), gaps=gaps)
+    assert all(e["norm_oracle"] > 1.0 for e in log)  # the clip is active
+
+
+def test_fp16_scaled_sequence():
+    """64 x 16,384 fp16 with dynamic loss scaling over 20 steps: skips at 3 and 11 and the
+    hand-derived S sequence, on the GPU."""
+    _, rows = read_golden("config1_scale_sequence.txt")
+    gpu, orc, log = run_parity(W.make("fp16_scaled"), compare_every=5)
+    for e, (step, log2s, skipped, count) in zip(log, rows):
+        assert e["S"] == 2.0 ** int(log2s) and e["skipped"] == int(skipped), e
+    assert gpu.status().t == 18
+
+
+def test_llama_10m():
+    """The ~10.3M-parameter Llama tensor list, k=4 with 5-20% padding, 10 steps."""
+    run_parity(W.make("llama_10m"), compare_every=5)
+
+
+# ---------------------------------------------------------------------------
+# ragged, misaligned, empty and degenerate lists
+# ---------------------------------------------------------------------------
+
+EDGE_LISTS = {
+    "one_element": [1],
+    "tails": [1, 7, 9, 127, 16383, 16384, 16385, 3 * 16384 + 5, 33],
+    "with_empty": [0, 5, 0, 4096, 0],
+    "odd_sizes": [3, 1023, 2047, 65537],
+}
+
+
+@pytest.mark.parametrize("lst", list(EDGE_LISTS), ids=list(EDGE_LISTS))
+@pytest.mark.parametrize("dtypes", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32"), ("f16", "bf16")],
+                         ids=lambda d: f"p{d[0]}-g{d[1]}")
+@pytest.mark.parametrize("gaps", [False, True], ids=["packed", "misaligned"])
+def test_edge_lists(lst, dtypes, gaps):
+    wl = custom(EDGE_LISTS[lst], pdtype=dtypes[0], gdtype=dtypes[1], k=3, steps=2, counts=[5, 1, 7])
+    run_parity(wl, gaps=gaps)
+
+
+@pytest.mark.parametrize("k", [1, 2, 5])
+def test_micro_batch_counts(k):
+    wl = custom([1000, 20000, 17], k=k, steps=2, counts=list(range(3, 3 + k)))
+    run_parity(wl, gaps=True)
+
+
+def test_empty_tensor_list():
+    """No tensors at all: the update still runs, commits and advances the scalars."""
+    wl = custom([], k=2, steps=3, counts=[2, 2])
+    gpu = GpuOptimizer(wl, torch.zeros(0))
+    for _ in range(3):
+        gpu.step([torch.zeros(0, dtype=torch.bfloat16)] * 2, [2, 2])
+    st = gpu.status()
+    assert st.t == 3 and st.skipped == 0 and st.norm == 0.0
+    assert st.b1p == float(np.float32(0.9)) ** 3 or abs(st.b1p - float(np.float32(0.9)) ** 3) < 1e-15
+
+
+def test_all_accumulated_then_unscale_null():
+    """tl_unscale_check(grads=NULL) after all k micro-batches went through tl_accumulate."""
+    wl = custom([4096, 333, 70000], k=3, steps=1, counts=[4, 4, 1])
+    master0 = W.master_init(wl)
+    gpu = GpuOptimizer(wl, master0, gaps=True)
+    orc = oracle_for(wl, master0)
+    grads = [W.grad_input(wl, 1, i) for i in range(3)]
+    ptrs = [gpu.grad_list(i, g) for i, g in enumerate(grads)]
+    for i in range(3):
+        tl.tl_accumulate(gpu.ctx, ptrs[i], [4, 4, 1][i], 9, 1 if i == 0 else 0)
+    tl.tl_unscale_check(gpu.ctx, None, 0, 9)
+    tl.tl_grad_norm(gpu.ctx, 1.0)
+    tl.tl_clip_adamw_step(gpu.ctx, tl.tl_adamw_hp(**W.HP))
+    tl.tl_scaler_update(gpu.ctx)
+    res = orc.step([grad_bits(g) for g in grads], [4, 4, 1], 1.0, **W.HP)
+    compare_scalars(gpu.status(), orc, res, "null-grads path")
+    compare_state(gpu.pull(), orc, wl, "null-grads path")
+
+
+@pytest.mark.parametrize("ntensors", [512, 513, 700])
+def test_long_lists_and_pointer_table_cache(ntensors):
+    """Lists longer than the by-value limit use cached device pointer tables; 20 distinct
+    gradient lists (more than the cache holds) force evictions."""
+    rng = np.random.default_rng(ntensors)
+    numel = [int(x) for x in rng.integers(1, 300, ntensors)]
+    wl = custom(numel, k=2, steps=10, counts=[3, 5])
+    master0 = W.master_init(wl)
+    gpu = GpuOptimizer(wl, master0, gaps=True)
+    orc = oracle_for(wl, master0)
+    for step in range(1, 11):
+        grads = [W.grad_input(wl, step, i) for i in range(2)]
+        slots = [(2 * step + i) % 20 for i in range(2)]
+        mbs = [gpu.grad_list(s, g) for s, g in zip(slots, grads)]
+        tl.logical_update(gpu.ctx, mbs, [3, 5], 1.0, tl.tl_adamw_hp(**W.HP))
+        res = orc.step([grad_bits(g) for g in grads], [3, 5], 1.0, **W.HP)
+        compare_scalars(gpu.status(), orc, res, f"long list step {step}")
+    compare_state(gpu.pull(), orc, wl, "long list")
+
+
+# ---------------------------------------------------------------------------
+# skip semantics, order of calls, state round trip, graphs, determinism
+# ---------------------------------------------------------------------------
+
+def test_skip_leaves_state_bitwise_unchanged():
+    """An overflowing update leaves master, m, v, params, t and beta powers bit-identical and
+    halves S; the next update carries nothing of the bad gradients."""
+    wl = custom([5000, 12345], pdtype="f16", gdtype="f16", k=2, steps=3, scaler=True, init_scale=2.0 ** 12,
+                interval=100, counts=[2, 7], injections={(2, 1): [(17, 0x7C00)]})
+    master0 = W.master_init(wl)
+    gpu = GpuOptimizer(wl, master0, gaps=True)
+    orc = oracle_for(wl, master0)
+    before = None
+    for step in (1, 2, 3):
+        grads = [W.grad_input(wl, step, i, scale=orc.state.S) for i in range(2)]
+        gpu.step(grads, [2, 7])
+        res = orc.step([grad_bits(g) for g in grads], [2, 7], 1.0, **W.HP)
+        st = gpu.status()
+        compare_scalars(st, orc, res, f"skip test step {step}")
+        now = gpu.pull()
+        if step == 1:
+            before = now
+        if step == 2:
+            assert st.skipped == 1 and st.S == 2.0 ** 11 and st.t == 1
+            for k in ("master", "m", "v", "param"):
+                assert np.array_equal(before[k].view(np.uint8), now[k].view(np.uint8)), k
+    compare_state(gpu.pull(), orc, wl, "after the skip")
+    assert gpu.status().t == 2
+
+
+def _small_ctx(scaler=False):
+    wl = custom([100, 28], k=2, steps=1, counts=[1, 1], scaler=scaler, init_scale=8.0, interval=3,
+                pdtype="f16" if scaler else "bf16", gdtype="f16" if scaler else "bf16")
+    gpu = GpuOptimizer(wl, W.master_init(wl))
+    g = gpu.grad_list(0, W.grad_input(wl, 1, 0, scale=8.0))
+    return gpu, g
+
+
+def test_call_order_and_count_errors():
+    gpu, g = _small_ctx()
+    ctx = gpu.ctx
+    hp = tl.tl_adamw_hp(**W.HP)
+
+    def expect(status, fn, *args):
+        with pytest.raises(tl.TLError) as ei:
+            fn(*args)
+        assert ei.value.status == status, str(ei.value)
+
+    expect(tl.TL_ESTATE, tl.tl_accumulate, ctx, g, 1, 2, 0)      # first=0 with nothing open
+    expect(tl.TL_ESTATE, tl.tl_grad_norm, ctx, 1.0)
+    expect(tl.TL_ESTATE, tl.tl_clip_adamw_step, ctx, hp)
+    expect(tl.TL_ESTATE, tl.tl_scaler_update, ctx)
+    expect(tl.TL_EINVAL, tl.tl_accumulate, ctx, g, 0, 2, 1)      # n_i = 0
+    expect(tl.TL_EINVAL, tl.tl_accumulate, ctx, g, 3, 2, 1)      # n_i > N
+    expect(tl.TL_EINVAL, tl.tl_accumulate, ctx, g, 1, 2 ** 53 + 1, 1)
+    expect(tl.TL_EINVAL, tl.tl_unscale_check, ctx, g, 1, 2)      # only micro-batch must be all of N
+    tl.tl_accumulate(ctx, g, 1, 3, 1)
+    expect(tl.TL_EINVAL, tl.tl_accumulate, ctx, g, 1, 4, 0)      # N changed mid-update
+    expect(tl.TL_EINVAL, tl.tl_unscale_check, ctx, g, 1, 3)      # 1 + 1 != 3
+    expect(tl.TL_EINVAL, tl.tl_unscale_check, ctx, None, 0, 3)   # accumulated 1 != 3
+    tl.tl_accumulate(ctx, g, 1, 3, 0)
+    tl.tl_unscale_check(ctx, g, 1, 3)
+    expect(tl.TL_ESTATE, tl.tl_unscale_check, ctx, g, 1, 3)
+    expect(tl.TL_ESTATE, tl.tl_accumulate, ctx, g, 1, 3, 1)      # past accumulation
+    expect(tl.TL_ESTATE, tl.tl_set_state, ctx, tl.tl_state(1.0, 0, 0, 1.0, 1.0))
+    tl.tl_grad_norm(ctx, 1.0)
+    expect(tl.TL_EINVAL, tl.tl_clip_adamw_step, ctx, tl.tl_adamw_hp(1e-3, 1.0, 0.95, 1e-8, 0.1))
+    tl.tl_clip_adamw_step(ctx, hp)
+    tl.tl_scaler_update(ctx)
+    st = gpu.status()
+    assert st.t == 1 and st.skipped == 0
+
+
+def test_restart_discards_partial_update():
+    """first=1 while an update is open restarts it: the partial sum is discarded."""
+    wl = custom([3000], k=2, steps=1, counts=[1, 2])
+    master0 = W.master_init(wl)
+    a = GpuOptimizer(wl, master0)
+    b = GpuOptimizer(wl, master0, key=50)
+    junk = W.grad_input(wl, 9, 0) * 1000
+    g = [W.grad_input(wl, 1, i) for i in range(2)]
+    pa = [a.grad_list(i, x) for i, x in enumerate(g)]
+    tl.tl_accumulate(a.ctx, a.grad_list(5, junk), 1, 3, 1)
+    tl.logical_update(a.ctx, pa, [1, 2], 1.0, tl.tl_adamw_hp(**W.HP))
+    b.step(g, [1, 2])
+    ra, rb = a.pull(), b.pull()
+    for k in ra:
+        assert np.array_equal(ra[k], rb[k]), k
+
+
+def test_state_roundtrip_resume():
+    """[MP] section 4: a resume keeps S and the good-step count; bad arguments raise."""
+    wl = custom([4096, 100], pdtype="f16", gdtype="f16", k=1, steps=7, scaler=True, init_scale=2.0 ** 10,
+                interval=3, counts=[10], injections={(4, 0): [(3, 0x7C00)]})
+    master0 = W.master_init(wl)
+    a = GpuOptimizer(wl, master0)
+    orc = oracle_for(wl, master0)
+    for step in range(1, 6):
+        grads = [W.grad_input(wl, step, 0, scale=orc.state.S)]
+        a.step(grads, [10])
+        orc.step([grad_bits(x) for x in grads], [10], 1.0, **W.HP)
+    st = tl.tl_get_state(a.ctx)
+    assert (st.S, st.count, st.t) == (orc.state.S, orc.state.count, orc.state.t)
+    # resume into a fresh context over copies of the tensors
+    b = GpuOptimizer(wl, master0, key=70)
+    for name in ("master", "m", "v", "param"):
+        b.lists[name].buf.copy_(a.lists[name].buf)
+    tl.tl_set_state(b.ctx, st)
+    for step in (6, 7):
+        grads = [W.grad_input(wl, step, 0, scale=orc.state.S)]
+        a.step(grads, [10])
+        b.step(grads, [10])
+        res = orc.step([grad_bits(x) for x in grads], [10], 1.0, **W.HP)
+        compare_scalars(b.status(), orc, res, f"resumed step {step}")
+    ra, rb = a.pull(), b.pull()
+    for k in ra:
+        assert np.array_equal(ra[k], rb[k]), k
+    for bad in (tl.tl_state(3.0, 0, 0, 1.0, 1.0), tl.tl_state(8.0, 3, 0, 1.0, 1.0),
+                tl.tl_state(8.0, 0, -1, 1.0, 1.0), tl.tl_state(0.25, 0, 0, 1.0, 1.0)):
+        with pytest.raises(tl.TLError) as ei:
+            tl.tl_set_state(b.ctx, bad)
+        assert ei.value.status == tl.TL_EINVAL
+
+
+def test_cuda_graph_capture_replay():
+    """The whole update has no host synchronisation, so it can be captured once and
+    replayed; replays match eager updates bit for bit."""
+    wl = custom([20000, 4099, 8], k=3, steps=4, counts=[3, 1, 2])
+    master0 = W.master_init(wl)
+    eager = GpuOptimizer(wl, master0)
+    graphed = GpuOptimizer(wl, master0, key=30)
+    grads = [W.grad_input(wl, 1, i) for i in range(3)]
+    pe = [eager.grad_list(i, g) for i, g in enumerate(grads)]
+    pg = [graphed.grad_list(i, g) for i, g in enumerate(grads)]
+    hp = tl.tl_adamw_hp(**W.HP)
+    tl.logical_update(graphed.ctx, pg, [3, 1, 2], 1.0, hp)   # warm-up outside capture
+    tl.logical_update(eager.ctx, pe, [3, 1, 2], 1.0, hp)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        tl.logical_update(graphed.ctx, pg, [3, 1, 2], 1.0, hp)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+        tl.logical_update(eager.ctx, pe, [3, 1, 2], 1.0, hp)
+    torch.cuda.synchronize()
+    re, rg = eager.pull(), graphed.pull()
+    for k in re:
+        assert np.array_equal(re[k], rg[k]), k
+    assert eager.status().t == graphed.status().t == 4
+
+
+def test_norm_is_deterministic():
+    wl = custom([300000, 77, 5000], k=2, steps=1, counts=[1, 1])
+    master0 = W.master_init(wl)
+    grads = [W.grad_input(wl, 1, i) for i in range(2)]
+    norms = []
+    for key in (0, 40):
+        g = GpuOptimizer(wl, master0, key=key)
+        g.step(grads, [1, 1])
+        st = g.status()
+        norms.append((st.norm, st.sumsq))
+    assert norms[0] == norms[1]
+
+
+class _DeviceScalar:
+    """A device address exposed through __cuda_array_interface__ (one fp32)."""
+
+    def __init__(self, addr):
+        self.__cuda_array_interface__ = {"shape": (1,), "typestr": "<f4", "data": (addr, True), "version": 2}
+
+
+def test_scale_pointer_tracks_the_device_scale():
+    """tl_scale_ptr lets the loss be scaled on the device; it follows the scaler without a
+    host read (here: 8 -> 4 after an overflowing update)."""
+    gpu, g = _small_ctx(scaler=True)
+    S_dev = torch.as_tensor(_DeviceScalar(tl.tl_scale_ptr(gpu.ctx)), device="cuda")
+    loss = torch.tensor([0.75], device="cuda")
+    assert float((loss * S_dev).item()) == 6.0
+    bad = W.grad_input(gpu.wl, 1, 0, scale=8.0)
+    bad.view(torch.int16)[3] = 0x7C00
+    gb = gpu.grad_list(1, bad)
+    tl.logical_update(gpu.ctx, [gb, gb], [1, 1], 1.0, tl.tl_adamw_hp(**W.HP))
+    assert float((loss * S_dev).item()) == 3.0
+    assert gpu.status().S == 4.0
+
+
+# ---------------------------------------------------------------------------
+# the full-size workloads
+# ---------------------------------------------------------------------------
+
+def test_ragged_100k_full():
+    """100,000 ragged tensors (~400M parameters), many starting off 16-byte boundaries;
+    fp16 with loss scaling, an inf in micro-batch 1 of step 2; every element compared."""
+    wl = W.make("ragged_100k")
+    run_parity(wl, gaps=True, compare_every=wl.steps)
+
+
+def test_llama_1b_full_size_sampled():
+    """The ~1.24B-parameter list at full size, k=8, in the benchmark's launch configuration:
+    the norm against the oracle's sum over every element (streamed through host memory in
+    slices), and 200,000 sampled elements of master, m, v and params computed one by one."""
+    import oracle
+    wl = W.make("llama_1b")
+    master0 = W.master_init(wl, "cuda")
+    gpu = GpuOptimizer(wl, master0)
+    counts = wl.counts(1)
+    N = sum(counts)
+    grads = [W.grad_input(wl, 1, i, device="cuda") for i in range(wl.k)]
+    rng = np.random.default_rng(123)
+    idx = np.unique(rng.integers(0, wl.P, 200_000))
+    idx_t = torch.from_numpy(idx).cuda()
+    w0 = master0[idx_t].cpu().numpy()
+    g_s = [grad_bits(g[idx_t]) for g in grads]
+    gpu.step(grads, counts)
+    st = gpu.status()
+    lib = oracle.load()
+
+    def P_(a):
+        return a.ctypes.data_as(ctypes.c_void_p)
+
+    weights = [lib.tlo_microbatch_weight(n, N) for n in counts]
+    # oracle squared norm over all elements, streamed in slices of 2^26
+    sumsq = 0.0
+    found = 0
+    step = 1 << 26
+    for lo in range(0, wl.P, step):
+        hi = min(wl.P, lo + step)
+        acc = np.empty(hi - lo, np.float32)
+        for i, g in enumerate(grads):
+            gb = grad_bits(g[lo:hi])
+            lib.tlo_accumulate(P_(acc), P_(gb), oracle.DT_BF16, hi - lo, weights[i], 1 if i == 0 else 0)
+        found |= lib.tlo_unscale_check(P_(acc), hi - lo, 1.0)
+        sumsq += lib.tlo_sumsq(P_(acc), hi - lo)
+    assert found == 0 and st.found_inf == 0 and st.skipped == 0
+    norm = lib.tlo_norm_from_sumsq(sumsq)
+    assert abs(st.norm - norm) <= 1e-6 * norm, (st.norm, norm)
+    coef = lib.tlo_clip_coef(norm, wl.max_norm)
+    # sampled elements, one by one, through the oracle's functions in the step's order
+    n = idx.size
+    acc = np.empty(n, np.float32)
+    for i in range(wl.k):
+        lib.tlo_accumulate(P_(acc), P_(np.ascontiguousarray(g_s[i])), oracle.DT_BF16, n, weights[i], 1 if i == 0 else 0)
+    lib.tlo_unscale_check(P_(acc), n, 1.0)
+    hp = oracle.AdamWHP(**{k: v for k, v in W.HP.items()})
+    sc = lib.tlo_adamw_prepare(ctypes.byref(hp), float(np.float32(0.9)), float(np.float32(0.95)))
+    w = w0.astype(np.float32).copy()
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    p = np.empty(n, np.uint16)
+    lib.tlo_adamw_recast(P_(w), P_(m), P_(v), P_(p), oracle.DT_BF16, P_(acc), n, coef, ctypes.byref(sc))
+    L = gpu.lists
+    assert_ulps32(L["master"].flat()[idx_t].cpu().numpy(), w, 2, "llama_1b master")
+    assert_ulps32(L["m"].flat()[idx_t].cpu().numpy(), m, 2, "llama_1b m")
+    assert_ulps32(L["v"].flat()[idx_t].cpu().numpy(), v, 2, "llama_1b v")
+    gp = L["param"].flat()[idx_t].cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_ulps16(gp, p, 1, "llama_1b param")
+    assert st.t == 1
