@@ -216,7 +216,7 @@ class GpuWorkload:
         def plist(t):
             es, base = t.element_size(), t.data_ptr()
             p = tl.PtrList([base + o * es for o in offs])
-            p.tensors = [t]
+            p.keep = t
             return p
 
         self.plists = {n: plist(getattr(self, n)) for n in ("param", "master", "m", "v", "acc")}

@@ -80,7 +80,7 @@ class DeviceList:
         es = self.buf.element_size()
         base = self.buf.data_ptr()
         self.ptrs = tl.PtrList([base + o * es for o in self.offs])
-        self.ptrs.tensors = [self.buf]  # keep the buffer alive with the pointer array
+        self.ptrs.keep = self.buf  # keep the buffer alive with the pointer array
 
     def load(self, flat):
         if self.index is None:

@@ -314,7 +314,7 @@ class _DeviceScalar:
     """A device address exposed through __cuda_array_interface__ (one fp32)."""
 
     def __init__(self, addr):
-        self.__cuda_array_interface__ = {"shape": (1,), "typestr": "<f4", "data": (addr, True), "version": 2}
+        self.__cuda_array_interface__ = {"shape": (1,), "typestr": "<f4", "data": (addr, False), "version": 2}
 
 
 def test_scale_pointer_tracks_the_device_scale():
