@@ -221,6 +221,37 @@ const float* tl_scale_ptr(const tl_ctx* ctx);
 int64_t tl_num_params(const tl_ctx* ctx);
 int64_t tl_num_chunks(const tl_ctx* ctx);
 
+/* Result of tl_unscale_norm_noalloc, written by the device into caller memory. */
+typedef struct {
+    float norm;         /* global L2 norm of the unscaled gradient */
+    float coef;         /* clip coefficient (<= 1; 1 when max_norm <= 0) */
+    int32_t found_inf;  /* 1 if some unscaled element, or the squared norm, is not finite */
+    int32_t reserved;
+    double sumsq;       /* squared norm in fp64 */
+} tl_norm_result;
+
+/* Unscale + overflow check + global norm + clip coefficient WITHOUT ANY
+ * ALLOCATION.  No passage of the pages has a counterpart: this entry point
+ * exists for callers that cannot call cudaMalloc (device memory owned by
+ * another allocator, no allocation allowed after start-up, or an allocation
+ * that would disturb a capture or a memory plan), who therefore cannot use
+ * tl_create.  It needs no context.
+ * acc: ntensors fp32 device tensors of numel[i] elements, holding the
+ * accumulated scaled gradient; they are overwritten with u = acc * (1/S).
+ * S: a positive power of two.  max_norm <= 0 disables clipping.  out: device
+ * memory (8-byte aligned) that receives the result; same arithmetic as
+ * tl_unscale_check + tl_grad_norm.
+ * Scratch: a fixed array inside the library (512 KiB of fp64 partials,
+ * allocated when the library is loaded and held by every GPU that loads it
+ * until the process exits).  Limits: ntensors <= 256 and at most 2^16 chunks
+ * of 16,384 elements (2^30 elements); larger lists give TL_EINVAL.  The first
+ * call on a device looks up the scratch address for that device, so make that
+ * first call before any stream capture.  Every call shares the scratch and
+ * writes every partial it reads; calls that overlap on the GPU race on it.
+ * Errors: TL_EINVAL (sizes, pointers, S), TL_ECUDA. */
+int tl_unscale_norm_noalloc(int64_t ntensors, const int64_t* numel, float* const* acc, float S,
+                            float max_norm, tl_norm_result* out, tl_stream stream);
+
 /* Number of kernels this context has launched so far. */
 int64_t tl_launch_count(const tl_ctx* ctx);
 

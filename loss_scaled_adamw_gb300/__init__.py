@@ -32,7 +32,7 @@ TL_F32, TL_BF16, TL_F16 = 0, 1, 2
 EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_unscale_check", "tl_grad_norm",
             "tl_clip_adamw_step", "tl_scaler_update", "tl_read_status", "tl_get_state", "tl_set_state",
             "tl_scale_ptr", "tl_num_params", "tl_num_chunks", "tl_launch_count", "tl_status_string",
-            "tl_last_error")
+            "tl_last_error", "tl_unscale_norm_noalloc")
 
 
 class TLError(RuntimeError):
@@ -69,6 +69,11 @@ class tl_status(ctypes.Structure):
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class tl_norm_result(ctypes.Structure):
+    _fields_ = [("norm", ctypes.c_float), ("coef", ctypes.c_float), ("found_inf", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("sumsq", ctypes.c_double)]
 
 
 def make_config(param_dtype: int = TL_BF16, grad_dtype: int = TL_BF16, scaler_enabled: bool = False,
@@ -116,6 +121,7 @@ def load_library():
         "tl_launch_count": (i64, [vp]),
         "tl_status_string": (ctypes.c_char_p, [i32]),
         "tl_last_error": (ctypes.c_char_p, [vp]),
+        "tl_unscale_norm_noalloc": (i32, [i64, ctypes.POINTER(i64), pp, f32, f32, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -272,3 +278,20 @@ def logical_update(ctx: Context, micro_batches, counts, max_norm: float, hp: tl_
     tl_grad_norm(ctx, max_norm, s)
     tl_clip_adamw_step(ctx, hp, s)
     tl_scaler_update(ctx, s)
+
+
+def tl_unscale_norm_noalloc(numel: Sequence[int], accs, S: float, max_norm: float, out_addr: int,
+                            stream=None) -> None:
+    """Unscale + overflow check + global norm + clip coefficient with no allocation (for
+    callers that cannot call cudaMalloc): accs are fp32 device tensors overwritten with
+    acc / S; out_addr is the device address of a tl_norm_result (24 bytes, 8-byte aligned)."""
+    lib = load_library()
+    n = len(numel)
+    lst = accs if isinstance(accs, PtrList) else PtrList(accs)
+    if len(lst) != n:
+        raise ValueError("accs must have len(numel) entries")
+    numel_arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numel])
+    rc = lib.tl_unscale_norm_noalloc(n, numel_arr, lst.array, float(S), float(max_norm),
+                                     ctypes.c_void_p(int(out_addr)), _stream(stream))
+    if rc != TL_OK:
+        raise TLError("tl_unscale_norm_noalloc", rc, lib.tl_status_string(rc).decode())

@@ -1,6 +1,7 @@
 """Build the CUDA library (libtl_gb300.so) in-tree with nvcc for sm_103a.
 
-Two translation units (kernels, host C ABI) compile in parallel, then link
+The translation units (kernels, host C ABI, the allocation-free entry point)
+compile in parallel, then link
 into one shared library with the CUDA runtime linked statically.
 """
 from __future__ import annotations
@@ -13,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtl_gb300.so")
-SOURCES = ["tl_kernels.cu", "tl_api.cu"]
+SOURCES = ["tl_kernels.cu", "tl_api.cu", "tl_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "tl_internal.cuh"), os.path.join(ROOT, "include", "tl.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
