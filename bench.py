@@ -47,6 +47,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama_1b")
+    ap.add_argument("--path", choices=["resident", "per_microbatch"], default="resident",
+                    help="resident: the k micro-batch gradient lists are read in one pass (tl_accumulate_many); "
+                         "per_microbatch: one tl_accumulate per micro-batch")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -185,14 +188,6 @@ class ClockSampler:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
-KERNEL_BYTES = {  # algorithmic bytes per parameter per launch (bf16 grads and params)
-    "accumulate_first": 2 + 4,
-    "accumulate": 2 + 4 + 4,
-    "unscale_check": 2 + 4 + 4,
-    "clip_adamw_step": 16 + 12 + 2,
-}
-
-
 class GpuWorkload:
     """Device-resident tensor lists of a workload, packed into flat buffers."""
 
@@ -221,6 +216,7 @@ class GpuWorkload:
 
         self.plists = {n: plist(getattr(self, n)) for n in ("param", "master", "m", "v", "acc")}
         self.gplists = [plist(g) for g in self.grads]
+        self.many = tl.ManyLists(self.gplists)
         dt = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32}
         cfg = tl.make_config(dt[wl.param_dtype], dt[wl.grad_dtype], wl.scaler_enabled,
                              wl.init_scale if wl.scaler_enabled else 1.0, interval=wl.interval)
@@ -229,29 +225,91 @@ class GpuWorkload:
         self.counts = wl.counts(1)
         self.N = sum(self.counts)
         self.hp = tl.tl_adamw_hp(1e-3, 0.9, 0.95, 1e-8, 0.1)
+        sg = {"bf16": 2, "f16": 2, "f32": 4}[wl.grad_dtype]
+        sp = {"bf16": 2, "f16": 2}[wl.param_dtype]
+        self.adam_bytes = 16 + 12 + sp
 
-    def step(self, events=None):
-        """One logical update; with `events`, a pair of CUDA events around every call."""
-        import loss_scaled_adamw_gb300 as tl
-        k = self.wl.k
-        calls = []
+        k = wl.k
+        # (kernel name, algorithmic bytes per parameter, call) for each path
+        per = []
         for i in range(k - 1):
-            calls.append(("accumulate_first" if i == 0 else "accumulate",
-                          lambda i=i: tl.tl_accumulate(self.ctx, self.gplists[i], self.counts[i], self.N, 1 if i == 0 else 0)))
-        calls.append(("unscale_check", lambda: tl.tl_unscale_check(self.ctx, self.gplists[k - 1], self.counts[k - 1], self.N)))
-        calls.append(("grad_norm", lambda: tl.tl_grad_norm(self.ctx, self.wl.max_norm)))
-        calls.append(("clip_adamw_step", lambda: tl.tl_clip_adamw_step(self.ctx, self.hp)))
-        calls.append(("scaler_update", lambda: tl.tl_scaler_update(self.ctx)))
-        for name, fn in calls:
+            per.append(("accumulate_first" if i == 0 else "accumulate", sg + 4 if i == 0 else sg + 8,
+                        lambda i=i: tl.tl_accumulate(self.ctx, self.gplists[i], self.counts[i], self.N, 1 if i == 0 else 0)))
+        per.append(("unscale_check", sg + (8 if k > 1 else 4),
+                    lambda: tl.tl_unscale_check(self.ctx, self.gplists[k - 1], self.counts[k - 1], self.N)))
+        tail = [("grad_norm", None, lambda: tl.tl_grad_norm(self.ctx, self.wl.max_norm)),
+                ("clip_adamw_step", self.adam_bytes, lambda: tl.tl_clip_adamw_step(self.ctx, self.hp)),
+                ("scaler_update", None, lambda: tl.tl_scaler_update(self.ctx))]
+        # the resident pass reads 8 lists per launch, writes acc once per launch
+        launches = (k + 7) // 8
+        many_bytes = k * sg + 4 * launches + 4 * (launches - 1)
+        res = [("accumulate_many", many_bytes,
+                lambda: tl.tl_accumulate_many(self.ctx, self.many, self.counts, self.N, 1))]
+        self.paths = {"resident": res + tail, "per_microbatch": per + tail}
+
+    def step_bytes(self, path):
+        return self.P * sum(b for _, b, _ in self.paths[path] if b)
+
+    def step(self, path, events=None):
+        """One logical update; with `events`, a pair of CUDA events around every call."""
+        import torch
+        for name, _, fn in self.paths[path]:
             if events is None:
                 fn()
             else:
-                import torch
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 fn()
                 b.record()
                 events.append((name, a, b))
+
+
+def time_path(args, gw, path, world):
+    """K timed steps of one path (after W warm-up steps), with per-kernel events."""
+    import torch
+    import loss_scaled_adamw_gb300 as tl
+    for _ in range(args.warmup):
+        gw.step(path)
+    torch.cuda.synchronize()
+    barrier()
+    events = []
+    launches0 = tl.tl_launch_count(gw.ctx)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        gw.step(path, events)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    launches = tl.tl_launch_count(gw.ctx) - launches0
+    elapsed_max = max_over_ranks(elapsed, gw.device)
+    peak, peak_kind = hbm_peak()
+    per = {}
+    for name, a, b in events:
+        per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    bytes_of = {n: b for n, b, _ in gw.paths[path]}
+    kernels = {}
+    for name, ts in per.items():
+        avg = sum(ts) / len(ts)
+        entry = {"launches": len(ts), "avg_ms": avg * 1e3, "share": sum(ts) / elapsed}
+        if bytes_of.get(name):
+            gbs = bytes_of[name] * gw.P / avg / 1e9
+            entry.update({"bytes_per_param": bytes_of[name], "bytes_per_launch": bytes_of[name] * gw.P,
+                          "achieved_gbs": gbs, "frac": gbs / peak})
+        kernels[name] = entry
+    sb = gw.step_bytes(path)
+    return {"elapsed_max": elapsed_max, "launches": launches, "kernels": kernels,
+            "value": whole_job_rate(gw.P, args.steps, world, elapsed_max),
+            "ms_per_step": elapsed_max / args.steps * 1e3,
+            "hbm": {"algorithmic_bytes_per_step": sb, "bytes_per_param": sb / gw.P,
+                    "achieved_gbs_per_gpu": sb * args.steps / elapsed_max / 1e9, "peak_gbs": peak,
+                    "peak_kind": peak_kind, "frac": sb * args.steps / elapsed_max / 1e9 / peak}}
+
+
+TRAFFIC_KEYS = {"accumulate": "k_accumulate_bf16", "clip_adamw_step": "k_adamw_bf16",
+                "unscale_check": "k_unscale_bf16_acc_grad", "accumulate_first": "k_accumulate_first_bf16",
+                "accumulate_many": "k_accum_many_bf16_first_last"}
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -266,74 +324,34 @@ def run_gpu(args, rank, world, local_rank):
     wl = W.make(args.workload)
     gw = GpuWorkload(wl, device)
     P, k = wl.P, wl.k
-    step_bytes = P * (KERNEL_BYTES["accumulate_first"] + (k - 2) * KERNEL_BYTES["accumulate"]
-                      + KERNEL_BYTES["unscale_check"] + KERNEL_BYTES["clip_adamw_step"]) if k > 1 else \
-        P * (6 + KERNEL_BYTES["clip_adamw_step"])
-    for _ in range(args.warmup):
-        gw.step()
-    torch.cuda.synchronize()
-    barrier()
-
-    # ---- device-resident timed region ----
-    events = []
-    launches0 = tl.tl_launch_count(gw.ctx)
     with ClockSampler(gpu_id(local_rank)) as clk:
-        torch.cuda.synchronize()
-        barrier()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for _ in range(args.steps):
-            gw.step(events)
-        t1.record()
-        torch.cuda.synchronize()
-        barrier()
-        elapsed = t0.elapsed_time(t1) / 1e3
-        launches = tl.tl_launch_count(gw.ctx) - launches0
-
-        # ---- end-to-end through host buffers ----
-        e2e = None
-        if not args.no_e2e:
-            e2e = run_e2e(args, gw, world)
-    elapsed_max = max_over_ranks(elapsed, device)
+        head = time_path(args, gw, args.path, world)
+        other_name = "per_microbatch" if args.path == "resident" else "resident"
+        other = time_path(args, gw, other_name, world)
+        e2e = None if args.no_e2e else run_e2e(args, gw, world)
     st = tl.tl_read_status(gw.ctx)
-
-    per = {}
-    for name, a, b in events:
-        per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    kernels = head["kernels"]
+    dom = max((n for n in kernels if "achieved_gbs" in kernels[n]), key=lambda n: kernels[n]["share"])
     peak, peak_kind = hbm_peak()
-    kernels = {}
-    for name, ts in per.items():
-        avg = sum(ts) / len(ts)
-        entry = {"launches": len(ts), "avg_ms": avg * 1e3, "share": sum(ts) / elapsed}
-        if name in KERNEL_BYTES:
-            gbs = KERNEL_BYTES[name] * P / avg / 1e9
-            entry.update({"bytes_per_launch": KERNEL_BYTES[name] * P, "achieved_gbs": gbs, "frac": gbs / peak})
-        kernels[name] = entry
-    dom = max((n for n in kernels if n in KERNEL_BYTES), key=lambda n: kernels[n]["share"] * 1.0)
-    value = whole_job_rate(P, args.steps, world, elapsed_max)
-    clocks = clk.summary()
-    traffic_key = {"accumulate": "k_accumulate_bf16", "clip_adamw_step": "k_adamw_bf16",
-                   "unscale_check": "k_unscale_bf16_acc_grad", "accumulate_first": "k_accumulate_first_bf16"}[dom]
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; random-init masters, N(0,1e-3) bf16 grads)",
         "config": {"workload": f"{wl.name}: ~1.24B-param Llama tensor list, {len(wl.numel)} tensors, P={P}, "
                                f"bf16 params/grads, fp32 master/m/v/acc, k={k} micro-batches"
                                if wl.name == "llama_1b" else f"{wl.name}: {len(wl.numel)} tensors, P={P}, k={k}",
-                   "P": P, "k": k, "tensors": len(wl.numel), "counts": gw.counts,
+                   "P": P, "k": k, "tensors": len(wl.numel), "counts": gw.counts, "path": args.path,
                    "l2": "no flush: every launch streams >= 7.4 GB, far above the 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "hbm": {"algorithmic_bytes_per_step": step_bytes, "bytes_per_param": step_bytes / P,
-                "achieved_gbs_per_gpu": step_bytes * args.steps / elapsed_max / 1e9,
-                "peak_gbs": peak, "peak_kind": peak_kind,
-                "frac": step_bytes * args.steps / elapsed_max / 1e9 / peak},
+        "hbm": head["hbm"],
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
                      "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_kind": peak_kind,
-                     "traffic": recorded_traffic(traffic_key)},
+                     "traffic": recorded_traffic(TRAFFIC_KEYS.get(dom, dom))},
         "kernels": kernels,
-        "gpu_launches": launches,
-        "clocks": clocks,
+        "gpu_launches": head["launches"],
+        "paths": {args.path: {k2: head[k2] for k2 in ("value", "ms_per_step", "hbm")},
+                  other_name: {k2: other[k2] for k2 in ("value", "ms_per_step", "hbm", "kernels")}},
+        "clocks": clk.summary(),
         "status": {"S": st.S, "t": st.t, "skipped": st.skipped, "norm": st.norm},
     }
     if e2e is not None:

@@ -34,7 +34,9 @@
  * anything else a scalar path.
  *
  * Errors.  Every function returns a status code; nothing is thrown across
- * this boundary.  A call that returns an error has enqueued no work.
+ * this boundary.  A call that returns an error has launched no kernel and
+ * touched no caller memory (at most it has refreshed the context's own cache
+ * of gradient pointer tables).
  * Non-finite gradients are NOT an error: they set the device overflow flag
  * and the update is skipped on the device.
  *
@@ -170,6 +172,22 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
  * Errors: TL_EINVAL (counts do not add up to N), TL_ESTATE (out of order). */
 int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t N,
                      tl_stream stream);
+
+/* Several resident micro-batches in one pass (a2 for each, and a3 when last = 1).
+ * For callers that keep the k micro-batch gradients resident (HBM is large on
+ * this part): grads holds k lists of ntensors device pointers, list-major
+ * (grads[i*ntensors + t] is tensor t of micro-batch i), n[i] their valid target
+ * counts, N the total of the update.  Per element the result is bit-identical
+ * to tl_accumulate(first=1) / tl_accumulate(first=0) ... / tl_unscale_check in
+ * the same order: acc = w_1 g_1, acc = fma(w_i, g_i, acc), then with last = 1
+ * u = acc * (1/S), the overflow flag and the squared-norm partials.  The fp32
+ * buffer is written once per 8 micro-batches instead of once per micro-batch
+ * (with k = 8: 2k + 4 bytes per parameter instead of 10k - 4).  Starts an
+ * update when none is open, else continues it; with last = 1 the counts of the
+ * update must total N, and the next call is tl_grad_norm.
+ * Errors: TL_EINVAL (counts, NULL pointers), TL_ESTATE (out of order). */
+int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64_t* n, int64_t N, int last,
+                       tl_stream stream);
 
 /* Global L2 norm and clip coefficient (a4).  [MEG] section 9: global_norm =
  * sqrt(sum ||grad||^2), clip_coef = max_norm / (global_norm + eps); the

@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_PKG, "libtl_gb300.so")
 TL_OK, TL_EINVAL, TL_ECUDA, TL_ESTATE, TL_ENOMEM = 0, 1, 2, 3, 4
 TL_F32, TL_BF16, TL_F16 = 0, 1, 2
 
-EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_unscale_check", "tl_grad_norm",
+EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "tl_unscale_check", "tl_grad_norm",
             "tl_clip_adamw_step", "tl_scaler_update", "tl_read_status", "tl_get_state", "tl_set_state",
             "tl_scale_ptr", "tl_num_params", "tl_num_chunks", "tl_launch_count", "tl_status_string",
             "tl_last_error", "tl_unscale_norm_noalloc")
@@ -108,6 +108,7 @@ def load_library():
                             ctypes.POINTER(tl_config), vp]),
         "tl_destroy": (i32, [vp]),
         "tl_accumulate": (i32, [vp, pp, i64, i64, i32, vp]),
+        "tl_accumulate_many": (i32, [vp, i32, pp, ctypes.POINTER(i64), i64, i32, vp]),
         "tl_unscale_check": (i32, [vp, pp, i64, i64, vp]),
         "tl_grad_norm": (i32, [vp, f32, vp]),
         "tl_clip_adamw_step": (i32, [vp, ctypes.POINTER(tl_adamw_hp), vp]),
@@ -214,6 +215,30 @@ def tl_accumulate(ctx: Context, grads, n_i: int, N: int, first: int, stream=None
                                                               int(first), _stream(stream)))
 
 
+class ManyLists:
+    """k gradient lists flattened list-major into one C pointer array (keeps them alive)."""
+
+    def __init__(self, lists: Sequence):
+        self.lists = [l if isinstance(l, PtrList) else PtrList(l) for l in lists]
+        n = len(self.lists[0]) if self.lists else 0
+        flat = []
+        for l in self.lists:
+            if len(l) != n:
+                raise ValueError("every gradient list must have the same number of tensors")
+            flat.extend(l.array[i] for i in range(n))
+        self.k = len(self.lists)
+        self.array = (ctypes.c_void_p * max(len(flat), 1))(*flat)
+
+
+def tl_accumulate_many(ctx: Context, lists, counts: Sequence[int], N: int, last: int, stream=None) -> None:
+    ml = lists if isinstance(lists, ManyLists) else ManyLists(lists)
+    cnt = (ctypes.c_int64 * max(ml.k, 1))(*[int(c) for c in counts])
+    if len(counts) != ml.k:
+        raise ValueError("one count per gradient list")
+    _check(ctx, "tl_accumulate_many", load_library().tl_accumulate_many(ctx.handle, ml.k, ml.array, cnt, int(N),
+                                                                        int(last), _stream(stream)))
+
+
 def tl_unscale_check(ctx: Context, grads, n_k: int, N: int, stream=None) -> None:
     _check(ctx, "tl_unscale_check", load_library().tl_unscale_check(ctx.handle, _ptrs(grads), int(n_k), int(N),
                                                                     _stream(stream)))
@@ -264,17 +289,23 @@ def tl_launch_count(ctx: Context) -> int:
     return int(load_library().tl_launch_count(ctx.handle))
 
 
-def logical_update(ctx: Context, micro_batches, counts, max_norm: float, hp: tl_adamw_hp, stream=None) -> None:
+def logical_update(ctx: Context, micro_batches, counts, max_norm: float, hp: tl_adamw_hp, stream=None,
+                   resident: bool = False) -> None:
     """One attempted logical update: the tl_* call sequence over k micro-batches
-    (micro_batches[i] is a tensor list or PtrList; counts[i] its valid targets)."""
-    k = len(micro_batches)
+    (micro_batches[i] is a tensor list or PtrList; counts[i] its valid targets).
+    resident=True reads all k lists in one pass (tl_accumulate_many); micro_batches
+    may then also be a prebuilt ManyLists."""
+    k = micro_batches.k if isinstance(micro_batches, ManyLists) else len(micro_batches)
     if k < 1 or len(counts) != k:
         raise ValueError("need one count per micro-batch and at least one micro-batch")
     N = int(sum(int(c) for c in counts))
     s = _stream(stream)
-    for i in range(k - 1):
-        tl_accumulate(ctx, micro_batches[i], counts[i], N, 1 if i == 0 else 0, s)
-    tl_unscale_check(ctx, micro_batches[k - 1], counts[k - 1], N, s)
+    if resident:
+        tl_accumulate_many(ctx, micro_batches, counts, N, 1, s)
+    else:
+        for i in range(k - 1):
+            tl_accumulate(ctx, micro_batches[i], counts[i], N, 1 if i == 0 else 0, s)
+        tl_unscale_check(ctx, micro_batches[k - 1], counts[k - 1], N, s)
     tl_grad_norm(ctx, max_norm, s)
     tl_clip_adamw_step(ctx, hp, s)
     tl_scaler_update(ctx, s)

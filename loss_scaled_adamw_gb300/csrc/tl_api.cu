@@ -76,6 +76,7 @@ struct tl_ctx {
     int grid_acc[3][2] = {{0}};
     int grid_uns[3][3] = {{0}};
     int grid_adam[3] = {0};
+    int grid_many[3][4] = {{0}};
     // the update in flight
     int phase = kIdle;
     int64_t n_sum = 0;
@@ -154,6 +155,9 @@ int check_grads(tl_ctx* ctx, const void* const* grads) {
 
 // Resolve the gradient table for one call: by value when short, else a cached
 // device table (uploaded on first use of this exact pointer list).
+int resolve_device_table(tl_ctx* ctx, const void* const* grads, cudaStream_t s, const void* const** dtab,
+                         GradSlot** used);
+
 int resolve_grads(tl_ctx* ctx, const void* const* grads, cudaStream_t s, GradTable* inl,
                   const void* const** dtab, GradSlot** used) {
     *dtab = nullptr;
@@ -164,6 +168,15 @@ int resolve_grads(tl_ctx* ctx, const void* const* grads, cudaStream_t s, GradTab
         for (int64_t i = 0; i < ctx->ntensors; ++i) inl->p[i] = grads[i];
         return TL_OK;
     }
+    return resolve_device_table(ctx, grads, s, dtab, used);
+}
+
+// A device-resident copy of one gradient pointer list, from the cache (uploaded
+// on the first use of this exact list).
+int resolve_device_table(tl_ctx* ctx, const void* const* grads, cudaStream_t s, const void* const** dtab,
+                         GradSlot** used) {
+    *dtab = nullptr;
+    *used = nullptr;
     const uint64_t h = hash_ptrs(grads, ctx->ntensors);
     ctx->clock += 1;
     for (GradSlot& sl : ctx->slots) {
@@ -314,7 +327,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
         free_ctx(ctx);
         return TL_ENOMEM;
     }
-    if (ntensors > kInlineGrads) {
+    if (ntensors > kInlineMany / kMaxMany) {
         for (GradSlot& sl : ctx->slots) {
             if (cudaMalloc(reinterpret_cast<void**>(&sl.d_tab), sizeof(void*) * size_t(ntensors)) != cudaSuccess ||
                 cudaMallocHost(reinterpret_cast<void**>(&sl.h_stage), sizeof(void*) * size_t(ntensors)) != cudaSuccess ||
@@ -351,6 +364,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
         for (int f = 0; f < 2; ++f) ctx->grid_acc[dt][f] = grid_for(ctx, blocks_per_sm(0, dt, f));
         for (int md = 0; md < 3; ++md) ctx->grid_uns[dt][md] = grid_for(ctx, blocks_per_sm(1, dt, md));
         ctx->grid_adam[dt] = dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(2, dt, 0));
+        for (int vr = 0; vr < 4; ++vr) ctx->grid_many[dt][vr] = grid_for(ctx, blocks_per_sm(3, dt, vr));
     }
     *out = ctx;
     return TL_OK;
@@ -442,6 +456,77 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
         ctx->n_sum = ctx->phase == kIdle ? n_k : ctx->n_sum + n_k;
     }
     ctx->phase = kUnscaled;
+    return TL_OK;
+}
+
+int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64_t* n, int64_t N, int last,
+                       tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (k < 1 || n == nullptr) return fail(ctx, TL_EINVAL, "need k >= 1 micro-batches and their counts");
+    if (grads == nullptr && ctx->ntensors > 0) return fail(ctx, TL_EINVAL, "grads must not be NULL");
+    if (last != 0 && last != 1) return fail(ctx, TL_EINVAL, "last must be 0 or 1");
+    int rc;
+    int64_t sum = 0;
+    for (int i = 0; i < k; ++i) {
+        if ((rc = check_counts(ctx, n[i], N)) != TL_OK) return rc;
+        sum += n[i];
+        if (sum > N) return fail(ctx, TL_EINVAL, "the counts exceed N");
+    }
+    bool first;
+    if (ctx->phase == kIdle) {
+        first = true;
+    } else if (ctx->phase == kAccum) {
+        first = false;
+        if (N != ctx->N_update) return fail(ctx, TL_EINVAL, "N differs from the N of the open update");
+        if (sum > N - ctx->n_sum) return fail(ctx, TL_EINVAL, "the counts exceed N");
+    } else {
+        return fail(ctx, TL_ESTATE, "an update is past its accumulation phase; finish it with tl_scaler_update");
+    }
+    const int64_t total = (first ? 0 : ctx->n_sum) + sum;
+    if (last && total != N) return fail(ctx, TL_EINVAL, "the counts do not add up to N");
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t nt = ctx->ntensors;
+    const bool by_value = nt <= kInlineMany / kMaxMany;
+    static thread_local GradTableMany inl;
+    // Resolve (and validate) every list before the first launch, so that an
+    // error leaves nothing enqueued.
+    std::vector<const void* const*> tabs(size_t(k), nullptr);
+    std::vector<GradSlot*> slots(size_t(k), nullptr);
+    if (nt > 0) {
+        for (int i = 0; i < k; ++i) {
+            const void* const* gi = grads + int64_t(i) * nt;
+            rc = by_value ? check_grads(ctx, gi) : resolve_device_table(ctx, gi, s, &tabs[i], &slots[i]);
+            if (rc != TL_OK) return rc;
+        }
+    }
+    for (int j = 0; j < k; j += kMaxMany) {
+        const int kk = std::min(kMaxMany, k - j);
+        ManyArgs a{};
+        a.k = kk;
+        a.ntensors = static_cast<int32_t>(nt);
+        for (int i = 0; i < kk; ++i) {
+            a.w[i] = static_cast<float>(static_cast<double>(n[j + i]) / static_cast<double>(N));
+            a.tabs[i] = by_value ? nullptr : tabs[j + i];
+            if (by_value)
+                for (int64_t t = 0; t < nt; ++t) inl.p[int64_t(i) * nt + t] = grads[int64_t(j + i) * nt + t];
+        }
+        const bool f = first && j == 0;
+        const bool l = last && j + kk == k;
+        if (ctx->nchunks > 0) {
+            const int vr = (f ? 1 : 0) | (l ? 2 : 0);
+            cudaError_t e = launch_accum_many(ctx->cfg.grad_dtype, f, l, ctx->d_chunks, ctx->nchunks, ctx->d_tp, inl,
+                                              a, ctx->d_state, ctx->d_partials,
+                                              ctx->grid_many[ctx->cfg.grad_dtype][vr], s);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "many-list accumulate launch");
+            ctx->launches += 1;
+            for (int i = 0; i < kk; ++i) mark_used(slots[j + i], s);
+        }
+    }
+    if (first) ctx->N_update = N;
+    ctx->n_sum = total;
+    ctx->accumulated = true;
+    ctx->phase = last ? kUnscaled : kAccum;
     return TL_OK;
 }
 

@@ -60,6 +60,21 @@ struct GradTable {
     const void* p[kInlineGrads];
 };
 
+// Resident micro-batches read by one launch of the many-list kernel.
+constexpr int kMaxMany = 8;
+constexpr int kInlineMany = 2048;  // k * ntensors gradient pointers travel by value up to this size
+
+struct GradTableMany {
+    const void* p[kInlineMany];     // list-major: p[i * ntensors + tensor]
+};
+
+struct ManyArgs {
+    const void* const* tabs[kMaxMany];  // device pointer tables per list (nullptr: use the by-value table)
+    float w[kMaxMany];                  // micro-batch weights n_i / N
+    int32_t k;                          // micro-batches in this launch (1..kMaxMany)
+    int32_t ntensors;
+};
+
 struct ScalerParams {
     int32_t enabled;
     float growth;
@@ -88,6 +103,9 @@ cudaError_t launch_accumulate(int gdt, bool first, const Chunk* chunks, int64_t 
 cudaError_t launch_unscale(int gdt, int mode, const Chunk* chunks, int64_t nchunks,
                            const TensorPtrs* tp, const GradTable& inl, const void* const* gtab,
                            float w, DevState* st, double* partials, int grid, cudaStream_t s);
+cudaError_t launch_accum_many(int gdt, bool first, bool last, const Chunk* chunks, int64_t nchunks,
+                              const TensorPtrs* tp, const GradTableMany& inl, const ManyArgs& a, DevState* st,
+                              double* partials, int grid, cudaStream_t s);
 cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm,
                         cudaStream_t s);
 cudaError_t launch_adamw(int pdt, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp,
@@ -95,7 +113,8 @@ cudaError_t launch_adamw(int pdt, const Chunk* chunks, int64_t nchunks, const Te
 cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
-// kind: 0 accumulate, 1 unscale, 2 adamw.
+// kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0
+// FIRST, bit 1 LAST).
 int blocks_per_sm(int kind, int dt, int variant);
 
 }  // namespace tl

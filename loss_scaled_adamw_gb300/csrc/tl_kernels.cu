@@ -207,25 +207,104 @@ __device__ __forceinline__ float unscale1(float a, float gj, float w, float inv_
     return __fmul_rn(__fmaf_rn(w, gj, a), inv_s);
 }
 
-__device__ __forceinline__ double sumsq8(const float (&u)[8]) {
-    float q[8];
+// Sum of the fp32 squares fl32(u*u) of one chunk without fp64 arithmetic in the
+// element loop (fp64 throughput is scarce on this part).  Ordinary values
+// (|u| < 2^56: every square is below 2^112, so no fp32 sum over a chunk can
+// overflow) are added into a float-float accumulator (hi, lo) with the
+// error-free TwoSum transformation, so a chunk partial is accurate to about
+// 1e-13 relative and the fp32 norm almost always rounds exactly as an fp64 sum
+// of the same squares does.  (A plain fp32 tree is not enough: it moves the
+// fp32 norm by an ulp, hence the clip coefficient, hence masters close to zero
+// by many ulps.)  A vector holding a larger or infinite value is summed in fp64
+// instead, so the total is infinite exactly when some fp32 square is; NaN
+// propagates through the float-float path.
+struct SumSq {
+    float hi = 0.0f;
+    float lo = 0.0f;
+    double d = 0.0;   // vectors with large values only
+    bool big = false;
+
+    __device__ __forceinline__ void add(float q) {
+        const float s = __fadd_rn(hi, q);
+        const float bb = __fsub_rn(s, hi);
+        const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(q, bb));  // hi + q - s, exactly
+        hi = s;
+        lo = __fadd_rn(lo, err);
+    }
+    __device__ __forceinline__ void vec8(const float (&u)[8]) {
+        float q[8];
+        float mx = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) q[e] = __fmul_rn(u[e], u[e]);
-    const float s = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
-                              __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
-    if (!isinf(s)) return static_cast<double>(s);
+        for (int e = 0; e < 8; ++e) {
+            q[e] = __fmul_rn(u[e], u[e]);
+            mx = fmaxf(mx, fabsf(u[e]));
+        }
+        if (mx >= 72057594037927936.0f) {  // 2^56 (or inf)
+            big = true;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) d = __dadd_rn(d, static_cast<double>(q[e]));
+            return;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) add(q[e]);
+    }
+    __device__ __forceinline__ void one(float u) {
+        const float q = __fmul_rn(u, u);
+        if (fabsf(u) >= 72057594037927936.0f) {
+            big = true;
+            d = __dadd_rn(d, static_cast<double>(q));
+            return;
+        }
+        add(q);
+    }
+};
+
+// Fixed-order block reduction of a chunk's SumSq: a float-float butterfly in each
+// warp (TwoSum gives the same exact error term in both lanes of a pair, so all
+// lanes agree), fp64 only in a warp that saw a large value; thread 0 then adds
+// the warp sums in warp order in fp64.  Returns the partial in thread 0.
+__device__ __forceinline__ double block_sumsq(SumSq acc, float* red_hi, float* red_lo, double* red_d) {
+    float hi = acc.hi, lo = acc.lo;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
+        const float s = __fadd_rn(hi, oh);
+        const float bb = __fsub_rn(s, hi);
+        const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(oh, bb));
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, ol), err);
+    }
     double d = 0.0;
+    if (__any_sync(0xffffffffu, acc.big)) {
+        d = acc.d;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) d = __dadd_rn(d, static_cast<double>(q[e]));
-    return d;
+        for (int o = 16; o > 0; o >>= 1) d = __dadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red_hi[threadIdx.x >> 5] = hi;
+        red_lo[threadIdx.x >> 5] = lo;
+        red_d[threadIdx.x >> 5] = d;
+    }
+    __syncthreads();
+    double total = 0.0;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int k = 0; k < kThreads / 32; ++k)
+            total = __dadd_rn(total, __dadd_rn(__dadd_rn(static_cast<double>(red_hi[k]), static_cast<double>(red_lo[k])),
+                                               red_d[k]));
+    }
+    return total;
 }
 
 template <int GDT, int MODE>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
           const __grid_constant__ GradTable inl, const void* const* __restrict__ gtab, float w,
           DevState* __restrict__ st, double* __restrict__ partials) {
-    __shared__ double red[kThreads / 32];
+    __shared__ float red_hi[kThreads / 32];
+    __shared__ float red_lo[kThreads / 32];
+    __shared__ double red_d[kThreads / 32];
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
     const float inv_s = __fdiv_rn(1.0f, st->S);
     constexpr bool kReadG = MODE != kAccOnly;
@@ -235,7 +314,7 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
         float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
         const void* g = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
         const int len = ch.len;
-        double tsum = 0.0;
+        SumSq sq;
         bool bad = false;
         int done = 0;
         if (aligned16(acc) && (!kReadG || aligned16(g))) {
@@ -258,7 +337,7 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
                         ax[u][e] = unscale1<MODE>(kReadAcc ? ax[u][e] : 0.0f, kReadG ? gx[u][e] : 0.0f, w, inv_s);
                         bad |= !isfinite(ax[u][e]);
                     }
-                    tsum = __dadd_rn(tsum, sumsq8(ax[u]));
+                    sq.vec8(ax[u]);
                 }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
@@ -272,31 +351,109 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
                     ax[e] = unscale1<MODE>(kReadAcc ? ax[e] : 0.0f, kReadG ? gx[e] : 0.0f, w, inv_s);
                     bad |= !isfinite(ax[e]);
                 }
-                tsum = __dadd_rn(tsum, sumsq8(ax));
+                sq.vec8(ax);
+                st8_f32(acc + i * kVec, ax);
+            }
+            done = nv * kVec;
+        }
+        for (int j = done + threadIdx.x; j < len; j += kThreads) {  // tails and misaligned chunks
+            const float u = unscale1<MODE>(kReadAcc ? acc[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g, j) : 0.0f, w, inv_s);
+            acc[j] = u;
+            bad |= !isfinite(u);
+            sq.one(u);
+        }
+        const double part = block_sumsq(sq, red_hi, red_lo, red_d);
+        const int any_bad = __syncthreads_or(bad);
+        if (threadIdx.x == 0) {
+            partials[c] = part;
+            if (any_bad) st->found_inf = 1;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a2 + a3 over resident micro-batches: up to kMaxMany gradient lists read in one
+// pass.  Per element the operations are those of the per-micro-batch kernels in
+// the same order (acc = w_1 g_1, then acc = fma(w_i, g_i, acc), then u = acc/S),
+// so the result is bit-identical; acc is written once (as u when LAST) instead
+// of once per micro-batch.  FIRST: no partial sum in acc yet.  LAST: finish
+// with the unscale, overflow check and squared-norm partial of a3.
+// ---------------------------------------------------------------------------
+template <int GDT, bool FIRST, bool LAST>
+__global__ void __launch_bounds__(kThreads)
+k_accum_many(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
+             const __grid_constant__ GradTableMany inl, const __grid_constant__ ManyArgs a,
+             DevState* __restrict__ st, double* __restrict__ partials) {
+    __shared__ float red_hi[kThreads / 32];
+    __shared__ float red_lo[kThreads / 32];
+    __shared__ double red_d[kThreads / 32];
+    const int kk = a.k;
+    const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
+        const char* g[kMaxMany];
+        bool al = aligned16(acc);
+#pragma unroll
+        for (int i = 0; i < kMaxMany; ++i) {
+            if (i < kk) {
+                const void* base = a.tabs[i] != nullptr ? a.tabs[i][ch.tensor] : inl.p[i * a.ntensors + ch.tensor];
+                g[i] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
+                al = al && aligned16(g[i]);
+            } else {
+                g[i] = nullptr;
+            }
+        }
+        const int len = ch.len;
+        SumSq sq;
+        bool bad = false;
+        int done = 0;
+        if (al) {
+            const int nv = len / kVec;
+            for (int i = threadIdx.x; i < nv; i += kThreads) {
+                float gx[kMaxMany][8];
+#pragma unroll
+                for (int q = 0; q < kMaxMany; ++q)
+                    if (q < kk) Grad<GDT>::ld8(g[q], int64_t(i) * kVec, gx[q]);
+                float ax[8];
+                if (!FIRST) ld8_f32(acc + i * kVec, ax);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float v = FIRST ? __fmul_rn(a.w[0], gx[0][e]) : __fmaf_rn(a.w[0], gx[0][e], ax[e]);
+#pragma unroll
+                    for (int q = 1; q < kMaxMany; ++q)
+                        if (q < kk) v = __fmaf_rn(a.w[q], gx[q][e], v);
+                    if (LAST) {
+                        v = __fmul_rn(v, inv_s);
+                        bad |= !isfinite(v);
+                    }
+                    ax[e] = v;
+                }
+                if (LAST) sq.vec8(ax);
                 st8_f32(acc + i * kVec, ax);
             }
             done = nv * kVec;
         }
         for (int j = done + threadIdx.x; j < len; j += kThreads) {
-            const float u = unscale1<MODE>(kReadAcc ? acc[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g, j) : 0.0f, w, inv_s);
-            acc[j] = u;
-            bad |= !isfinite(u);
-            tsum = __dadd_rn(tsum, static_cast<double>(__fmul_rn(u, u)));
-        }
-        // Fixed-order block reduction: butterfly within each warp, then warp 0's
-        // sums added in warp order by thread 0.
+            float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j)) : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j), acc[j]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tsum = __dadd_rn(tsum, __shfl_xor_sync(0xffffffffu, tsum, o));
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = tsum;
-        const int any_bad = __syncthreads_or(bad);
-        if (threadIdx.x == 0) {
-            double s = 0.0;
-#pragma unroll
-            for (int k = 0; k < kThreads / 32; ++k) s = __dadd_rn(s, red[k]);
-            partials[c] = s;
-            if (any_bad) st->found_inf = 1;
+            for (int q = 1; q < kMaxMany; ++q)
+                if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j), v);
+            if (LAST) {
+                v = __fmul_rn(v, inv_s);
+                bad |= !isfinite(v);
+                sq.one(v);
+            }
+            acc[j] = v;
         }
-        __syncthreads();
+        if (LAST) {
+            const double part = block_sumsq(sq, red_hi, red_lo, red_d);
+            const int any_bad = __syncthreads_or(bad);
+            if (threadIdx.x == 0) {
+                partials[c] = part;
+                if (any_bad) st->found_inf = 1;
+            }
+        }
     }
 }
 
@@ -514,6 +671,24 @@ UnsFn uns_fn(int gdt, int mode) {
     }
 }
 
+using ManyFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, const GradTableMany, const ManyArgs, DevState*,
+                        double*);
+
+template <int GDT>
+ManyFn many_fn_dt(bool first, bool last) {
+    if (first) return last ? k_accum_many<GDT, true, true> : k_accum_many<GDT, true, false>;
+    return last ? k_accum_many<GDT, false, true> : k_accum_many<GDT, false, false>;
+}
+
+ManyFn many_fn(int gdt, bool first, bool last) {
+    switch (gdt) {
+        case kBF16: return many_fn_dt<kBF16>(first, last);
+        case kF16: return many_fn_dt<kF16>(first, last);
+        case kF32: return many_fn_dt<kF32>(first, last);
+        default: return nullptr;
+    }
+}
+
 AdamFn adam_fn(int pdt) {
     switch (pdt) {
         case kBF16: return k_adamw<kBF16>;
@@ -541,6 +716,15 @@ cudaError_t launch_unscale(int gdt, int mode, const Chunk* chunks, int64_t nchun
     return cudaGetLastError();
 }
 
+cudaError_t launch_accum_many(int gdt, bool first, bool last, const Chunk* chunks, int64_t nchunks,
+                              const TensorPtrs* tp, const GradTableMany& inl, const ManyArgs& a, DevState* st,
+                              double* partials, int grid, cudaStream_t s) {
+    ManyFn f = many_fn(gdt, first, last);
+    if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, inl, a, st, partials);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm, cudaStream_t s) {
     k_norm<<<1, kNormThreads, 0, s>>>(partials, nchunks, st, max_norm);
     return cudaGetLastError();
@@ -564,6 +748,7 @@ int blocks_per_sm(int kind, int dt, int variant) {
     if (kind == 0) f = reinterpret_cast<const void*>(acc_fn(dt, variant != 0));
     else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn(dt, variant));
     else if (kind == 2) f = reinterpret_cast<const void*>(adam_fn(dt));
+    else if (kind == 3) f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0));
     if (f == nullptr) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess || n < 1) return 1;

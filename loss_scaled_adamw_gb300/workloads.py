@@ -21,6 +21,8 @@ Workloads (all seeded with 39):
   ragged_100k     100,000 tensors with lognormal sizes (median 512, max 2^20, ~400M total);
                   fp16 params and grads, grads N(0, 1e-2) * S with S = 2^14; k=2; inf in
                   one element of micro-batch 1 at step 2; 3 steps.
+  stream_64m      16 x 4M = 64M parameters, bf16, k=3: a small case of the same kernels for
+                  hardware-counter captures (each list larger than L2).
 Every workload uses AdamW lr 1e-3, betas (0.9, 0.95), eps 1e-8, weight decay 0.1 and
 master weights N(0, 0.02).
 """
@@ -115,6 +117,10 @@ def make(name: str) -> Workload:
         return Workload(name, nm, "f16", "f16", steps=3, k=2, grad_std=1e-2, scaler_enabled=True,
                         init_scale=2.0 ** 14, interval=2000, grads_prescaled=True,
                         injections={(2, 0): [(int(sum(nm) * 0.61803), 0x7C00)]})
+    if name == "stream_64m":
+        # a small case of the 1.24B workload's kernels for counter captures: every list
+        # is larger than the 129 MB L2 while the whole case holds ~1.5 GB of HBM
+        return Workload(name, [1 << 22] * 16, "bf16", "bf16", steps=2, k=3, grad_std=1e-3)
     raise KeyError(name)
 
 

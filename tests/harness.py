@@ -128,11 +128,12 @@ class GpuOptimizer:
         self.grad_lists[slot].load(flat)
         return self.grad_lists[slot].ptrs
 
-    def step(self, grads_flat, counts, hp=None, max_norm=None):
+    def step(self, grads_flat, counts, hp=None, max_norm=None, resident=False):
         hp = hp or W.HP
         mbs = [self.grad_list(i, g) for i, g in enumerate(grads_flat)]
         tl.logical_update(self.ctx, mbs, counts, self.wl.max_norm if max_norm is None else max_norm,
-                          tl.tl_adamw_hp(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"]))
+                          tl.tl_adamw_hp(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"]),
+                          resident=resident)
 
     def status(self):
         return tl.tl_read_status(self.ctx)
@@ -185,9 +186,11 @@ def compare_scalars(st, orc, res, what: str, check_norm=True):
         assert abs(st.coef - res.coef) <= 2e-6 * abs(res.coef), f"{what}: coef {st.coef} vs {res.coef}"
 
 
-def run_parity(wl: W.Workload, gaps=False, device="cuda", steps=None, compare_every=1, hp=None, max_norm=None):
+def run_parity(wl: W.Workload, gaps=False, device="cuda", steps=None, compare_every=1, hp=None, max_norm=None,
+               resident=False):
     """Run `steps` logical updates of a workload on the GPU and in the oracle from the same
-    inputs, comparing scalars after every step and the state every `compare_every` steps."""
+    inputs, comparing scalars after every step and the state every `compare_every` steps.
+    resident=True drives the many-list pass (all k micro-batches read in one pass)."""
     import torch
     master0 = W.master_init(wl, "cpu")
     gpu = GpuOptimizer(wl, master0, gaps=gaps, device=device)
@@ -200,7 +203,7 @@ def run_parity(wl: W.Workload, gaps=False, device="cuda", steps=None, compare_ev
         counts = wl.counts(step)
         S = orc.state.S  # the oracle's loss scale decides how the next gradients are scaled
         grads = [W.grad_input(wl, step, i, scale=S, device="cpu") for i in range(wl.k)]
-        gpu.step(grads, counts, hp=hp, max_norm=mn)
+        gpu.step(grads, counts, hp=hp, max_norm=mn, resident=resident)
         res = orc.step([grad_bits(g) for g in grads], counts, mn, **hp)
         st = gpu.status()
         compare_scalars(st, orc, res, f"{wl.name} step {step}")
