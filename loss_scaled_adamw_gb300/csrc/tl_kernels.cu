@@ -28,6 +28,15 @@
 namespace tl {
 namespace {
 
+// Minimum resident CTAs per SM requested from the compiler (register budget) for
+// the many-list and AdamW kernels.
+#ifndef TL_MINB_MANY
+#define TL_MINB_MANY 3
+#endif
+#ifndef TL_MINB_ADAM
+#define TL_MINB_ADAM 1
+#endif
+
 constexpr int kVec = 8;     // elements per vector access (16 B of a 16-bit stream)
 constexpr int kUnroll = 4;  // vectors in flight per thread in the accumulate/unscale kernels
 constexpr int kUnrollAdam = 2;
@@ -36,16 +45,80 @@ constexpr int kUnrollAdam = 2;
 // 8-element vector access
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void ld8_f32(const float* __restrict__ p, float (&x)[8]) {
+// fp32 streams: 8 elements = 32 bytes per access.  TL_V8 selects one 256-bit
+// access (sm_100+ ld/st.global.v8) instead of two 128-bit ones; TL_LDHINT /
+// TL_STHINT select L1 no-allocate or evict-first (streaming) cache hints.  The
+// defaults (256-bit, L1 no-allocate) were the fastest of the measured variants
+// on every kernel (e.g. clip+AdamW 6.13 -> 6.47 TB/s, first accumulation
+// 5.16 -> 6.16 TB/s at 1.24B parameters).
+#ifndef TL_V8
+#define TL_V8 1
+#endif
+#ifndef TL_LDHINT
+#define TL_LDHINT 1
+#endif
+#ifndef TL_STHINT
+#define TL_STHINT 1
+#endif
+
+#if TL_LDHINT == 1
+#define TL_LD_Q ".L1::no_allocate"
+#elif TL_LDHINT == 2
+#define TL_LD_Q ".cs"
+#else
+#define TL_LD_Q ""
+#endif
+#if TL_STHINT == 1
+#define TL_ST_Q ".L1::no_allocate"
+#elif TL_STHINT == 2
+#define TL_ST_Q ".cs"
+#else
+#define TL_ST_Q ""
+#endif
+
+// `wide` (all fp32 pointers of the chunk 32-byte aligned, checked per chunk)
+// selects the 256-bit form, which needs 32-byte alignment; otherwise two
+// 128-bit accesses, which need 16.
+__device__ __forceinline__ void ld8_f32(const float* __restrict__ p, float (&x)[8], bool wide) {
+#if TL_V8
+    if (wide) {
+        asm volatile("ld.global" TL_LD_Q ".v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7])
+                     : "l"(p));
+        return;
+    }
+#endif
+#if TL_LDHINT != 0
+    asm volatile("ld.global" TL_LD_Q ".v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]) : "l"(p));
+    asm volatile("ld.global" TL_LD_Q ".v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7]) : "l"(p + 4));
+#else
     const float4 a = reinterpret_cast<const float4*>(p)[0];
     const float4 b = reinterpret_cast<const float4*>(p)[1];
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+#endif
 }
 
-__device__ __forceinline__ void st8_f32(float* __restrict__ p, const float (&x)[8]) {
+__device__ __forceinline__ void st8_f32(float* __restrict__ p, const float (&x)[8], bool wide) {
+#if TL_V8
+    if (wide) {
+        asm volatile("st.global" TL_ST_Q ".v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                     :: "l"(p), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7])
+                     : "memory");
+        return;
+    }
+#endif
+#if TL_STHINT != 0
+    asm volatile("st.global" TL_ST_Q ".v4.f32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]) : "memory");
+    asm volatile("st.global" TL_ST_Q ".v4.f32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p + 4), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]) : "memory");
+#else
     reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
     reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+#endif
 }
 
 __device__ __forceinline__ void unpack_bf16x2(uint32_t r, float& lo, float& hi) {
@@ -102,6 +175,45 @@ template <> struct Grad<kF32> {
     }
 };
 
+// Raw 16-byte loads of 8 gradient elements and the exact conversion of element e
+// (for the many-list kernel, which keeps only the raw words live).
+template <int DT> struct GradRaw;
+
+template <> struct GradRaw<kBF16> {
+    using T = uint4;
+    __device__ static __forceinline__ T ld(const void* base, int64_t i) {
+        return __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
+    }
+    __device__ static __forceinline__ float at(const T& r, int e) {
+        const uint32_t w = e < 2 ? r.x : e < 4 ? r.y : e < 6 ? r.z : r.w;
+        return (e & 1) ? __uint_as_float(w & 0xffff0000u) : __uint_as_float(w << 16);
+    }
+};
+
+template <> struct GradRaw<kF16> {
+    using T = uint4;
+    __device__ static __forceinline__ T ld(const void* base, int64_t i) {
+        return __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
+    }
+    __device__ static __forceinline__ float at(const T& r, int e) {
+        const uint32_t w = e < 2 ? r.x : e < 4 ? r.y : e < 6 ? r.z : r.w;
+        return __half2float(__ushort_as_half(static_cast<unsigned short>((e & 1) ? (w >> 16) : (w & 0xffffu))));
+    }
+};
+
+template <> struct GradRaw<kF32> {
+    struct T { float4 a, b; };
+    __device__ static __forceinline__ T ld(const void* base, int64_t i) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+        return T{__ldg(p), __ldg(p + 1)};
+    }
+    __device__ static __forceinline__ float at(const T& r, int e) {
+        const float4& h = e < 4 ? r.a : r.b;
+        const int k = e & 3;
+        return k == 0 ? h.x : k == 1 ? h.y : k == 2 ? h.z : h.w;
+    }
+};
+
 // Model-precision parameter stores: round to nearest even ([MP] section 2, rd16).
 template <int DT> struct Param;
 
@@ -139,6 +251,10 @@ __device__ __forceinline__ bool aligned16(const void* p) {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+__device__ __forceinline__ bool aligned32(const void* p) {
+    return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
+}
+
 // ---------------------------------------------------------------------------
 // a2: accumulate micro-batch i.  [RST] ch. 13 "Weight each mean by the targets
 // it represents"; [MP] section 2 "Gradient accumulation" (no zeroing between
@@ -154,6 +270,7 @@ k_accumulate(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs
         float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
         const void* g = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
         const int len = ch.len;
+        const bool wide = aligned32(acc);
         int done = 0;
         if (aligned16(acc) && aligned16(g)) {
             const int nv = len / kVec;
@@ -164,7 +281,7 @@ k_accumulate(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs
                 for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * kThreads) * kVec, gx[u]);
                 if (!FIRST) {
 #pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
                 }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u)
@@ -172,15 +289,15 @@ k_accumulate(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs
                     for (int e = 0; e < 8; ++e)
                         ax[u][e] = FIRST ? __fmul_rn(w, gx[u][e]) : __fmaf_rn(w, gx[u][e], ax[u][e]);
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
             }
             for (; i < nv; i += kThreads) {
                 float gx[8], ax[8];
                 Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
-                if (!FIRST) ld8_f32(acc + i * kVec, ax);
+                if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ax[e] = FIRST ? __fmul_rn(w, gx[e]) : __fmaf_rn(w, gx[e], ax[e]);
-                st8_f32(acc + i * kVec, ax);
+                st8_f32(acc + i * kVec, ax, wide);
             }
             done = nv * kVec;
         }
@@ -316,6 +433,7 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
         const int len = ch.len;
         SumSq sq;
         bool bad = false;
+        const bool wide = aligned32(acc);
         int done = 0;
         if (aligned16(acc) && (!kReadG || aligned16(g))) {
             const int nv = len / kVec;
@@ -328,7 +446,7 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
                 }
                 if (kReadAcc) {
 #pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
                 }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
@@ -340,19 +458,19 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
                     sq.vec8(ax[u]);
                 }
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u]);
+                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
             }
             for (; i < nv; i += kThreads) {
                 float gx[8], ax[8];
                 if (kReadG) Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
-                if (kReadAcc) ld8_f32(acc + i * kVec, ax);
+                if (kReadAcc) ld8_f32(acc + i * kVec, ax, wide);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     ax[e] = unscale1<MODE>(kReadAcc ? ax[e] : 0.0f, kReadG ? gx[e] : 0.0f, w, inv_s);
                     bad |= !isfinite(ax[e]);
                 }
                 sq.vec8(ax);
-                st8_f32(acc + i * kVec, ax);
+                st8_f32(acc + i * kVec, ax, wide);
             }
             done = nv * kVec;
         }
@@ -380,7 +498,7 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
 // with the unscale, overflow check and squared-norm partial of a3.
 // ---------------------------------------------------------------------------
 template <int GDT, bool FIRST, bool LAST>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, GDT == kF32 ? (TL_MINB_MANY < 2 ? TL_MINB_MANY : 2) : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
              const __grid_constant__ GradTableMany inl, const __grid_constant__ ManyArgs a,
              DevState* __restrict__ st, double* __restrict__ partials) {
@@ -407,30 +525,38 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs
         const int len = ch.len;
         SumSq sq;
         bool bad = false;
+        const bool wide = aligned32(acc);
         int done = 0;
         if (al) {
             const int nv = len / kVec;
             for (int i = threadIdx.x; i < nv; i += kThreads) {
-                float gx[kMaxMany][8];
+                // all kk loads in flight first; each stream's 8 values are unpacked
+                // inside the multiply-add chain (per element still q = 0, 1, ... in order)
+                typename GradRaw<GDT>::T raw[kMaxMany];
 #pragma unroll
                 for (int q = 0; q < kMaxMany; ++q)
-                    if (q < kk) Grad<GDT>::ld8(g[q], int64_t(i) * kVec, gx[q]);
+                    if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q], int64_t(i) * kVec);
                 float ax[8];
-                if (!FIRST) ld8_f32(acc + i * kVec, ax);
+                if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float v = FIRST ? __fmul_rn(a.w[0], gx[0][e]) : __fmaf_rn(a.w[0], gx[0][e], ax[e]);
+                for (int e = 0; e < 8; ++e)
+                    ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
+                                  : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
 #pragma unroll
-                    for (int q = 1; q < kMaxMany; ++q)
-                        if (q < kk) v = __fmaf_rn(a.w[q], gx[q][e], v);
-                    if (LAST) {
-                        v = __fmul_rn(v, inv_s);
-                        bad |= !isfinite(v);
+                for (int q = 1; q < kMaxMany; ++q)
+                    if (q < kk) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
                     }
-                    ax[e] = v;
+                if (LAST) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        ax[e] = __fmul_rn(ax[e], inv_s);
+                        bad |= !isfinite(ax[e]);
+                    }
                 }
                 if (LAST) sq.vec8(ax);
-                st8_f32(acc + i * kVec, ax);
+                st8_f32(acc + i * kVec, ax, wide);
             }
             done = nv * kVec;
         }
@@ -512,7 +638,7 @@ __device__ __forceinline__ void adamw1(float u, float& w, float& m, float& v, co
 }
 
 template <int PDT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, TL_MINB_ADAM)
 k_adamw(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
         DevState* __restrict__ st, AdamHP hp) {
     __shared__ AdamConsts sk;
@@ -550,6 +676,7 @@ k_adamw(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __r
         float* __restrict__ v = t.v + ch.start;
         void* p = static_cast<unsigned short*>(t.param) + ch.start;
         const int len = ch.len;
+        const bool wide = aligned32(u) && aligned32(w) && aligned32(m) && aligned32(v);
         int done = 0;
         if (aligned16(u) && aligned16(w) && aligned16(m) && aligned16(v) && aligned16(p)) {
             const int nv = len / kVec;
@@ -559,34 +686,34 @@ k_adamw(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __r
 #pragma unroll
                 for (int q = 0; q < kUnrollAdam; ++q) {
                     const int o = (i + q * kThreads) * kVec;
-                    ld8_f32(u + o, ux[q]);
-                    ld8_f32(w + o, wx[q]);
-                    ld8_f32(m + o, mx[q]);
-                    ld8_f32(v + o, vx[q]);
+                    ld8_f32(u + o, ux[q], wide);
+                    ld8_f32(w + o, wx[q], wide);
+                    ld8_f32(m + o, mx[q], wide);
+                    ld8_f32(v + o, vx[q], wide);
                 }
 #pragma unroll
                 for (int q = 0; q < kUnrollAdam; ++q) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) adamw1(ux[q][e], wx[q][e], mx[q][e], vx[q][e], k);
                     const int o = (i + q * kThreads) * kVec;
-                    st8_f32(w + o, wx[q]);
-                    st8_f32(m + o, mx[q]);
-                    st8_f32(v + o, vx[q]);
+                    st8_f32(w + o, wx[q], wide);
+                    st8_f32(m + o, mx[q], wide);
+                    st8_f32(v + o, vx[q], wide);
                     st8_param<PDT>(p, o, wx[q]);
                 }
             }
             for (; i < nv; i += kThreads) {
                 float ux[8], wx[8], mx[8], vx[8];
                 const int o = i * kVec;
-                ld8_f32(u + o, ux);
-                ld8_f32(w + o, wx);
-                ld8_f32(m + o, mx);
-                ld8_f32(v + o, vx);
+                ld8_f32(u + o, ux, wide);
+                ld8_f32(w + o, wx, wide);
+                ld8_f32(m + o, mx, wide);
+                ld8_f32(v + o, vx, wide);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) adamw1(ux[e], wx[e], mx[e], vx[e], k);
-                st8_f32(w + o, wx);
-                st8_f32(m + o, mx);
-                st8_f32(v + o, vx);
+                st8_f32(w + o, wx, wide);
+                st8_f32(m + o, mx, wide);
+                st8_f32(v + o, vx, wide);
                 st8_param<PDT>(p, o, wx);
             }
             done = nv * kVec;
