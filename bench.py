@@ -360,52 +360,83 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def run_e2e(args, gw, world):
-    """Same metric through the binding with the k micro-batch gradients copied from pinned
-    host memory every step (on a copy stream, overlapped with the accumulations) and the
-    status read back to the host."""
+    """Same metric through the binding with every step's k micro-batch gradients copied
+    from pinned host memory inside the timed region, and the step's status read back to
+    the host.  Two device sets of gradient buffers alternate between steps, so the copies
+    of step s+1 stream over the host link while step s computes (the link, ~211 GB/s on
+    this box, is the bound: 19.8 GB per step at 1.24B parameters and k = 8)."""
     import torch
     import loss_scaled_adamw_gb300 as tl
     k = gw.wl.k
     host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gw.grads]
     for h, g in zip(host, gw.grads):
         h.copy_(g)
+    sets = [gw.grads, [torch.empty_like(g) for g in gw.grads]]
+    offs = np.cumsum([0] + gw.wl.numel[:-1]).tolist()
+
+    def plist(t):
+        es, base = t.element_size(), t.data_ptr()
+        p = tl.PtrList([base + o * es for o in offs])
+        p.keep = t
+        return p
+
+    many = [gw.many, tl.ManyLists([plist(g) for g in sets[1]])]
     torch.cuda.synchronize()
     copy_stream = torch.cuda.Stream()
     compute = torch.cuda.current_stream()
     h2d = sum(h.numel() * h.element_size() for h in host)
-    status_bytes = 64  # sizeof(tl_status)
+    status_bytes = ctypes_sizeof_status()
+    landed = [None, None]      # copy-done event of each set
+    released = [None, None]    # compute-done-reading event of each set
 
-    def one():
-        evs = []
+    def enqueue_copies(step):
+        b = step % 2
         with torch.cuda.stream(copy_stream):
+            if released[b] is not None:
+                copy_stream.wait_event(released[b])
             for i in range(k):
-                gw.grads[i].copy_(host[i], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(copy_stream)
-                evs.append(e)
-        for i in range(k - 1):
-            compute.wait_event(evs[i])
-            tl.tl_accumulate(gw.ctx, gw.gplists[i], gw.counts[i], gw.N, 1 if i == 0 else 0)
-        compute.wait_event(evs[k - 1])
-        tl.tl_unscale_check(gw.ctx, gw.gplists[k - 1], gw.counts[k - 1], gw.N)
+                sets[b][i].copy_(host[i], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(copy_stream)
+            landed[b] = e
+
+    def compute_step(step):
+        b = step % 2
+        compute.wait_event(landed[b])
+        tl.tl_accumulate_many(gw.ctx, many[b], gw.counts, gw.N, 1)
+        e = torch.cuda.Event()
+        e.record(compute)
+        released[b] = e
         tl.tl_grad_norm(gw.ctx, gw.wl.max_norm)
         tl.tl_clip_adamw_step(gw.ctx, gw.hp)
         tl.tl_scaler_update(gw.ctx)
-        copy_stream.wait_stream(compute)  # the next step's copies overwrite the device grads
-        return tl.tl_read_status(gw.ctx)  # device -> host read of the step's result
 
-    one()
-    torch.cuda.synchronize()
+    def run(nsteps):
+        enqueue_copies(0)
+        for step in range(nsteps):
+            if step + 1 < nsteps:
+                enqueue_copies(step + 1)
+            compute_step(step)
+            tl.tl_read_status(gw.ctx)  # device -> host read of the step's result
+        torch.cuda.synchronize()
+
+    run(2)
     barrier()
     t = time.perf_counter()
-    for _ in range(args.steps):
-        one()
-    torch.cuda.synchronize()
+    run(args.steps)
     el = max_over_ranks(time.perf_counter() - t, gw.device)
     return {"value": whole_job_rate(gw.P, args.steps, world, el), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": status_bytes, "ms_per_step": el / args.steps * 1e3,
-            "how": "grads copied from pinned host memory each step on a copy stream overlapped with the "
-                   "accumulations; status read back each step"}
+            "h2d_gbs": h2d * args.steps / el / 1e9,
+            "how": "every step: the k gradient lists copied from pinned host memory (copy stream, into one of "
+                   "two device buffer sets, overlapping the previous step's compute), the resident pass, "
+                   "norm, clip+AdamW, scaler, and a blocking read of the step's status"}
+
+
+def ctypes_sizeof_status() -> int:
+    import ctypes
+    import loss_scaled_adamw_gb300 as tl
+    return ctypes.sizeof(tl.tl_status)
 
 
 # ---------------------------------------------------------------------------
@@ -425,8 +456,10 @@ def oracle_sample(wl, n_params: int):
     return master, p0, grads
 
 
-def time_oracle(wl, seconds: float, steps: int = 1):
-    """Time the oracle's logical update on a sample sized for about `seconds` of CPU time."""
+def time_oracle(wl, seconds: float, steps=None):
+    """Time the oracle's logical update on a contiguous sample of the workload sized for
+    about `seconds` of CPU time (at most 2^27 parameters, repeated over several logical
+    updates when the cap binds, unless `steps` is given)."""
     import oracle
     n = 1 << 20
     master, p0, grads = oracle_sample(wl, n)
@@ -434,7 +467,9 @@ def time_oracle(wl, seconds: float, steps: int = 1):
     t = time.perf_counter()
     o.step(grads, wl.counts(1), wl.max_norm)
     per_param = (time.perf_counter() - t) / n
-    n = int(min(max(seconds / max(steps, 1) / per_param, 1 << 20), 1 << 27, wl.P))
+    n = int(min(max(seconds / per_param / (steps or 1), 1 << 20), 1 << 27, wl.P))
+    if steps is None:
+        steps = max(1, int(round(seconds / (per_param * n))))
     master, p0, grads = oracle_sample(wl, n)
     o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype)
     t = time.perf_counter()
