@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--path", choices=["resident", "per_microbatch"], default="resident",
                     help="resident: the k micro-batch gradient lists are read in one pass (tl_accumulate_many); "
                          "per_microbatch: one tl_accumulate per micro-batch")
+    ap.add_argument("--layout", choices=["aligned", "misaligned"], default="aligned",
+                    help="tensor placement inside the flat buffers (see GpuWorkload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -191,7 +193,7 @@ class ClockSampler:
 class GpuWorkload:
     """Device-resident tensor lists of a workload, packed into flat buffers."""
 
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, layout="aligned"):
         import torch
         import loss_scaled_adamw_gb300 as tl
         from loss_scaled_adamw_gb300 import workloads as W
@@ -199,14 +201,35 @@ class GpuWorkload:
         P = wl.P
         self.P = P
         self.device = device
-        offs = np.cumsum([0] + wl.numel[:-1]).tolist()
-        assert all(o % 8 == 0 for o in offs)  # every tensor starts on a 16-byte boundary
-        self.master = W.master_init(wl, device)
-        self.param = W.to_16bit(self.master, wl.param_dtype)
-        self.m = torch.zeros(P, dtype=torch.float32, device=device)
-        self.v = torch.zeros(P, dtype=torch.float32, device=device)
-        self.acc = torch.empty(P, dtype=torch.float32, device=device)
-        self.grads = [W.grad_input(wl, 1, i, device=device) for i in range(wl.k)]
+        # tensor offsets inside each flat buffer: "aligned" starts every tensor on a
+        # 32-byte boundary (packed when the sizes allow), "misaligned" puts a seeded 0-3
+        # element gap before every tensor (many start off any 16-byte boundary)
+        offs, total = W.layout_offsets(wl.numel, layout == "misaligned", 8, 0)
+        self.offs, self.total = offs, total
+        gscale = wl.init_scale if wl.grads_prescaled else 1.0
+
+        def spread(flat, dtype):
+            if offs == np.cumsum([0] + wl.numel[:-1]).tolist():
+                return flat
+            buf = torch.zeros(total + 16, dtype=dtype, device=device)
+            n = torch.tensor(wl.numel, dtype=torch.int64)
+            shift = torch.tensor(offs, dtype=torch.int64) - (torch.cumsum(n, 0) - n)
+            idx = torch.arange(P, dtype=torch.int64, device=device) + torch.repeat_interleave(shift.to(device), n.to(device))
+            buf[idx] = flat
+            return buf
+
+        master = W.master_init(wl, device)
+        self.master = spread(master, torch.float32)
+        self.param = spread(W.to_16bit(master, wl.param_dtype), W.to_16bit(master[:1], wl.param_dtype).dtype)
+        del master
+        self.m = torch.zeros(self.master.numel(), dtype=torch.float32, device=device)
+        self.v = torch.zeros_like(self.m)
+        self.acc = torch.empty_like(self.m)
+        self.grads = []
+        for i in range(wl.k):
+            g = W.grad_input(wl, 1, i, scale=gscale, device=device)
+            self.grads.append(spread(g, g.dtype))
+            del g
 
         def plist(t):
             es, base = t.element_size(), t.data_ptr()
@@ -322,7 +345,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     wl = W.make(args.workload)
-    gw = GpuWorkload(wl, device)
+    gw = GpuWorkload(wl, device, args.layout)
     P, k = wl.P, wl.k
     with ClockSampler(gpu_id(local_rank)) as clk:
         head = time_path(args, gw, args.path, world)
@@ -339,9 +362,13 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; random-init masters, N(0,1e-3) bf16 grads)",
         "config": {"workload": f"{wl.name}: ~1.24B-param Llama tensor list, {len(wl.numel)} tensors, P={P}, "
                                f"bf16 params/grads, fp32 master/m/v/acc, k={k} micro-batches"
-                               if wl.name == "llama_1b" else f"{wl.name}: {len(wl.numel)} tensors, P={P}, k={k}",
+                               if wl.name == "llama_1b" else
+                               f"{wl.name}: {len(wl.numel)} tensors, P={P}, {wl.param_dtype} params, "
+                               f"{wl.grad_dtype} grads, k={k}",
                    "P": P, "k": k, "tensors": len(wl.numel), "counts": gw.counts, "path": args.path,
-                   "l2": "no flush: every launch streams >= 7.4 GB, far above the 129 MB L2",
+                   "layout": args.layout,
+                   "l2": ("no flush: every launch streams >= 7.4 GB, far above the 129 MB L2" if P * 6 > 10 * 129e6
+                          else "small case: the working set fits in L2 (launch-latency bound)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm": head["hbm"],
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
@@ -372,7 +399,7 @@ def run_e2e(args, gw, world):
     for h, g in zip(host, gw.grads):
         h.copy_(g)
     sets = [gw.grads, [torch.empty_like(g) for g in gw.grads]]
-    offs = np.cumsum([0] + gw.wl.numel[:-1]).tolist()
+    offs = gw.offs
 
     def plist(t):
         es, base = t.element_size(), t.data_ptr()

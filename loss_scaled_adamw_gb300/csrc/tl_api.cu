@@ -67,16 +67,19 @@ struct tl_ctx {
     int64_t nchunks = 0;
     std::vector<int64_t> numel;
     std::vector<Interval> state_iv;  // sorted intervals of every state tensor
-    Chunk* d_chunks = nullptr;
+    Chunk* d_chunks = nullptr;     // segments
+    int32_t* d_cbegin = nullptr;   // chunk -> first segment (nchunks + 1 entries)
     TensorPtrs* d_tp = nullptr;
     double* d_partials = nullptr;
     DevState* d_state = nullptr;
     GradSlot slots[kGradSlots];
     uint64_t clock = 0;
-    int grid_acc[3][2] = {{0}};
-    int grid_uns[3][3] = {{0}};
-    int grid_adam[3] = {0};
-    int grid_many[3][4] = {{0}};
+    int64_t nbig = 0;              // chunks [0, nbig) are whole-CTA segments, [nbig, nchunks) small-tensor groups
+    // persistent grid sizes per kernel variant, [..][0] for the whole-CTA part, [..][1] for the groups
+    int grid_acc[3][2][2] = {};
+    int grid_uns[3][3][2] = {};
+    int grid_adam[3][2] = {};
+    int grid_many[3][4][2] = {};
     // the update in flight
     int phase = kIdle;
     int64_t n_sum = 0;
@@ -221,16 +224,34 @@ void mark_used(GradSlot* sl, cudaStream_t s) {
         cudaEventRecord(sl->last_use, s);
 }
 
-int grid_for(tl_ctx* ctx, int per_sm) {
+int grid_for(tl_ctx* ctx, int per_sm, int64_t nchunks) {
     int64_t g = int64_t(ctx->sm_count) * per_sm;
-    if (g > ctx->nchunks) g = ctx->nchunks;
+    if (g > nchunks) g = nchunks;
     if (g < 1) g = 1;
     return int(g);
+}
+
+// Launch one streaming operation over the chunk table: the whole-CTA part and
+// the small-tensor groups are separate launches (launch(small, c0, c1)).
+template <typename Launch>
+cudaError_t over_parts(tl_ctx* ctx, Launch launch) {
+    if (ctx->nbig > 0) {
+        cudaError_t e = launch(false, int64_t(0), ctx->nbig);
+        if (e != cudaSuccess) return e;
+        ctx->launches += 1;
+    }
+    if (ctx->nchunks > ctx->nbig) {
+        cudaError_t e = launch(true, ctx->nbig, ctx->nchunks);
+        if (e != cudaSuccess) return e;
+        ctx->launches += 1;
+    }
+    return cudaSuccess;
 }
 
 void free_ctx(tl_ctx* ctx) {
     if (ctx == nullptr) return;
     cudaFree(ctx->d_chunks);
+    cudaFree(ctx->d_cbegin);
     cudaFree(ctx->d_tp);
     cudaFree(ctx->d_partials);
     cudaFree(ctx->d_state);
@@ -309,17 +330,62 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
-    // Chunk table and per-tensor pointers.
-    std::vector<Chunk> chunks;
-    chunks.reserve(size_t(nchunks));
+    // Segments, chunks and per-tensor pointers.  A large tensor becomes one chunk
+    // per kChunk elements; small tensors (<= kSmall elements) are grouped kGroup
+    // to a chunk, one per warp.  Chunks are then ordered by work, largest first
+    // (stable), so every round of the persistent grid gets chunks of similar size.
+    struct ChunkBuild {
+        std::vector<Chunk> segs;
+        int64_t work = 0;
+    };
+    std::vector<ChunkBuild> built;
+    ChunkBuild group;
     std::vector<TensorPtrs> tp(size_t(std::max<int64_t>(ntensors, 1)));
     for (int64_t i = 0; i < ntensors; ++i) {
         tp[i] = TensorPtrs{master[i], m[i], v[i], acc[i], param[i], numel[i]};
-        for (int64_t st = 0; st < numel[i]; st += kChunk)
-            chunks.push_back(Chunk{int32_t(i), int32_t(std::min<int64_t>(kChunk, numel[i] - st)), st});
+        if (numel[i] == 0) continue;
+        if (numel[i] <= kSmall) {
+            group.segs.push_back(Chunk{int32_t(i), int32_t(numel[i]), 0});
+            group.work += numel[i];
+            if (int(group.segs.size()) == kGroup) {
+                built.push_back(std::move(group));
+                group = ChunkBuild();
+            }
+            continue;
+        }
+        for (int64_t st = 0; st < numel[i]; st += kChunk) {
+            ChunkBuild one;
+            const int32_t len = int32_t(std::min<int64_t>(kChunk, numel[i] - st));
+            one.segs.push_back(Chunk{int32_t(i), len, st});
+            one.work = len;
+            built.push_back(std::move(one));
+        }
     }
+    if (!group.segs.empty()) built.push_back(std::move(group));
+    // whole-CTA chunks first, then the groups; each part by work, largest first
+    std::stable_sort(built.begin(), built.end(), [](const ChunkBuild& a, const ChunkBuild& b) {
+        const bool ga = a.segs.size() > 1 || a.segs[0].len <= kSmall;
+        const bool gb = b.segs.size() > 1 || b.segs[0].len <= kSmall;
+        if (ga != gb) return gb;
+        return a.work > b.work;
+    });
+    int64_t nbig = 0;
+    for (const ChunkBuild& cb : built)
+        if (!(cb.segs.size() > 1 || cb.segs[0].len <= kSmall)) ++nbig;
+    std::vector<Chunk> chunks;
+    std::vector<int32_t> cbegin;
+    cbegin.reserve(built.size() + 1);
+    for (const ChunkBuild& cb : built) {
+        cbegin.push_back(int32_t(chunks.size()));
+        chunks.insert(chunks.end(), cb.segs.begin(), cb.segs.end());
+    }
+    cbegin.push_back(int32_t(chunks.size()));
+    nchunks = int64_t(built.size());
+    ctx->nchunks = nchunks;
+    ctx->nbig = nbig;
     const size_t nc_alloc = size_t(std::max<int64_t>(nchunks, 1));
-    if (cudaMalloc(&ctx->d_chunks, sizeof(Chunk) * nc_alloc) != cudaSuccess ||
+    if (cudaMalloc(&ctx->d_chunks, sizeof(Chunk) * std::max<size_t>(chunks.size(), 1)) != cudaSuccess ||
+        cudaMalloc(&ctx->d_cbegin, sizeof(int32_t) * cbegin.size()) != cudaSuccess ||
         cudaMalloc(&ctx->d_tp, sizeof(TensorPtrs) * tp.size()) != cudaSuccess ||
         cudaMalloc(&ctx->d_partials, sizeof(double) * nc_alloc) != cudaSuccess ||
         cudaMalloc(&ctx->d_state, sizeof(DevState)) != cudaSuccess) {
@@ -354,17 +420,25 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && nchunks > 0)
         e = cudaMemcpyAsync(ctx->d_chunks, chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ctx->d_cbegin, cbegin.data(), sizeof(int32_t) * cbegin.size(), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && ntensors > 0)
         e = cudaMemcpyAsync(ctx->d_tp, tp.data(), sizeof(TensorPtrs) * size_t(ntensors), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
     // Persistent grid sizes from the occupancy of each kernel variant.
-    for (int dt = 0; dt < 3; ++dt) {
-        for (int f = 0; f < 2; ++f) ctx->grid_acc[dt][f] = grid_for(ctx, blocks_per_sm(0, dt, f));
-        for (int md = 0; md < 3; ++md) ctx->grid_uns[dt][md] = grid_for(ctx, blocks_per_sm(1, dt, md));
-        ctx->grid_adam[dt] = dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(2, dt, 0));
-        for (int vr = 0; vr < 4; ++vr) ctx->grid_many[dt][vr] = grid_for(ctx, blocks_per_sm(3, dt, vr));
+    for (int part = 0; part < 2; ++part) {
+        const bool small = part == 1;
+        const int64_t n = small ? nchunks - nbig : nbig;
+        for (int dt = 0; dt < 3; ++dt) {
+            for (int f = 0; f < 2; ++f) ctx->grid_acc[dt][f][part] = grid_for(ctx, blocks_per_sm(0, dt, f, small), n);
+            for (int md = 0; md < 3; ++md)
+                ctx->grid_uns[dt][md][part] = grid_for(ctx, blocks_per_sm(1, dt, md, small), n);
+            ctx->grid_adam[dt][part] = dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(2, dt, 0, small), n);
+            for (int vr = 0; vr < 4; ++vr)
+                ctx->grid_many[dt][vr][part] = grid_for(ctx, blocks_per_sm(3, dt, vr, small), n);
+        }
     }
     *out = ctx;
     return TL_OK;
@@ -399,10 +473,12 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
     if (ctx->ntensors > 0 && (rc = resolve_grads(ctx, grads, s, &inl, &dtab, &used)) != TL_OK) return rc;
     const float w = static_cast<float>(static_cast<double>(n_i) / static_cast<double>(N));
     if (ctx->nchunks > 0) {
-        cudaError_t e = launch_accumulate(ctx->cfg.grad_dtype, first != 0, ctx->d_chunks, ctx->nchunks, ctx->d_tp,
-                                          inl, dtab, w, ctx->grid_acc[ctx->cfg.grad_dtype][first], s);
+        const int gdt = ctx->cfg.grad_dtype;
+        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+            return launch_accumulate(gdt, first != 0, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, inl,
+                                     dtab, w, ctx->grid_acc[gdt][first][small ? 1 : 0], s);
+        });
         if (e != cudaSuccess) return cuda_fail(ctx, e, "accumulate launch");
-        ctx->launches += 1;
         mark_used(used, s);
     }
     if (first) {
@@ -445,10 +521,12 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
         return rc;
     const float w = grads == nullptr ? 1.0f : static_cast<float>(static_cast<double>(n_k) / static_cast<double>(N));
     if (ctx->nchunks > 0) {
-        cudaError_t e = launch_unscale(ctx->cfg.grad_dtype, mode, ctx->d_chunks, ctx->nchunks, ctx->d_tp, inl, dtab, w,
-                                       ctx->d_state, ctx->d_partials, ctx->grid_uns[ctx->cfg.grad_dtype][mode], s);
+        const int gdt = ctx->cfg.grad_dtype;
+        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+            return launch_unscale(gdt, mode, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, inl, dtab, w,
+                                  ctx->d_state, ctx->d_partials, ctx->grid_uns[gdt][mode][small ? 1 : 0], s);
+        });
         if (e != cudaSuccess) return cuda_fail(ctx, e, "unscale launch");
-        ctx->launches += 1;
         mark_used(used, s);
     }
     if (grads != nullptr) {
@@ -515,11 +593,12 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
         const bool l = last && j + kk == k;
         if (ctx->nchunks > 0) {
             const int vr = (f ? 1 : 0) | (l ? 2 : 0);
-            cudaError_t e = launch_accum_many(ctx->cfg.grad_dtype, f, l, ctx->d_chunks, ctx->nchunks, ctx->d_tp, inl,
-                                              a, ctx->d_state, ctx->d_partials,
-                                              ctx->grid_many[ctx->cfg.grad_dtype][vr], s);
+            const int gdt = ctx->cfg.grad_dtype;
+            cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, inl, a,
+                                         ctx->d_state, ctx->d_partials, ctx->grid_many[gdt][vr][small ? 1 : 0], s);
+            });
             if (e != cudaSuccess) return cuda_fail(ctx, e, "many-list accumulate launch");
-            ctx->launches += 1;
             for (int i = 0; i < kk; ++i) mark_used(slots[j + i], s);
         }
     }
@@ -553,12 +632,21 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
     int rc;
     if ((rc = check_device(ctx)) != TL_OK) return rc;
     AdamHP h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
-    // Launched even with no elements: its first CTA also computes the beta
-    // powers the scaler kernel commits.
-    cudaError_t e = launch_adamw(ctx->cfg.param_dtype, ctx->d_chunks, ctx->nchunks, ctx->d_tp, ctx->d_state, h,
-                                 ctx->grid_adam[ctx->cfg.param_dtype], static_cast<cudaStream_t>(stream));
+    const int pdt = ctx->cfg.param_dtype;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (ctx->nchunks == 0) {
+        // no elements: still one launch, whose first CTA computes the beta powers
+        // the scaler kernel commits
+        e = launch_adamw(pdt, false, ctx->d_chunks, ctx->d_cbegin, 0, 0, ctx->d_tp, ctx->d_state, h, 1, s);
+        if (e == cudaSuccess) ctx->launches += 1;
+    } else {
+        e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+            return launch_adamw(pdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, ctx->d_state, h,
+                                ctx->grid_adam[pdt][small ? 1 : 0], s);
+        });
+    }
     if (e != cudaSuccess) return cuda_fail(ctx, e, "adamw launch");
-    ctx->launches += 1;
     ctx->phase = kStepped;
     return TL_OK;
 }

@@ -8,12 +8,21 @@
 
 namespace tl {
 
-// Work decomposition (multi-tensor apply).  Every tensor is cut into chunks of
-// at most kChunk elements; a chunk never spans two tensors, so a chunk has one
-// base pointer per list.  CTAs of a persistent grid walk the chunk table with
-// a fixed stride, and every chunk writes its own squared-norm partial, so the
-// reduction order (and the norm) does not depend on the grid size.
+// Work decomposition (multi-tensor apply).  A segment is a piece of one tensor
+// (at most kChunk elements), so it has one base pointer per list.  A chunk is
+// either one segment of a large tensor, worked by a whole CTA, or a group of up
+// to kGroup small tensors (at most kSmall elements each), one per warp.  The
+// whole-CTA chunks come first in the table, then the groups, each part ordered
+// by work, largest first, so that every round of a persistent grid (CTA b takes
+// chunks b, b + G, b + 2G, ...) is balanced; the two parts run as separate
+// launches.  Every chunk writes its own squared-norm partial, so the reduction
+// order (and the norm) does not depend on the grid size.
 constexpr int kChunk = 16384;
+#ifndef TL_SMALL
+#define TL_SMALL 1024
+#endif
+constexpr int kSmall = TL_SMALL;
+constexpr int kGroup = 8;            // = warps per CTA
 constexpr int kThreads = 256;        // streaming kernels: 8 warps per CTA
 constexpr int kNormThreads = 1024;   // the single-CTA second-stage reduce
 constexpr int kInlineGrads = 512;    // gradient pointer tables up to this size travel in the kernel parameters
@@ -33,7 +42,8 @@ struct TensorPtrs {
     int64_t numel;
 };
 
-// One work chunk: elements [start, start + len) of tensor `tensor` (16 bytes).
+// One segment: elements [start, start + len) of tensor `tensor` (16 bytes).
+// Chunk c covers segments [cbegin[c], cbegin[c + 1]).
 struct Chunk {
     int32_t tensor;
     int32_t len;
@@ -95,26 +105,27 @@ enum UnscaleMode : int {
     kAccAndGrad = 2 // u = fma(w, g, acc) / S: the last of several micro-batches
 };
 
-// Launchers (tl_kernels.cu).  `grid` is the persistent grid size; a gtab of
-// nullptr means the pointers are in `inl`.
-cudaError_t launch_accumulate(int gdt, bool first, const Chunk* chunks, int64_t nchunks,
-                              const TensorPtrs* tp, const GradTable& inl, const void* const* gtab,
-                              float w, int grid, cudaStream_t s);
-cudaError_t launch_unscale(int gdt, int mode, const Chunk* chunks, int64_t nchunks,
-                           const TensorPtrs* tp, const GradTable& inl, const void* const* gtab,
-                           float w, DevState* st, double* partials, int grid, cudaStream_t s);
-cudaError_t launch_accum_many(int gdt, bool first, bool last, const Chunk* chunks, int64_t nchunks,
-                              const TensorPtrs* tp, const GradTableMany& inl, const ManyArgs& a, DevState* st,
-                              double* partials, int grid, cudaStream_t s);
-cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm,
-                        cudaStream_t s);
-cudaError_t launch_adamw(int pdt, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp,
-                         DevState* st, AdamHP hp, int grid, cudaStream_t s);
+// Launchers (tl_kernels.cu).  Each streaming launcher covers chunks [c0, c1):
+// small = false for whole-CTA chunks (one segment of a large tensor each),
+// small = true for groups of small tensors (one warp per tensor).  `grid` is
+// the persistent grid size; a gtab of nullptr means the pointers are in `inl`.
+cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+                              int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
+                              int grid, cudaStream_t s);
+cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+                           int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
+                           DevState* st, double* partials, int grid, cudaStream_t s);
+cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
+                              int64_t c0, int64_t c1, const TensorPtrs* tp, const GradTableMany& inl,
+                              const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s);
+cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm, cudaStream_t s);
+cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+                         const TensorPtrs* tp, DevState* st, AdamHP hp, int grid, cudaStream_t s);
 cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0
 // FIRST, bit 1 LAST).
-int blocks_per_sm(int kind, int dt, int variant);
+int blocks_per_sm(int kind, int dt, int variant, bool small);
 
 }  // namespace tl

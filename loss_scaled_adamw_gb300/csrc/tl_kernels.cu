@@ -255,56 +255,70 @@ __device__ __forceinline__ bool aligned32(const void* p) {
     return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
 }
 
+// A chunk is one segment (a piece of one large tensor, worked by the whole CTA:
+// NT = kThreads) or a group of up to kGroup small tensors (one per warp: NT =
+// 32; warps beyond the group idle).  Each kernel's per-segment body is a
+// template on NT, so both forms have compile-time strides.
+
 // ---------------------------------------------------------------------------
 // a2: accumulate micro-batch i.  [RST] ch. 13 "Weight each mean by the targets
 // it represents"; [MP] section 2 "Gradient accumulation" (no zeroing between
 // micro-batches).  acc = w*g (first) or fma(w, g, acc).
 // ---------------------------------------------------------------------------
-template <int GDT, bool FIRST>
+template <int NT, int GDT, bool FIRST>
+__device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
+                                                   const void* const* gp, float w) {
+    float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
+    const void* g = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
+    const int len = ch.len;
+    const bool wide = aligned32(acc);
+    int done = 0;
+    if (aligned16(acc) && aligned16(g)) {
+        const int nv = len / kVec;
+        int i = t;
+        for (; i + (kUnroll - 1) * NT < nv; i += kUnroll * NT) {
+            float gx[kUnroll][8], ax[kUnroll][8];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * NT) * kVec, gx[u]);
+            if (!FIRST) {
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * NT) * kVec, ax[u], wide);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ax[u][e] = FIRST ? __fmul_rn(w, gx[u][e]) : __fmaf_rn(w, gx[u][e], ax[u][e]);
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * NT) * kVec, ax[u], wide);
+        }
+        for (; i < nv; i += NT) {
+            float gx[8], ax[8];
+            Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
+            if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ax[e] = FIRST ? __fmul_rn(w, gx[e]) : __fmaf_rn(w, gx[e], ax[e]);
+            st8_f32(acc + i * kVec, ax, wide);
+        }
+        done = nv * kVec;
+    }
+    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
+        const float gj = Grad<GDT>::ld1(g, j);
+        acc[j] = FIRST ? __fmul_rn(w, gj) : __fmaf_rn(w, gj, acc[j]);
+    }
+}
+
+template <int NT, int GDT, bool FIRST>
 __global__ void __launch_bounds__(kThreads)
-k_accumulate(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
-             const __grid_constant__ GradTable inl, const void* const* __restrict__ gtab, float w) {
+k_accumulate(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+             const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTable inl,
+             const void* const* __restrict__ gtab, float w) {
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        const Chunk ch = chunks[c];
-        float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
-        const void* g = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
-        const int len = ch.len;
-        const bool wide = aligned32(acc);
-        int done = 0;
-        if (aligned16(acc) && aligned16(g)) {
-            const int nv = len / kVec;
-            int i = threadIdx.x;
-            for (; i + (kUnroll - 1) * kThreads < nv; i += kUnroll * kThreads) {
-                float gx[kUnroll][8], ax[kUnroll][8];
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * kThreads) * kVec, gx[u]);
-                if (!FIRST) {
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        ax[u][e] = FIRST ? __fmul_rn(w, gx[u][e]) : __fmaf_rn(w, gx[u][e], ax[u][e]);
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
-            }
-            for (; i < nv; i += kThreads) {
-                float gx[8], ax[8];
-                Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
-                if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ax[e] = FIRST ? __fmul_rn(w, gx[e]) : __fmaf_rn(w, gx[e], ax[e]);
-                st8_f32(acc + i * kVec, ax, wide);
-            }
-            done = nv * kVec;
-        }
-        for (int j = done + threadIdx.x; j < len; j += kThreads) {
-            const float gj = Grad<GDT>::ld1(g, j);
-            acc[j] = FIRST ? __fmul_rn(w, gj) : __fmaf_rn(w, gj, acc[j]);
-        }
+    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+        const int b0 = cbegin[c];
+        const int wi = threadIdx.x >> 5;
+        if (NT == kThreads) accumulate_segment<kThreads, GDT, FIRST>(chunks[b0], threadIdx.x, tp, gp, w);
+        else if (wi < cbegin[c + 1] - b0) accumulate_segment<32, GDT, FIRST>(chunks[b0 + wi], threadIdx.x & 31, tp, gp, w);
     }
 }
 
@@ -414,72 +428,82 @@ __device__ __forceinline__ double block_sumsq(SumSq acc, float* red_hi, float* r
     return total;
 }
 
-template <int GDT, int MODE>
-__global__ void __launch_bounds__(kThreads, 3)
-k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
-          const __grid_constant__ GradTable inl, const void* const* __restrict__ gtab, float w,
-          DevState* __restrict__ st, double* __restrict__ partials) {
+template <int NT, int GDT, int MODE>
+__device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
+                                                const void* const* gp, float w, float inv_s, SumSq& sq,
+                                                bool& bad) {
+    constexpr bool kReadG = MODE != kAccOnly;
+    constexpr bool kReadAcc = MODE != kFirstOnly;
+    float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
+    const void* g = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
+    const int len = ch.len;
+    const bool wide = aligned32(acc);
+    int done = 0;
+    if (aligned16(acc) && (!kReadG || aligned16(g))) {
+        const int nv = len / kVec;
+        int i = t;
+        for (; i + (kUnroll - 1) * NT < nv; i += kUnroll * NT) {
+            float gx[kUnroll][8], ax[kUnroll][8];
+            if (kReadG) {
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * NT) * kVec, gx[u]);
+            }
+            if (kReadAcc) {
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * NT) * kVec, ax[u], wide);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    ax[u][e] = unscale1<MODE>(kReadAcc ? ax[u][e] : 0.0f, kReadG ? gx[u][e] : 0.0f, w, inv_s);
+                    bad |= !isfinite(ax[u][e]);
+                }
+                sq.vec8(ax[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * NT) * kVec, ax[u], wide);
+        }
+        for (; i < nv; i += NT) {
+            float gx[8], ax[8];
+            if (kReadG) Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
+            if (kReadAcc) ld8_f32(acc + i * kVec, ax, wide);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                ax[e] = unscale1<MODE>(kReadAcc ? ax[e] : 0.0f, kReadG ? gx[e] : 0.0f, w, inv_s);
+                bad |= !isfinite(ax[e]);
+            }
+            sq.vec8(ax);
+            st8_f32(acc + i * kVec, ax, wide);
+        }
+        done = nv * kVec;
+    }
+    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
+        const float u = unscale1<MODE>(kReadAcc ? acc[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g, j) : 0.0f, w, inv_s);
+        acc[j] = u;
+        bad |= !isfinite(u);
+        sq.one(u);
+    }
+}
+
+template <int NT, int GDT, int MODE>
+__global__ void __launch_bounds__(kThreads, NT == kThreads && GDT != kF32 ? 3 : 2)
+k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+          const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTable inl,
+          const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials) {
     __shared__ float red_hi[kThreads / 32];
     __shared__ float red_lo[kThreads / 32];
     __shared__ double red_d[kThreads / 32];
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
     const float inv_s = __fdiv_rn(1.0f, st->S);
-    constexpr bool kReadG = MODE != kAccOnly;
-    constexpr bool kReadAcc = MODE != kFirstOnly;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        const Chunk ch = chunks[c];
-        float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
-        const void* g = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
-        const int len = ch.len;
+    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+        const int b0 = cbegin[c];
+        const int wi = threadIdx.x >> 5;
         SumSq sq;
         bool bad = false;
-        const bool wide = aligned32(acc);
-        int done = 0;
-        if (aligned16(acc) && (!kReadG || aligned16(g))) {
-            const int nv = len / kVec;
-            int i = threadIdx.x;
-            for (; i + (kUnroll - 1) * kThreads < nv; i += kUnroll * kThreads) {
-                float gx[kUnroll][8], ax[kUnroll][8];
-                if (kReadG) {
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * kThreads) * kVec, gx[u]);
-                }
-                if (kReadAcc) {
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        ax[u][e] = unscale1<MODE>(kReadAcc ? ax[u][e] : 0.0f, kReadG ? gx[u][e] : 0.0f, w, inv_s);
-                        bad |= !isfinite(ax[u][e]);
-                    }
-                    sq.vec8(ax[u]);
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * kThreads) * kVec, ax[u], wide);
-            }
-            for (; i < nv; i += kThreads) {
-                float gx[8], ax[8];
-                if (kReadG) Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
-                if (kReadAcc) ld8_f32(acc + i * kVec, ax, wide);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ax[e] = unscale1<MODE>(kReadAcc ? ax[e] : 0.0f, kReadG ? gx[e] : 0.0f, w, inv_s);
-                    bad |= !isfinite(ax[e]);
-                }
-                sq.vec8(ax);
-                st8_f32(acc + i * kVec, ax, wide);
-            }
-            done = nv * kVec;
-        }
-        for (int j = done + threadIdx.x; j < len; j += kThreads) {  // tails and misaligned chunks
-            const float u = unscale1<MODE>(kReadAcc ? acc[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g, j) : 0.0f, w, inv_s);
-            acc[j] = u;
-            bad |= !isfinite(u);
-            sq.one(u);
-        }
+        if (NT == kThreads) unscale_segment<kThreads, GDT, MODE>(chunks[b0], threadIdx.x, tp, gp, w, inv_s, sq, bad);
+        else if (wi < cbegin[c + 1] - b0)
+            unscale_segment<32, GDT, MODE>(chunks[b0 + wi], threadIdx.x & 31, tp, gp, w, inv_s, sq, bad);
         const double part = block_sumsq(sq, red_hi, red_lo, red_d);
         const int any_bad = __syncthreads_or(bad);
         if (threadIdx.x == 0) {
@@ -497,81 +521,91 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* _
 // of once per micro-batch.  FIRST: no partial sum in acc yet.  LAST: finish
 // with the unscale, overflow check and squared-norm partial of a3.
 // ---------------------------------------------------------------------------
-template <int GDT, bool FIRST, bool LAST>
-__global__ void __launch_bounds__(kThreads, GDT == kF32 ? (TL_MINB_MANY < 2 ? TL_MINB_MANY : 2) : TL_MINB_MANY)
-k_accum_many(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
-             const __grid_constant__ GradTableMany inl, const __grid_constant__ ManyArgs a,
-             DevState* __restrict__ st, double* __restrict__ partials) {
+template <int NT, int GDT, bool FIRST, bool LAST>
+__device__ __forceinline__ void many_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
+                                             const GradTableMany& inl, const ManyArgs& a, float inv_s, SumSq& sq,
+                                             bool& bad) {
+    const int kk = a.k;
+    float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
+    const char* g[kMaxMany];
+    bool al = aligned16(acc);
+#pragma unroll
+    for (int q = 0; q < kMaxMany; ++q) {
+        if (q < kk) {
+            const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
+            g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
+            al = al && aligned16(g[q]);
+        } else {
+            g[q] = nullptr;
+        }
+    }
+    const int len = ch.len;
+    const bool wide = aligned32(acc);
+    int done = 0;
+    if (al) {
+        const int nv = len / kVec;
+        for (int i = t; i < nv; i += NT) {
+            // all kk loads in flight first; each stream's 8 values are unpacked
+            // inside the multiply-add chain (per element still q = 0, 1, ... in order)
+            typename GradRaw<GDT>::T raw[kMaxMany];
+#pragma unroll
+            for (int q = 0; q < kMaxMany; ++q)
+                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q], int64_t(i) * kVec);
+            float ax[8];
+            if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
+                              : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
+#pragma unroll
+            for (int q = 1; q < kMaxMany; ++q)
+                if (q < kk) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
+                }
+            if (LAST) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    ax[e] = __fmul_rn(ax[e], inv_s);
+                    bad |= !isfinite(ax[e]);
+                }
+                sq.vec8(ax);
+            }
+            st8_f32(acc + i * kVec, ax, wide);
+        }
+        done = nv * kVec;
+    }
+    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
+        float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j)) : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j), acc[j]);
+#pragma unroll
+        for (int q = 1; q < kMaxMany; ++q)
+            if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j), v);
+        if (LAST) {
+            v = __fmul_rn(v, inv_s);
+            bad |= !isfinite(v);
+            sq.one(v);
+        }
+        acc[j] = v;
+    }
+}
+
+template <int NT, int GDT, bool FIRST, bool LAST>
+__global__ void __launch_bounds__(kThreads, NT != kThreads ? 1 : GDT == kF32 ? (TL_MINB_MANY < 2 ? TL_MINB_MANY : 2) : TL_MINB_MANY)
+k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+             const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTableMany inl,
+             const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
     __shared__ float red_hi[kThreads / 32];
     __shared__ float red_lo[kThreads / 32];
     __shared__ double red_d[kThreads / 32];
-    const int kk = a.k;
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        const Chunk ch = chunks[c];
-        float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
-        const char* g[kMaxMany];
-        bool al = aligned16(acc);
-#pragma unroll
-        for (int i = 0; i < kMaxMany; ++i) {
-            if (i < kk) {
-                const void* base = a.tabs[i] != nullptr ? a.tabs[i][ch.tensor] : inl.p[i * a.ntensors + ch.tensor];
-                g[i] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
-                al = al && aligned16(g[i]);
-            } else {
-                g[i] = nullptr;
-            }
-        }
-        const int len = ch.len;
+    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+        const int b0 = cbegin[c];
+        const int wi = threadIdx.x >> 5;
         SumSq sq;
         bool bad = false;
-        const bool wide = aligned32(acc);
-        int done = 0;
-        if (al) {
-            const int nv = len / kVec;
-            for (int i = threadIdx.x; i < nv; i += kThreads) {
-                // all kk loads in flight first; each stream's 8 values are unpacked
-                // inside the multiply-add chain (per element still q = 0, 1, ... in order)
-                typename GradRaw<GDT>::T raw[kMaxMany];
-#pragma unroll
-                for (int q = 0; q < kMaxMany; ++q)
-                    if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q], int64_t(i) * kVec);
-                float ax[8];
-                if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
-                                  : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
-#pragma unroll
-                for (int q = 1; q < kMaxMany; ++q)
-                    if (q < kk) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
-                    }
-                if (LAST) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        ax[e] = __fmul_rn(ax[e], inv_s);
-                        bad |= !isfinite(ax[e]);
-                    }
-                }
-                if (LAST) sq.vec8(ax);
-                st8_f32(acc + i * kVec, ax, wide);
-            }
-            done = nv * kVec;
-        }
-        for (int j = done + threadIdx.x; j < len; j += kThreads) {
-            float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j)) : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j), acc[j]);
-#pragma unroll
-            for (int q = 1; q < kMaxMany; ++q)
-                if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j), v);
-            if (LAST) {
-                v = __fmul_rn(v, inv_s);
-                bad |= !isfinite(v);
-                sq.one(v);
-            }
-            acc[j] = v;
-        }
+        if (NT == kThreads) many_segment<kThreads, GDT, FIRST, LAST>(chunks[b0], threadIdx.x, tp, inl, a, inv_s, sq, bad);
+        else if (wi < cbegin[c + 1] - b0)
+            many_segment<32, GDT, FIRST, LAST>(chunks[b0 + wi], threadIdx.x & 31, tp, inl, a, inv_s, sq, bad);
         if (LAST) {
             const double part = block_sumsq(sq, red_hi, red_lo, red_d);
             const int any_bad = __syncthreads_or(bad);
@@ -637,9 +671,72 @@ __device__ __forceinline__ void adamw1(float u, float& w, float& m, float& v, co
     w = __fsub_rn(wd, __fmul_rn(k.step, __fdiv_rn(m, denom)));
 }
 
-template <int PDT>
+template <int NT, int PDT>
+__device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
+                                              const AdamConsts& k) {
+    const TensorPtrs tpp = tp[ch.tensor];
+    const float* __restrict__ u = tpp.acc + ch.start;
+    float* __restrict__ w = tpp.master + ch.start;
+    float* __restrict__ m = tpp.m + ch.start;
+    float* __restrict__ v = tpp.v + ch.start;
+    void* p = static_cast<unsigned short*>(tpp.param) + ch.start;
+    const int len = ch.len;
+    const bool wide = aligned32(u) && aligned32(w) && aligned32(m) && aligned32(v);
+    int done = 0;
+    if (aligned16(u) && aligned16(w) && aligned16(m) && aligned16(v) && aligned16(p)) {
+        const int nv = len / kVec;
+        int i = t;
+        for (; i + (kUnrollAdam - 1) * NT < nv; i += kUnrollAdam * NT) {
+            float ux[kUnrollAdam][8], wx[kUnrollAdam][8], mx[kUnrollAdam][8], vx[kUnrollAdam][8];
+#pragma unroll
+            for (int q = 0; q < kUnrollAdam; ++q) {
+                const int o = (i + q * NT) * kVec;
+                ld8_f32(u + o, ux[q], wide);
+                ld8_f32(w + o, wx[q], wide);
+                ld8_f32(m + o, mx[q], wide);
+                ld8_f32(v + o, vx[q], wide);
+            }
+#pragma unroll
+            for (int q = 0; q < kUnrollAdam; ++q) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) adamw1(ux[q][e], wx[q][e], mx[q][e], vx[q][e], k);
+                const int o = (i + q * NT) * kVec;
+                st8_f32(w + o, wx[q], wide);
+                st8_f32(m + o, mx[q], wide);
+                st8_f32(v + o, vx[q], wide);
+                st8_param<PDT>(p, o, wx[q]);
+            }
+        }
+        for (; i < nv; i += NT) {
+            float ux[8], wx[8], mx[8], vx[8];
+            const int o = i * kVec;
+            ld8_f32(u + o, ux, wide);
+            ld8_f32(w + o, wx, wide);
+            ld8_f32(m + o, mx, wide);
+            ld8_f32(v + o, vx, wide);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) adamw1(ux[e], wx[e], mx[e], vx[e], k);
+            st8_f32(w + o, wx, wide);
+            st8_f32(m + o, mx, wide);
+            st8_f32(v + o, vx, wide);
+            st8_param<PDT>(p, o, wx);
+        }
+        done = nv * kVec;
+    }
+    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
+        float wj = w[j], mj = m[j], vj = v[j];
+        adamw1(u[j], wj, mj, vj, k);
+        w[j] = wj;
+        m[j] = mj;
+        v[j] = vj;
+        Param<PDT>::st1(p, j, wj);
+    }
+}
+
+template <int NT, int PDT>
 __global__ void __launch_bounds__(kThreads, TL_MINB_ADAM)
-k_adamw(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __restrict__ tp,
+k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+        const TensorPtrs* __restrict__ tp,
         DevState* __restrict__ st, AdamHP hp) {
     __shared__ AdamConsts sk;
     __shared__ int skip;
@@ -667,65 +764,11 @@ k_adamw(const Chunk* __restrict__ chunks, int64_t nchunks, const TensorPtrs* __r
     __syncthreads();
     if (skip) return;
     const AdamConsts k = sk;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        const Chunk ch = chunks[c];
-        const TensorPtrs t = tp[ch.tensor];
-        const float* __restrict__ u = t.acc + ch.start;
-        float* __restrict__ w = t.master + ch.start;
-        float* __restrict__ m = t.m + ch.start;
-        float* __restrict__ v = t.v + ch.start;
-        void* p = static_cast<unsigned short*>(t.param) + ch.start;
-        const int len = ch.len;
-        const bool wide = aligned32(u) && aligned32(w) && aligned32(m) && aligned32(v);
-        int done = 0;
-        if (aligned16(u) && aligned16(w) && aligned16(m) && aligned16(v) && aligned16(p)) {
-            const int nv = len / kVec;
-            int i = threadIdx.x;
-            for (; i + (kUnrollAdam - 1) * kThreads < nv; i += kUnrollAdam * kThreads) {
-                float ux[kUnrollAdam][8], wx[kUnrollAdam][8], mx[kUnrollAdam][8], vx[kUnrollAdam][8];
-#pragma unroll
-                for (int q = 0; q < kUnrollAdam; ++q) {
-                    const int o = (i + q * kThreads) * kVec;
-                    ld8_f32(u + o, ux[q], wide);
-                    ld8_f32(w + o, wx[q], wide);
-                    ld8_f32(m + o, mx[q], wide);
-                    ld8_f32(v + o, vx[q], wide);
-                }
-#pragma unroll
-                for (int q = 0; q < kUnrollAdam; ++q) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) adamw1(ux[q][e], wx[q][e], mx[q][e], vx[q][e], k);
-                    const int o = (i + q * kThreads) * kVec;
-                    st8_f32(w + o, wx[q], wide);
-                    st8_f32(m + o, mx[q], wide);
-                    st8_f32(v + o, vx[q], wide);
-                    st8_param<PDT>(p, o, wx[q]);
-                }
-            }
-            for (; i < nv; i += kThreads) {
-                float ux[8], wx[8], mx[8], vx[8];
-                const int o = i * kVec;
-                ld8_f32(u + o, ux, wide);
-                ld8_f32(w + o, wx, wide);
-                ld8_f32(m + o, mx, wide);
-                ld8_f32(v + o, vx, wide);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) adamw1(ux[e], wx[e], mx[e], vx[e], k);
-                st8_f32(w + o, wx, wide);
-                st8_f32(m + o, mx, wide);
-                st8_f32(v + o, vx, wide);
-                st8_param<PDT>(p, o, wx);
-            }
-            done = nv * kVec;
-        }
-        for (int j = done + threadIdx.x; j < len; j += kThreads) {
-            float wj = w[j], mj = m[j], vj = v[j];
-            adamw1(u[j], wj, mj, vj, k);
-            w[j] = wj;
-            m[j] = mj;
-            v[j] = vj;
-            Param<PDT>::st1(p, j, wj);
-        }
+    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+        const int b0 = cbegin[c];
+        const int wi = threadIdx.x >> 5;
+        if (NT == kThreads) adamw_segment<kThreads, PDT>(chunks[b0], threadIdx.x, tp, k);
+        else if (wi < cbegin[c + 1] - b0) adamw_segment<32, PDT>(chunks[b0 + wi], threadIdx.x & 31, tp, k);
     }
 }
 
@@ -763,92 +806,106 @@ __global__ void k_scaler(DevState* __restrict__ st, ScalerParams sp) {
 }
 
 // ---------------------------------------------------------------------------
-// dispatch tables
+// dispatch tables.  `small` selects the instantiation for small-tensor groups
+// (one warp per tensor) over whole-CTA segments; each has its own register
+// budget.
 // ---------------------------------------------------------------------------
-using AccFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, const GradTable, const void* const*, float);
-using UnsFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, const GradTable, const void* const*, float,
-                       DevState*, double*);
-using AdamFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, DevState*, AdamHP);
+using AccFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, const GradTable,
+                       const void* const*, float);
+using UnsFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, const GradTable,
+                       const void* const*, float, DevState*, double*);
+using ManyFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, const GradTableMany,
+                        const ManyArgs, DevState*, double*);
+using AdamFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, DevState*, AdamHP);
 
-AccFn acc_fn(int gdt, bool first) {
+template <int NT>
+AccFn acc_fn_nt(int gdt, bool first) {
     switch (gdt) {
-        case kBF16: return first ? k_accumulate<kBF16, true> : k_accumulate<kBF16, false>;
-        case kF16: return first ? k_accumulate<kF16, true> : k_accumulate<kF16, false>;
-        case kF32: return first ? k_accumulate<kF32, true> : k_accumulate<kF32, false>;
+        case kBF16: return first ? k_accumulate<NT, kBF16, true> : k_accumulate<NT, kBF16, false>;
+        case kF16: return first ? k_accumulate<NT, kF16, true> : k_accumulate<NT, kF16, false>;
+        case kF32: return first ? k_accumulate<NT, kF32, true> : k_accumulate<NT, kF32, false>;
         default: return nullptr;
     }
 }
 
-template <int GDT>
+AccFn acc_fn(int gdt, bool first, bool small) { return small ? acc_fn_nt<32>(gdt, first) : acc_fn_nt<kThreads>(gdt, first); }
+
+template <int NT, int GDT>
 UnsFn uns_fn_dt(int mode) {
     switch (mode) {
-        case kAccOnly: return k_unscale<GDT, kAccOnly>;
-        case kFirstOnly: return k_unscale<GDT, kFirstOnly>;
-        case kAccAndGrad: return k_unscale<GDT, kAccAndGrad>;
+        case kAccOnly: return k_unscale<NT, GDT, kAccOnly>;
+        case kFirstOnly: return k_unscale<NT, GDT, kFirstOnly>;
+        case kAccAndGrad: return k_unscale<NT, GDT, kAccAndGrad>;
         default: return nullptr;
     }
 }
 
-UnsFn uns_fn(int gdt, int mode) {
+template <int NT>
+UnsFn uns_fn_nt(int gdt, int mode) {
     switch (gdt) {
-        case kBF16: return uns_fn_dt<kBF16>(mode);
-        case kF16: return uns_fn_dt<kF16>(mode);
-        case kF32: return uns_fn_dt<kF32>(mode);
+        case kBF16: return uns_fn_dt<NT, kBF16>(mode);
+        case kF16: return uns_fn_dt<NT, kF16>(mode);
+        case kF32: return uns_fn_dt<NT, kF32>(mode);
         default: return nullptr;
     }
 }
 
-using ManyFn = void (*)(const Chunk*, int64_t, const TensorPtrs*, const GradTableMany, const ManyArgs, DevState*,
-                        double*);
+UnsFn uns_fn(int gdt, int mode, bool small) { return small ? uns_fn_nt<32>(gdt, mode) : uns_fn_nt<kThreads>(gdt, mode); }
 
-template <int GDT>
+template <int NT, int GDT>
 ManyFn many_fn_dt(bool first, bool last) {
-    if (first) return last ? k_accum_many<GDT, true, true> : k_accum_many<GDT, true, false>;
-    return last ? k_accum_many<GDT, false, true> : k_accum_many<GDT, false, false>;
+    if (first) return last ? k_accum_many<NT, GDT, true, true> : k_accum_many<NT, GDT, true, false>;
+    return last ? k_accum_many<NT, GDT, false, true> : k_accum_many<NT, GDT, false, false>;
 }
 
-ManyFn many_fn(int gdt, bool first, bool last) {
+template <int NT>
+ManyFn many_fn_nt(int gdt, bool first, bool last) {
     switch (gdt) {
-        case kBF16: return many_fn_dt<kBF16>(first, last);
-        case kF16: return many_fn_dt<kF16>(first, last);
-        case kF32: return many_fn_dt<kF32>(first, last);
+        case kBF16: return many_fn_dt<NT, kBF16>(first, last);
+        case kF16: return many_fn_dt<NT, kF16>(first, last);
+        case kF32: return many_fn_dt<NT, kF32>(first, last);
         default: return nullptr;
     }
 }
 
-AdamFn adam_fn(int pdt) {
+ManyFn many_fn(int gdt, bool first, bool last, bool small) {
+    return small ? many_fn_nt<32>(gdt, first, last) : many_fn_nt<kThreads>(gdt, first, last);
+}
+
+AdamFn adam_fn(int pdt, bool small) {
     switch (pdt) {
-        case kBF16: return k_adamw<kBF16>;
-        case kF16: return k_adamw<kF16>;
+        case kBF16: return small ? k_adamw<32, kBF16> : k_adamw<kThreads, kBF16>;
+        case kF16: return small ? k_adamw<32, kF16> : k_adamw<kThreads, kF16>;
         default: return nullptr;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_accumulate(int gdt, bool first, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp,
-                              const GradTable& inl, const void* const* gtab, float w, int grid, cudaStream_t s) {
-    AccFn f = acc_fn(gdt, first);
+cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+                              int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
+                              int grid, cudaStream_t s) {
+    AccFn f = acc_fn(gdt, first, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, inl, gtab, w);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, inl, gtab, w);
     return cudaGetLastError();
 }
 
-cudaError_t launch_unscale(int gdt, int mode, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp,
-                           const GradTable& inl, const void* const* gtab, float w, DevState* st,
-                           double* partials, int grid, cudaStream_t s) {
-    UnsFn f = uns_fn(gdt, mode);
+cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+                           int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
+                           DevState* st, double* partials, int grid, cudaStream_t s) {
+    UnsFn f = uns_fn(gdt, mode, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, inl, gtab, w, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, inl, gtab, w, st, partials);
     return cudaGetLastError();
 }
 
-cudaError_t launch_accum_many(int gdt, bool first, bool last, const Chunk* chunks, int64_t nchunks,
-                              const TensorPtrs* tp, const GradTableMany& inl, const ManyArgs& a, DevState* st,
-                              double* partials, int grid, cudaStream_t s) {
-    ManyFn f = many_fn(gdt, first, last);
+cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
+                              int64_t c0, int64_t c1, const TensorPtrs* tp, const GradTableMany& inl,
+                              const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s) {
+    ManyFn f = many_fn(gdt, first, last, small);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, inl, a, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, inl, a, st, partials);
     return cudaGetLastError();
 }
 
@@ -857,11 +914,11 @@ cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, f
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw(int pdt, const Chunk* chunks, int64_t nchunks, const TensorPtrs* tp, DevState* st,
-                         AdamHP hp, int grid, cudaStream_t s) {
-    AdamFn f = adam_fn(pdt);
+cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+                         const TensorPtrs* tp, DevState* st, AdamHP hp, int grid, cudaStream_t s) {
+    AdamFn f = adam_fn(pdt, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, nchunks, tp, st, hp);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, st, hp);
     return cudaGetLastError();
 }
 
@@ -870,12 +927,12 @@ cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-int blocks_per_sm(int kind, int dt, int variant) {
+int blocks_per_sm(int kind, int dt, int variant, bool small) {
     const void* f = nullptr;
-    if (kind == 0) f = reinterpret_cast<const void*>(acc_fn(dt, variant != 0));
-    else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn(dt, variant));
-    else if (kind == 2) f = reinterpret_cast<const void*>(adam_fn(dt));
-    else if (kind == 3) f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0));
+    if (kind == 0) f = reinterpret_cast<const void*>(acc_fn(dt, variant != 0, small));
+    else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn(dt, variant, small));
+    else if (kind == 2) f = reinterpret_cast<const void*>(adam_fn(dt, small));
+    else if (kind == 3) f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0, small));
     if (f == nullptr) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess || n < 1) return 1;
