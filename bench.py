@@ -52,6 +52,7 @@ def parse_args(argv=None):
                          "per_microbatch: one tl_accumulate per micro-batch")
     ap.add_argument("--layout", choices=["aligned", "misaligned"], default="aligned",
                     help="tensor placement inside the flat buffers (see GpuWorkload)")
+    ap.add_argument("--graph", action="store_true", help="also time both sequences replayed from a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -287,6 +288,38 @@ class GpuWorkload:
                 events.append((name, a, b))
 
 
+def time_graph(args, gw, path, world):
+    """K steps of one path replayed from a CUDA graph captured once (the update has no
+    host synchronisation, so the whole step captures): no per-call host overhead."""
+    import torch
+    import loss_scaled_adamw_gb300 as tl
+    for _ in range(max(args.warmup, 1)):
+        gw.step(path)  # also uploads any device pointer tables before capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    launches0 = tl.tl_launch_count(gw.ctx)
+    with torch.cuda.graph(g, stream=s):
+        gw.step(path)
+    per_step = tl.tl_launch_count(gw.ctx) - launches0
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    el = max_over_ranks(t0.elapsed_time(t1) / 1e3, gw.device)
+    return {"value": whole_job_rate(gw.P, args.steps, world, el), "ms_per_step": el / args.steps * 1e3,
+            "launches_per_step": per_step}
+
+
 def time_path(args, gw, path, world):
     """K timed steps of one path (after W warm-up steps), with per-kernel events."""
     import torch
@@ -351,6 +384,7 @@ def run_gpu(args, rank, world, local_rank):
         head = time_path(args, gw, args.path, world)
         other_name = "per_microbatch" if args.path == "resident" else "resident"
         other = time_path(args, gw, other_name, world)
+        graphs = {p: time_graph(args, gw, p, world) for p in (args.path, other_name)} if args.graph else None
         e2e = None if args.no_e2e else run_e2e(args, gw, world)
     st = tl.tl_read_status(gw.ctx)
     kernels = head["kernels"]
@@ -379,6 +413,7 @@ def run_gpu(args, rank, world, local_rank):
         "paths": {args.path: {k2: head[k2] for k2 in ("value", "ms_per_step", "hbm")},
                   other_name: {k2: other[k2] for k2 in ("value", "ms_per_step", "hbm", "kernels")}},
         "clocks": clk.summary(),
+        **({"cuda_graph": graphs} if graphs else {}),
         "status": {"S": st.S, "t": st.t, "skipped": st.skipped, "norm": st.norm},
     }
     if e2e is not None:

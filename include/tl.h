@@ -235,6 +235,14 @@ int tl_set_state(tl_ctx* ctx, const tl_state* in, tl_stream stream);
  * Valid until tl_destroy. */
 const float* tl_scale_ptr(const tl_ctx* ctx);
 
+/* The backward seed of micro-batch i: S * n_i / N in fp32, written by the device
+ * to out (one float of device memory) at the point of the stream where it runs,
+ * so the loss can be seeded without a host read of S ([RST] ch. 13 "Weight each
+ * mean by the targets it represents": reverse mode is seeded with S * n_i / N;
+ * [MP] section 4: scale(loss) = loss * S).  With S a power of two the value is
+ * exactly S * fl32(n_i / N).  Errors: TL_EINVAL (counts, out NULL). */
+int tl_loss_seed(tl_ctx* ctx, int64_t n_i, int64_t N, float* out, tl_stream stream);
+
 /* Sizes of the context: total elements and work chunks. */
 int64_t tl_num_params(const tl_ctx* ctx);
 int64_t tl_num_chunks(const tl_ctx* ctx);

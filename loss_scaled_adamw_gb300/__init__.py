@@ -32,7 +32,7 @@ TL_F32, TL_BF16, TL_F16 = 0, 1, 2
 EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "tl_unscale_check", "tl_grad_norm",
             "tl_clip_adamw_step", "tl_scaler_update", "tl_read_status", "tl_get_state", "tl_set_state",
             "tl_scale_ptr", "tl_num_params", "tl_num_chunks", "tl_launch_count", "tl_status_string",
-            "tl_last_error", "tl_unscale_norm_noalloc")
+            "tl_last_error", "tl_unscale_norm_noalloc", "tl_loss_seed")
 
 
 class TLError(RuntimeError):
@@ -123,6 +123,7 @@ def load_library():
         "tl_status_string": (ctypes.c_char_p, [i32]),
         "tl_last_error": (ctypes.c_char_p, [vp]),
         "tl_unscale_norm_noalloc": (i32, [i64, ctypes.POINTER(i64), pp, f32, f32, vp, vp]),
+        "tl_loss_seed": (i32, [vp, i64, i64, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -275,6 +276,12 @@ def tl_set_state(ctx: Context, state: tl_state, stream=None) -> None:
 
 def tl_scale_ptr(ctx: Context) -> int:
     return int(load_library().tl_scale_ptr(ctx.handle) or 0)
+
+
+def tl_loss_seed(ctx: Context, n_i: int, N: int, out_addr: int, stream=None) -> None:
+    """Write S * n_i / N (fp32) to the device address out_addr on the stream."""
+    _check(ctx, "tl_loss_seed", load_library().tl_loss_seed(ctx.handle, int(n_i), int(N),
+                                                            ctypes.c_void_p(int(out_addr)), _stream(stream)))
 
 
 def tl_num_params(ctx: Context) -> int:

@@ -738,6 +738,19 @@ int tl_set_state(tl_ctx* ctx, const tl_state* in, tl_stream stream) {
     return TL_OK;
 }
 
+int tl_loss_seed(tl_ctx* ctx, int64_t n_i, int64_t N, float* out, tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 3u) != 0) return fail(ctx, TL_EINVAL, "out must be a 4-byte aligned device address");
+    int rc;
+    if ((rc = check_counts(ctx, n_i, N)) != TL_OK) return rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    const float w = static_cast<float>(static_cast<double>(n_i) / static_cast<double>(N));
+    cudaError_t e = launch_seed(ctx->d_state, w, out, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "seed launch");
+    ctx->launches += 1;
+    return TL_OK;
+}
+
 const float* tl_scale_ptr(const tl_ctx* ctx) {
     return ctx == nullptr ? nullptr : &ctx->d_state->S;
 }

@@ -122,6 +122,7 @@ cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, f
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
                          const TensorPtrs* tp, DevState* st, AdamHP hp, int grid, cudaStream_t s);
 cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);
+cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s);
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0

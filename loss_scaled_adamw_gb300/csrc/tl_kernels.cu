@@ -806,6 +806,14 @@ __global__ void k_scaler(DevState* __restrict__ st, ScalerParams sp) {
 }
 
 // ---------------------------------------------------------------------------
+// The backward seed S * w_i of a micro-batch ([RST] ch. 13: reverse mode seeded
+// with S * n_i / N), read from the device scale at its point in the stream.
+// ---------------------------------------------------------------------------
+__global__ void k_seed(const DevState* __restrict__ st, float w, float* __restrict__ out) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) out[0] = __fmul_rn(st->S, w);
+}
+
+// ---------------------------------------------------------------------------
 // dispatch tables.  `small` selects the instantiation for small-tensor groups
 // (one warp per tensor) over whole-CTA segments; each has its own register
 // budget.
@@ -924,6 +932,11 @@ cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t
 
 cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s) {
     k_scaler<<<1, 32, 0, s>>>(st, sp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s) {
+    k_seed<<<1, 32, 0, s>>>(st, w, out);
     return cudaGetLastError();
 }
 

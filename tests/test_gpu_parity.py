@@ -332,6 +332,90 @@ def test_scale_pointer_tracks_the_device_scale():
     assert gpu.status().S == 4.0
 
 
+def test_loss_seed_follows_the_device_scale():
+    """[RST] ch. 13: reverse mode seeded with S * n_i / N (at S = 128, 85.33333333333333 and
+    42.666666666666664 for the shares 6/9 and 3/9; here in fp32); after an overflowing update
+    the seed halves with S, with no host read of S."""
+    wl = custom([64], pdtype="f16", gdtype="f16", k=2, steps=1, counts=[6, 3], scaler=True, init_scale=128.0,
+                interval=1000)
+    gpu = GpuOptimizer(wl, W.master_init(wl))
+    out = torch.zeros(2, dtype=torch.float32, device="cuda")
+    tl.tl_loss_seed(gpu.ctx, 6, 9, out.data_ptr())
+    tl.tl_loss_seed(gpu.ctx, 3, 9, out.data_ptr() + 4)
+    torch.cuda.synchronize()
+    assert out[0].item() == np.float32(85.33333333333333) and out[1].item() == np.float32(42.666666666666664)
+    bad = W.grad_input(wl, 1, 0, scale=128.0)
+    bad.view(torch.int16)[0] = 0x7C00
+    gb = gpu.grad_list(0, bad)
+    tl.logical_update(gpu.ctx, [gb, gb], [6, 3], 1.0, tl.tl_adamw_hp(**W.HP))
+    tl.tl_loss_seed(gpu.ctx, 6, 9, out.data_ptr())
+    torch.cuda.synchronize()
+    assert out[0].item() == np.float32(85.33333333333333) / 2
+    with pytest.raises(tl.TLError) as ei:
+        tl.tl_loss_seed(gpu.ctx, 0, 9, out.data_ptr())
+    assert ei.value.status == tl.TL_EINVAL
+
+
+def test_single_tensor_beyond_2_pow_31_full():
+    """Maximum-size edge case: one tensor of 2^31 + 77 elements (64-bit chunk offsets)
+    next to a 5-element one.  Sampled elements at the start, around element 2^31 and at
+    the end against the oracle, one by one; the norm against the fp64 sum of the fp32
+    squares computed on the device by torch."""
+    import oracle
+    n0 = (1 << 31) + 77
+    numel = [n0, 5]
+    off1 = (n0 + 7) // 8 * 8
+    total = off1 + 8
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    master = torch.randn(total, generator=gen, device="cuda") * 0.02
+    param = master.to(torch.bfloat16)
+    m = torch.zeros(total, device="cuda")
+    v = torch.zeros(total, device="cuda")
+    acc = torch.empty(total, device="cuda")
+    grads = (torch.randn(total, generator=gen, device="cuda") * 1e-2).to(torch.bfloat16)
+
+    def plist(t):
+        es = t.element_size()
+        p = tl.PtrList([t.data_ptr(), t.data_ptr() + off1 * es])
+        p.keep = t
+        return p
+
+    flat_idx = np.concatenate([np.arange(0, 100), np.arange((1 << 31) - 50, (1 << 31) + 50),
+                               np.arange(n0 - 100, n0), off1 + np.arange(5)])
+    it = torch.from_numpy(flat_idx).cuda()
+    w0 = master[it].cpu().numpy()
+    gbits = grads[it].cpu().view(torch.int16).numpy().view(np.uint16)
+    cfg = tl.make_config(tl.TL_BF16, tl.TL_BF16)
+    ctx = tl.tl_create(numel, plist(param), plist(master), plist(m), plist(v), plist(acc), cfg)
+    gl = plist(grads)
+    tl.logical_update(ctx, [gl], [7], 0.0, tl.tl_adamw_hp(**W.HP))
+    st = tl.tl_read_status(ctx)
+    assert st.t == 1 and st.skipped == 0 and st.coef == 1.0
+    gf = torch.cat([grads[:n0], grads[off1:off1 + 5]]).float()
+    ref = float((gf * gf).double().sum())
+    del gf
+    assert abs(st.sumsq - ref) <= 1e-9 * ref and abs(st.norm - math.sqrt(ref)) <= 1e-6 * math.sqrt(ref)
+    lib = oracle.load()
+    n = flat_idx.size
+    P_ = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    u = np.empty(n, np.float32)
+    lib.tlo_accumulate(P_(u), P_(np.ascontiguousarray(gbits)), oracle.DT_BF16, n, lib.tlo_microbatch_weight(7, 7), 1)
+    lib.tlo_unscale_check(P_(u), n, 1.0)
+    hp = oracle.AdamWHP(**W.HP)
+    sc = lib.tlo_adamw_prepare(ctypes.byref(hp), float(np.float32(0.9)), float(np.float32(0.95)))
+    w = w0.astype(np.float32).copy()
+    mo = np.zeros(n, np.float32)
+    vo = np.zeros(n, np.float32)
+    po = np.empty(n, np.uint16)
+    lib.tlo_adamw_recast(P_(w), P_(mo), P_(vo), P_(po), oracle.DT_BF16, P_(u), n, lib.tlo_clip_coef(st.norm, 0.0),
+                         ctypes.byref(sc))
+    torch.cuda.synchronize()
+    assert_ulps32(master[it].cpu().numpy(), w, 2, "2^31 master")
+    assert_ulps32(m[it].cpu().numpy(), mo, 2, "2^31 m")
+    assert_ulps32(v[it].cpu().numpy(), vo, 2, "2^31 v")
+    assert_ulps16(param[it].cpu().view(torch.int16).numpy().view(np.uint16), po, 1, "2^31 param")
+
+
 # ---------------------------------------------------------------------------
 # the full-size workloads
 # ---------------------------------------------------------------------------
