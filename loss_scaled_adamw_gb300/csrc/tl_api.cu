@@ -71,6 +71,7 @@ struct tl_ctx {
     int32_t* d_cbegin = nullptr;   // chunk -> first segment (nchunks + 1 entries)
     TensorPtrs* d_tp = nullptr;
     double* d_partials = nullptr;
+    double* d_norm_slots = nullptr;  // one per CTA of the second-stage reduce
     DevState* d_state = nullptr;
     GradSlot slots[kGradSlots];
     uint64_t clock = 0;
@@ -254,6 +255,7 @@ void free_ctx(tl_ctx* ctx) {
     cudaFree(ctx->d_cbegin);
     cudaFree(ctx->d_tp);
     cudaFree(ctx->d_partials);
+    cudaFree(ctx->d_norm_slots);
     cudaFree(ctx->d_state);
     for (GradSlot& sl : ctx->slots) {
         cudaFree(sl.d_tab);
@@ -387,7 +389,8 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     if (cudaMalloc(&ctx->d_chunks, sizeof(Chunk) * std::max<size_t>(chunks.size(), 1)) != cudaSuccess ||
         cudaMalloc(&ctx->d_cbegin, sizeof(int32_t) * cbegin.size()) != cudaSuccess ||
         cudaMalloc(&ctx->d_tp, sizeof(TensorPtrs) * tp.size()) != cudaSuccess ||
-        cudaMalloc(&ctx->d_partials, sizeof(double) * nc_alloc) != cudaSuccess ||
+        cudaMalloc(&ctx->d_partials, sizeof(double) * nc_alloc * kGroup) != cudaSuccess ||
+        cudaMalloc(&ctx->d_norm_slots, sizeof(double) * kNormBlocks) != cudaSuccess ||
         cudaMalloc(&ctx->d_state, sizeof(DevState)) != cudaSuccess) {
         cudaGetLastError();
         free_ctx(ctx);
@@ -417,6 +420,8 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     ds.sumsq = 0.0;
     ds.b1p_next = 1.0;
     ds.b2p_next = 1.0;
+    ds.norm_ticket = 0;
+    ds.pad = 0;
     e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && nchunks > 0)
         e = cudaMemcpyAsync(ctx->d_chunks, chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice, s);
@@ -615,7 +620,8 @@ int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream) {
     if (std::isnan(max_norm)) return fail(ctx, TL_EINVAL, "max_norm is NaN");
     int rc;
     if ((rc = check_device(ctx)) != TL_OK) return rc;
-    cudaError_t e = launch_norm(ctx->d_partials, ctx->nchunks, ctx->d_state, max_norm, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_norm(ctx->d_partials, ctx->nchunks * kGroup, ctx->d_norm_slots, ctx->d_state, max_norm,
+                                static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(ctx, e, "norm launch");
     ctx->launches += 1;
     ctx->phase = kNormed;

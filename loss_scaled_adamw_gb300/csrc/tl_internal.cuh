@@ -24,7 +24,8 @@ constexpr int kChunk = 16384;
 constexpr int kSmall = TL_SMALL;
 constexpr int kGroup = 8;            // = warps per CTA
 constexpr int kThreads = 256;        // streaming kernels: 8 warps per CTA
-constexpr int kNormThreads = 1024;   // the single-CTA second-stage reduce
+constexpr int kNormThreads = 256;    // threads per CTA of the second-stage reduce
+constexpr int kNormBlocks = 128;     // CTAs of the second-stage reduce: fixed, so its order is device-independent
 constexpr int kInlineGrads = 512;    // gradient pointer tables up to this size travel in the kernel parameters
 
 // Element types (values of TL_F32 / TL_BF16 / TL_F16 in include/tl.h).
@@ -63,6 +64,8 @@ struct DevState {
     double sumsq;         // squared norm (fp64)
     double b1p_next;      // beta powers of the update in flight (committed by the scaler kernel)
     double b2p_next;
+    uint32_t norm_ticket; // CTAs of the second-stage reduce that have finished, modulo 2^32
+    uint32_t pad;
 };
 
 // Gradient pointers passed by value (kernel parameter space).
@@ -118,7 +121,8 @@ cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, c
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
                               int64_t c0, int64_t c1, const TensorPtrs* tp, const GradTableMany& inl,
                               const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s);
-cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm, cudaStream_t s);
+cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevState* st, float max_norm,
+                        cudaStream_t s);
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
                          const TensorPtrs* tp, DevState* st, AdamHP hp, int grid, cudaStream_t s);
 cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);

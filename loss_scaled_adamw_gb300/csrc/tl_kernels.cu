@@ -390,11 +390,13 @@ struct SumSq {
     }
 };
 
-// Fixed-order block reduction of a chunk's SumSq: a float-float butterfly in each
-// warp (TwoSum gives the same exact error term in both lanes of a pair, so all
-// lanes agree), fp64 only in a warp that saw a large value; thread 0 then adds
-// the warp sums in warp order in fp64.  Returns the partial in thread 0.
-__device__ __forceinline__ double block_sumsq(SumSq acc, float* red_hi, float* red_lo, double* red_d) {
+// Fixed-order reduction of a SumSq within a warp: a float-float butterfly
+// (TwoSum gives the same exact error term in both lanes of a pair, so every lane
+// ends with the same value), fp64 only in a warp that saw a large value.  Each
+// warp writes its own partial (kGroup partials per chunk), so finishing a chunk
+// needs no block barrier; the partial of warp w of chunk c is always the same
+// elements' sum, whatever the grid.
+__device__ __forceinline__ double warp_sumsq(const SumSq& acc) {
     float hi = acc.hi, lo = acc.lo;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -412,20 +414,18 @@ __device__ __forceinline__ double block_sumsq(SumSq acc, float* red_hi, float* r
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) d = __dadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
     }
+    return __dadd_rn(__dadd_rn(static_cast<double>(hi), static_cast<double>(lo)), d);
+}
+
+// Write warp w's partial of chunk c and raise the overflow flag if any lane saw a
+// non-finite value.
+__device__ __forceinline__ void finish_warp(const SumSq& sq, bool bad, int64_t c, DevState* st, double* partials) {
+    const double part = warp_sumsq(sq);
+    const bool any_bad = __any_sync(0xffffffffu, bad);
     if ((threadIdx.x & 31) == 0) {
-        red_hi[threadIdx.x >> 5] = hi;
-        red_lo[threadIdx.x >> 5] = lo;
-        red_d[threadIdx.x >> 5] = d;
+        partials[c * kGroup + (threadIdx.x >> 5)] = part;
+        if (any_bad) st->found_inf = 1;
     }
-    __syncthreads();
-    double total = 0.0;
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int k = 0; k < kThreads / 32; ++k)
-            total = __dadd_rn(total, __dadd_rn(__dadd_rn(static_cast<double>(red_hi[k]), static_cast<double>(red_lo[k])),
-                                               red_d[k]));
-    }
-    return total;
 }
 
 template <int NT, int GDT, int MODE>
@@ -491,9 +491,6 @@ __global__ void __launch_bounds__(kThreads, NT == kThreads && GDT != kF32 ? 3 : 
 k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
           const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTable inl,
           const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials) {
-    __shared__ float red_hi[kThreads / 32];
-    __shared__ float red_lo[kThreads / 32];
-    __shared__ double red_d[kThreads / 32];
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
     const float inv_s = __fdiv_rn(1.0f, st->S);
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
@@ -504,12 +501,7 @@ k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, 
         if (NT == kThreads) unscale_segment<kThreads, GDT, MODE>(chunks[b0], threadIdx.x, tp, gp, w, inv_s, sq, bad);
         else if (wi < cbegin[c + 1] - b0)
             unscale_segment<32, GDT, MODE>(chunks[b0 + wi], threadIdx.x & 31, tp, gp, w, inv_s, sq, bad);
-        const double part = block_sumsq(sq, red_hi, red_lo, red_d);
-        const int any_bad = __syncthreads_or(bad);
-        if (threadIdx.x == 0) {
-            partials[c] = part;
-            if (any_bad) st->found_inf = 1;
-        }
+        finish_warp(sq, bad, c, st, partials);
     }
 }
 
@@ -594,9 +586,6 @@ __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1 : GDT == kF32 ? (
 k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
              const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTableMany inl,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
-    __shared__ float red_hi[kThreads / 32];
-    __shared__ float red_lo[kThreads / 32];
-    __shared__ double red_d[kThreads / 32];
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         const int b0 = cbegin[c];
@@ -606,48 +595,78 @@ k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegi
         if (NT == kThreads) many_segment<kThreads, GDT, FIRST, LAST>(chunks[b0], threadIdx.x, tp, inl, a, inv_s, sq, bad);
         else if (wi < cbegin[c + 1] - b0)
             many_segment<32, GDT, FIRST, LAST>(chunks[b0 + wi], threadIdx.x & 31, tp, inl, a, inv_s, sq, bad);
-        if (LAST) {
-            const double part = block_sumsq(sq, red_hi, red_lo, red_d);
-            const int any_bad = __syncthreads_or(bad);
-            if (threadIdx.x == 0) {
-                partials[c] = part;
-                if (any_bad) st->found_inf = 1;
-            }
-        }
+        if (LAST) finish_warp(sq, bad, c, st, partials);
     }
 }
 
 // ---------------------------------------------------------------------------
 // a4: deterministic second stage.  [MEG] section 9: global_norm =
 // sqrt(sum ||g||^2), clip_coef = max_norm / (global_norm + eps), applied only
-// below 1 (eps = 1e-6).  One CTA: thread t adds partials t, t+1024, ... in
-// order, then a fixed butterfly and a fixed warp-order sum.
+// below 1 (eps = 1e-6).  kNormBlocks CTAs each reduce a fixed contiguous range
+// of the per-warp partials (per thread eight interleaved accumulators, then a
+// fixed butterfly and a fixed warp-order sum) into one slot.  Each CTA then
+// takes a ticket; the CTA holding the last ticket of the launch adds the slots
+// in slot order and finishes.  Nothing waits: the last CTA only runs after every
+// other CTA has published its slot.  The ticket counter is never reset; the
+// launch's last ticket is the one that is kNormBlocks - 1 modulo kNormBlocks.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kNormThreads)
-k_norm(const double* __restrict__ partials, int64_t n, DevState* __restrict__ st, float max_norm) {
-    __shared__ double red[kNormThreads / 32];
-    double s = 0.0;
-    for (int64_t i = threadIdx.x; i < n; i += kNormThreads) s = __dadd_rn(s, partials[i]);
+__device__ __forceinline__ double block_sum(double s, double* red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        double v = red[threadIdx.x];
+    double t = 0.0;
+    if (threadIdx.x == 0) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (threadIdx.x == 0) {
-            st->sumsq = v;
-            if (!isfinite(v)) st->found_inf = 1;   // an fp32 square overflowed: treated as an overflow
-            const float norm = __double2float_rn(__dsqrt_rn(v));
-            st->norm = norm;
-            float coef = 1.0f;
-            if (max_norm > 0.0f) {
-                const float cc = __fdiv_rn(max_norm, __fadd_rn(norm, 1e-6f));
-                if (cc < 1.0f) coef = cc;
-            }
-            st->coef = coef;
+        for (int k = 0; k < kNormThreads / 32; ++k) t = __dadd_rn(t, red[k]);
+    }
+    return t;
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+k_norm(const double* __restrict__ partials, int64_t n, double* __restrict__ slots, DevState* __restrict__ st,
+       float max_norm) {
+    __shared__ double red[kNormThreads / 32];
+    __shared__ bool last;
+    const int64_t per = (n + kNormBlocks - 1) / kNormBlocks;
+    const int64_t lo = min(n, per * blockIdx.x);
+    const int64_t hi = min(n, lo + per);
+    double acc8[8] = {0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0};
+    int64_t i = lo + threadIdx.x;
+    for (; i + 7 * kNormThreads < hi; i += 8 * kNormThreads) {
+        double x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = partials[i + q * kNormThreads];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc8[q] = __dadd_rn(acc8[q], x[q]);
+    }
+    double s = 0.0;
+    for (; i < hi; i += kNormThreads) s = __dadd_rn(s, partials[i]);  // the last < 8 rounds
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s = __dadd_rn(s, acc8[q]);
+    s = block_sum(s, red);
+    if (threadIdx.x == 0) {
+        slots[blockIdx.x] = s;
+        __threadfence();
+        const uint32_t ticket = atomicAdd(&st->norm_ticket, 1u);
+        last = (ticket % kNormBlocks) == kNormBlocks - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double v = threadIdx.x < kNormBlocks ? __ldcg(slots + threadIdx.x) : 0.0;  // slots written by other SMs
+    v = block_sum(v, red);
+    if (threadIdx.x == 0) {
+        st->sumsq = v;
+        if (!isfinite(v)) st->found_inf = 1;   // an fp32 square overflowed: treated as an overflow
+        const float norm = __double2float_rn(__dsqrt_rn(v));
+        st->norm = norm;
+        float coef = 1.0f;
+        if (max_norm > 0.0f) {
+            const float cc = __fdiv_rn(max_norm, __fadd_rn(norm, 1e-6f));
+            if (cc < 1.0f) coef = cc;
         }
+        st->coef = coef;
     }
 }
 
@@ -917,8 +936,11 @@ cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_norm(const double* partials, int64_t nchunks, DevState* st, float max_norm, cudaStream_t s) {
-    k_norm<<<1, kNormThreads, 0, s>>>(partials, nchunks, st, max_norm);
+cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevState* st, float max_norm,
+                        cudaStream_t s) {
+    static_assert(kNormBlocks <= kNormThreads, "the last CTA reads one slot per thread");
+    static_assert((kNormBlocks & (kNormBlocks - 1)) == 0, "the ticket counter wraps modulo a multiple of kNormBlocks");
+    k_norm<<<kNormBlocks, kNormThreads, 0, s>>>(partials, n, slots, st, max_norm);
     return cudaGetLastError();
 }
 

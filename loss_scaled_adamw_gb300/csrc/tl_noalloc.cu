@@ -30,6 +30,7 @@ namespace tl {
 namespace {
 
 constexpr int kNoAllocMaxTensors = 256;
+constexpr int kNoAllocNormThreads = 1024;  // one CTA; its last warp reads one per-warp sum per lane
 constexpr int64_t kNoAllocMaxChunks = int64_t(1) << 16;
 constexpr int kMaxDevices = 64;
 
@@ -114,11 +115,11 @@ k_noalloc_unscale(const __grid_constant__ NoAllocList L, float inv_s, int64_t nc
 
 // Fixed-order reduction of the partials, then norm, clip coefficient and the
 // overflow decision (a non-finite u makes its square, hence the sum, non-finite).
-__global__ void __launch_bounds__(kNormThreads)
+__global__ void __launch_bounds__(kNoAllocNormThreads)
 k_noalloc_norm(const double* __restrict__ partials, int64_t nchunks, float max_norm, tl_norm_result* out) {
-    __shared__ double red[kNormThreads / 32];
+    __shared__ double red[kNoAllocNormThreads / 32];
     double s = 0.0;
-    for (int64_t i = threadIdx.x; i < nchunks; i += kNormThreads) s = __dadd_rn(s, partials[i]);
+    for (int64_t i = threadIdx.x; i < nchunks; i += kNoAllocNormThreads) s = __dadd_rn(s, partials[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
@@ -213,7 +214,7 @@ extern "C" int tl_unscale_norm_noalloc(int64_t ntensors, const int64_t* numel, f
         k_noalloc_unscale<<<g, kThreads, 0, s>>>(L, 1.0f / S, nchunks);  // S a power of two: exact
         if (cudaGetLastError() != cudaSuccess) return TL_ECUDA;
     }
-    k_noalloc_norm<<<1, kNormThreads, 0, s>>>(partials, nchunks, max_norm, out);
+    k_noalloc_norm<<<1, kNoAllocNormThreads, 0, s>>>(partials, nchunks, max_norm, out);
     if (cudaGetLastError() != cudaSuccess) return TL_ECUDA;
     return TL_OK;
 }
