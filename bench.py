@@ -50,7 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--path", choices=["resident", "per_microbatch"], default="resident",
                     help="resident: the k micro-batch gradient lists are read in one pass (tl_accumulate_many); "
                          "per_microbatch: one tl_accumulate per micro-batch")
-    ap.add_argument("--layout", choices=["aligned", "misaligned"], default="aligned",
+    ap.add_argument("--layout", choices=["aligned", "packed", "misaligned"], default="aligned",
                     help="tensor placement inside the flat buffers (see GpuWorkload)")
     ap.add_argument("--graph", action="store_true", help="also time both sequences replayed from a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
@@ -203,13 +203,23 @@ class GpuWorkload:
         self.P = P
         self.device = device
         # tensor offsets inside each flat buffer: "aligned" starts every tensor on a
-        # 32-byte boundary (packed when the sizes allow), "misaligned" puts a seeded 0-3
+        # 32-byte boundary (packed when the sizes allow), "packed" puts tensors back to
+        # back (same element phase in every list), "misaligned" puts a seeded 0-3
         # element gap before every tensor (many start off any 16-byte boundary)
-        offs, total = W.layout_offsets(wl.numel, layout == "misaligned", 8, 0)
-        self.offs, self.total = offs, total
+        # with "misaligned" every list gets its own gaps (no common element phase)
+        self.layout = layout
+        self.offs_of = {}
+
+        def offsets(key):
+            if key not in self.offs_of:
+                self.offs_of[key] = W.layout_offsets(wl.numel, layout == "misaligned", 1 if layout == "packed" else 8,
+                                                     key if layout == "misaligned" else 0)
+            return self.offs_of[key]
+
         gscale = wl.init_scale if wl.grads_prescaled else 1.0
 
-        def spread(flat, dtype):
+        def spread(flat, dtype, key):
+            offs, total = offsets(key)
             if offs == np.cumsum([0] + wl.numel[:-1]).tolist():
                 return flat
             buf = torch.zeros(total + 16, dtype=dtype, device=device)
@@ -219,27 +229,29 @@ class GpuWorkload:
             buf[idx] = flat
             return buf
 
+        keys = {"param": 1, "master": 2, "m": 3, "v": 4, "acc": 5}
         master = W.master_init(wl, device)
-        self.master = spread(master, torch.float32)
-        self.param = spread(W.to_16bit(master, wl.param_dtype), W.to_16bit(master[:1], wl.param_dtype).dtype)
+        self.master = spread(master, torch.float32, keys["master"])
+        self.param = spread(W.to_16bit(master, wl.param_dtype), W.to_16bit(master[:1], wl.param_dtype).dtype, keys["param"])
         del master
-        self.m = torch.zeros(self.master.numel(), dtype=torch.float32, device=device)
-        self.v = torch.zeros_like(self.m)
-        self.acc = torch.empty_like(self.m)
+        self.m = torch.zeros(offsets(keys["m"])[1] + 16, dtype=torch.float32, device=device)
+        self.v = torch.zeros(offsets(keys["v"])[1] + 16, dtype=torch.float32, device=device)
+        self.acc = torch.empty(offsets(keys["acc"])[1] + 16, dtype=torch.float32, device=device)
         self.grads = []
         for i in range(wl.k):
             g = W.grad_input(wl, 1, i, scale=gscale, device=device)
-            self.grads.append(spread(g, g.dtype))
+            self.grads.append(spread(g, g.dtype, 10 + i))
             del g
 
-        def plist(t):
+        def plist(t, key):
             es, base = t.element_size(), t.data_ptr()
-            p = tl.PtrList([base + o * es for o in offs])
+            p = tl.PtrList([base + o * es for o in offsets(key)[0]])
             p.keep = t
             return p
 
-        self.plists = {n: plist(getattr(self, n)) for n in ("param", "master", "m", "v", "acc")}
-        self.gplists = [plist(g) for g in self.grads]
+        self.plist = plist
+        self.plists = {n: plist(getattr(self, n), keys[n]) for n in keys}
+        self.gplists = [plist(g, 10 + i) for i, g in enumerate(self.grads)]
         self.many = tl.ManyLists(self.gplists)
         dt = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32}
         cfg = tl.make_config(dt[wl.param_dtype], dt[wl.grad_dtype], wl.scaler_enabled,
@@ -434,15 +446,7 @@ def run_e2e(args, gw, world):
     for h, g in zip(host, gw.grads):
         h.copy_(g)
     sets = [gw.grads, [torch.empty_like(g) for g in gw.grads]]
-    offs = gw.offs
-
-    def plist(t):
-        es, base = t.element_size(), t.data_ptr()
-        p = tl.PtrList([base + o * es for o in offs])
-        p.keep = t
-        return p
-
-    many = [gw.many, tl.ManyLists([plist(g) for g in sets[1]])]
+    many = [gw.many, tl.ManyLists([gw.plist(g, 10 + i) for i, g in enumerate(sets[1])])]
     torch.cuda.synchronize()
     copy_stream = torch.cuda.Stream()
     compute = torch.cuda.current_stream()

@@ -265,16 +265,39 @@ __device__ __forceinline__ bool aligned32(const void* p) {
 // it represents"; [MP] section 2 "Gradient accumulation" (no zeroing between
 // micro-batches).  acc = w*g (first) or fma(w, g, acc).
 // ---------------------------------------------------------------------------
+// Vector plan of one segment.  head elements are done one by one first, then
+// whole 8-element vectors from element head on, then the tail.  head is 0 when
+// every stream is already on a 16-byte boundary; when the streams are not, but
+// all sit at the same element phase r modulo 8 (tensors packed back to back in
+// every list), head = 8 - r puts each fp32 stream on a 32-byte and each 16-bit
+// stream on a 16-byte boundary; otherwise there is no vector part.
+struct VecPlan {
+    int head;
+    bool vec;
+    bool wide;  // fp32 streams 32-byte aligned from head on: 256-bit accesses
+};
+
+template <int ES>
+__device__ __forceinline__ int ephase(const void* p) {
+    return static_cast<int>((reinterpret_cast<uintptr_t>(p) / ES) & 7);
+}
+
 template <int NT, int GDT, bool FIRST>
 __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
                                                    const void* const* gp, float w) {
-    float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
-    const void* g = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
+    float* __restrict__ acc0 = tp[ch.tensor].acc + ch.start;
+    const char* g0 = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
     const int len = ch.len;
-    const bool wide = aligned32(acc);
-    int done = 0;
-    if (aligned16(acc) && aligned16(g)) {
-        const int nv = len / kVec;
+    VecPlan pl{0, false, false};
+    if (aligned16(acc0) && aligned16(g0)) pl = VecPlan{0, true, aligned32(acc0)};
+    else if (ephase<4>(acc0) == ephase<Grad<GDT>::kBytes>(g0)) pl = VecPlan{(8 - ephase<4>(acc0)) & 7, true, true};
+    int head = 0, done = 0;
+    if (pl.vec) {
+        head = min(pl.head, len);
+        const bool wide = pl.wide;
+        float* __restrict__ acc = acc0 + head;
+        const void* g = g0 + head * Grad<GDT>::kBytes;
+        const int nv = (len - head) / kVec;
         int i = t;
         for (; i + (kUnroll - 1) * NT < nv; i += kUnroll * NT) {
             float gx[kUnroll][8], ax[kUnroll][8];
@@ -300,12 +323,14 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
             for (int e = 0; e < 8; ++e) ax[e] = FIRST ? __fmul_rn(w, gx[e]) : __fmaf_rn(w, gx[e], ax[e]);
             st8_f32(acc + i * kVec, ax, wide);
         }
-        done = nv * kVec;
+        done = head + nv * kVec;
     }
-    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
-        const float gj = Grad<GDT>::ld1(g, j);
-        acc[j] = FIRST ? __fmul_rn(w, gj) : __fmaf_rn(w, gj, acc[j]);
-    }
+    auto one = [&](int j) {
+        const float gj = Grad<GDT>::ld1(g0, j);
+        acc0[j] = FIRST ? __fmul_rn(w, gj) : __fmaf_rn(w, gj, acc0[j]);
+    };
+    for (int j = t; j < head; j += NT) one(j);          // head
+    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
 }
 
 template <int NT, int GDT, bool FIRST>
@@ -434,13 +459,19 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const Te
                                                 bool& bad) {
     constexpr bool kReadG = MODE != kAccOnly;
     constexpr bool kReadAcc = MODE != kFirstOnly;
-    float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
-    const void* g = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
+    float* __restrict__ acc0 = tp[ch.tensor].acc + ch.start;
+    const char* g0 = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
     const int len = ch.len;
-    const bool wide = aligned32(acc);
-    int done = 0;
-    if (aligned16(acc) && (!kReadG || aligned16(g))) {
-        const int nv = len / kVec;
+    VecPlan pl{0, false, false};
+    if (aligned16(acc0) && (!kReadG || aligned16(g0))) pl = VecPlan{0, true, aligned32(acc0)};
+    else if (!kReadG || ephase<4>(acc0) == ephase<Grad<GDT>::kBytes>(g0)) pl = VecPlan{(8 - ephase<4>(acc0)) & 7, true, true};
+    int head = 0, done = 0;
+    if (pl.vec) {
+        head = min(pl.head, len);
+        const bool wide = pl.wide;
+        float* __restrict__ acc = acc0 + head;
+        const void* g = kReadG ? g0 + head * Grad<GDT>::kBytes : nullptr;
+        const int nv = (len - head) / kVec;
         int i = t;
         for (; i + (kUnroll - 1) * NT < nv; i += kUnroll * NT) {
             float gx[kUnroll][8], ax[kUnroll][8];
@@ -476,14 +507,16 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const Te
             sq.vec8(ax);
             st8_f32(acc + i * kVec, ax, wide);
         }
-        done = nv * kVec;
+        done = head + nv * kVec;
     }
-    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
-        const float u = unscale1<MODE>(kReadAcc ? acc[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g, j) : 0.0f, w, inv_s);
-        acc[j] = u;
+    auto one = [&](int j) {
+        const float u = unscale1<MODE>(kReadAcc ? acc0[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g0, j) : 0.0f, w, inv_s);
+        acc0[j] = u;
         bad |= !isfinite(u);
         sq.one(u);
-    }
+    };
+    for (int j = t; j < head; j += NT) one(j);          // head
+    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
 }
 
 template <int NT, int GDT, int MODE>
@@ -518,31 +551,40 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const Tenso
                                              const GradTableMany& inl, const ManyArgs& a, float inv_s, SumSq& sq,
                                              bool& bad) {
     const int kk = a.k;
-    float* __restrict__ acc = tp[ch.tensor].acc + ch.start;
+    float* __restrict__ acc0 = tp[ch.tensor].acc + ch.start;
     const char* g[kMaxMany];
-    bool al = aligned16(acc);
+    bool al = aligned16(acc0);
+    bool same = true;
+    const int r = ephase<4>(acc0);
 #pragma unroll
     for (int q = 0; q < kMaxMany; ++q) {
         if (q < kk) {
             const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
             g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
             al = al && aligned16(g[q]);
+            same = same && ephase<Grad<GDT>::kBytes>(g[q]) == r;
         } else {
             g[q] = nullptr;
         }
     }
     const int len = ch.len;
-    const bool wide = aligned32(acc);
-    int done = 0;
-    if (al) {
-        const int nv = len / kVec;
+    VecPlan pl{0, false, false};
+    if (al) pl = VecPlan{0, true, aligned32(acc0)};
+    else if (same) pl = VecPlan{(8 - r) & 7, true, true};
+    int head = 0, done = 0;
+    if (pl.vec) {
+        head = min(pl.head, len);
+        const bool wide = pl.wide;
+        float* __restrict__ acc = acc0 + head;
+        const int gofs = head * Grad<GDT>::kBytes;
+        const int nv = (len - head) / kVec;
         for (int i = t; i < nv; i += NT) {
             // all kk loads in flight first; each stream's 8 values are unpacked
             // inside the multiply-add chain (per element still q = 0, 1, ... in order)
             typename GradRaw<GDT>::T raw[kMaxMany];
 #pragma unroll
             for (int q = 0; q < kMaxMany; ++q)
-                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q], int64_t(i) * kVec);
+                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q] + gofs, int64_t(i) * kVec);
             float ax[8];
             if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
 #pragma unroll
@@ -565,10 +607,10 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const Tenso
             }
             st8_f32(acc + i * kVec, ax, wide);
         }
-        done = nv * kVec;
+        done = head + nv * kVec;
     }
-    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
-        float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j)) : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j), acc[j]);
+    auto one = [&](int j) {
+        float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j)) : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j), acc0[j]);
 #pragma unroll
         for (int q = 1; q < kMaxMany; ++q)
             if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j), v);
@@ -577,8 +619,10 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const Tenso
             bad |= !isfinite(v);
             sq.one(v);
         }
-        acc[j] = v;
-    }
+        acc0[j] = v;
+    };
+    for (int j = t; j < head; j += NT) one(j);          // head
+    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
 }
 
 template <int NT, int GDT, bool FIRST, bool LAST>
@@ -694,16 +738,30 @@ template <int NT, int PDT>
 __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
                                               const AdamConsts& k) {
     const TensorPtrs tpp = tp[ch.tensor];
-    const float* __restrict__ u = tpp.acc + ch.start;
-    float* __restrict__ w = tpp.master + ch.start;
-    float* __restrict__ m = tpp.m + ch.start;
-    float* __restrict__ v = tpp.v + ch.start;
-    void* p = static_cast<unsigned short*>(tpp.param) + ch.start;
+    const float* __restrict__ u0 = tpp.acc + ch.start;
+    float* __restrict__ w0 = tpp.master + ch.start;
+    float* __restrict__ m0 = tpp.m + ch.start;
+    float* __restrict__ v0 = tpp.v + ch.start;
+    unsigned short* p0 = static_cast<unsigned short*>(tpp.param) + ch.start;
     const int len = ch.len;
-    const bool wide = aligned32(u) && aligned32(w) && aligned32(m) && aligned32(v);
-    int done = 0;
-    if (aligned16(u) && aligned16(w) && aligned16(m) && aligned16(v) && aligned16(p)) {
-        const int nv = len / kVec;
+    VecPlan pl{0, false, false};
+    if (aligned16(u0) && aligned16(w0) && aligned16(m0) && aligned16(v0) && aligned16(p0)) {
+        pl = VecPlan{0, true, aligned32(u0) && aligned32(w0) && aligned32(m0) && aligned32(v0)};
+    } else {
+        const int r = ephase<4>(u0);
+        if (ephase<4>(w0) == r && ephase<4>(m0) == r && ephase<4>(v0) == r && ephase<2>(p0) == r)
+            pl = VecPlan{(8 - r) & 7, true, true};
+    }
+    int head = 0, done = 0;
+    if (pl.vec) {
+        head = min(pl.head, len);
+        const bool wide = pl.wide;
+        const float* __restrict__ u = u0 + head;
+        float* __restrict__ w = w0 + head;
+        float* __restrict__ m = m0 + head;
+        float* __restrict__ v = v0 + head;
+        void* p = p0 + head;
+        const int nv = (len - head) / kVec;
         int i = t;
         for (; i + (kUnrollAdam - 1) * NT < nv; i += kUnrollAdam * NT) {
             float ux[kUnrollAdam][8], wx[kUnrollAdam][8], mx[kUnrollAdam][8], vx[kUnrollAdam][8];
@@ -740,16 +798,18 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Tens
             st8_f32(v + o, vx, wide);
             st8_param<PDT>(p, o, wx);
         }
-        done = nv * kVec;
+        done = head + nv * kVec;
     }
-    for (int j = done + t; j < len; j += NT) {  // tails and misaligned segments
-        float wj = w[j], mj = m[j], vj = v[j];
-        adamw1(u[j], wj, mj, vj, k);
-        w[j] = wj;
-        m[j] = mj;
-        v[j] = vj;
-        Param<PDT>::st1(p, j, wj);
-    }
+    auto one = [&](int j) {
+        float wj = w0[j], mj = m0[j], vj = v0[j];
+        adamw1(u0[j], wj, mj, vj, k);
+        w0[j] = wj;
+        m0[j] = mj;
+        v0[j] = vj;
+        Param<PDT>::st1(p0, j, wj);
+    };
+    for (int j = t; j < head; j += NT) one(j);          // head
+    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
 }
 
 template <int NT, int PDT>

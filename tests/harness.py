@@ -67,10 +67,16 @@ def build_index(numel, offs, device):
 class DeviceList:
     """One tensor list in a flat device buffer; `ptrs` are the tensors' addresses."""
 
-    def __init__(self, numel, dtype, gaps: bool, key: int, device="cuda", fill=0.0):
+    def __init__(self, numel, dtype, gaps, key: int, device="cuda", fill=0.0):
+        """gaps: False (every tensor on a 32-byte boundary), True (seeded 0-3 element gaps,
+        independent per list) or "packed" (back to back, no padding: every list puts a
+        tensor at the same element offset)."""
         import torch
         self.numel = list(numel)
-        self.offs, total = W.layout_offsets(self.numel, gaps, 8, key)
+        if gaps == "packed":
+            self.offs, total = W.layout_offsets(self.numel, False, 1, key)
+        else:
+            self.offs, total = W.layout_offsets(self.numel, bool(gaps), 8, key)
         self.torch_dtype = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
         self.buf = torch.full((total + 16,), fill, dtype=self.torch_dtype, device=device)
         packed = self.offs == list(np.cumsum([0] + self.numel[:-1])) if self.numel else True

@@ -45,7 +45,7 @@ def custom(numel, pdtype="bf16", gdtype="bf16", k=2, steps=2, scaler=False, init
 # the workloads at their stated sizes
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("gaps", [False, True], ids=["packed", "misaligned"])
+@pytest.mark.parametrize("gaps", [False, True], ids=["aligned", "misaligned"])
 def test_bf16_small(gaps):
     """12 x 4,096 bf16, k=2 with 6 and 3 targets, clip active, 3 steps."""
     _, _, log = run_parity(W.make("bf16_small"), gaps=gaps)
@@ -82,7 +82,7 @@ EDGE_LISTS = {
 @pytest.mark.parametrize("lst", list(EDGE_LISTS), ids=list(EDGE_LISTS))
 @pytest.mark.parametrize("dtypes", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32"), ("f16", "bf16")],
                          ids=lambda d: f"p{d[0]}-g{d[1]}")
-@pytest.mark.parametrize("gaps", [False, True], ids=["packed", "misaligned"])
+@pytest.mark.parametrize("gaps", [False, True, "packed"], ids=["aligned", "misaligned", "packed"])
 def test_edge_lists(lst, dtypes, gaps):
     wl = custom(EDGE_LISTS[lst], pdtype=dtypes[0], gdtype=dtypes[1], k=3, steps=2, counts=[5, 1, 7])
     run_parity(wl, gaps=gaps)
@@ -420,11 +420,14 @@ def test_single_tensor_beyond_2_pow_31_full():
 # the full-size workloads
 # ---------------------------------------------------------------------------
 
-def test_ragged_100k_full():
-    """100,000 ragged tensors (~400M parameters), many starting off 16-byte boundaries;
-    fp16 with loss scaling, an inf in micro-batch 1 of step 2; every element compared."""
+@pytest.mark.parametrize("layout", [True, "packed"], ids=["misaligned", "packed"])
+def test_ragged_100k_full(layout):
+    """100,000 ragged tensors (~400M parameters) in flat buffers, either with independent
+    seeded gaps (most tensors off any 16-byte boundary, scalar paths) or packed back to
+    back (same element phase in every list: peeled vector paths); fp16 with loss
+    scaling, an inf in micro-batch 1 of step 2; every element compared."""
     wl = W.make("ragged_100k")
-    run_parity(wl, gaps=True, compare_every=wl.steps)
+    run_parity(wl, gaps=layout, compare_every=wl.steps)
 
 
 def test_llama_1b_full_size_sampled():

@@ -36,7 +36,7 @@ def test_workloads_resident(name):
 
 
 @pytest.mark.parametrize("k", [1, 3, 8, 9, 11, 17])
-@pytest.mark.parametrize("gaps", [False, True], ids=["packed", "misaligned"])
+@pytest.mark.parametrize("gaps", [False, True, "packed"], ids=["aligned", "misaligned", "packed"])
 def test_micro_batch_counts_resident(k, gaps):
     wl = custom([1, 9, 16385, 5000, 0, 77], k=k, steps=2, counts=[3 + (i * 7) % 11 for i in range(k)])
     run_parity(wl, gaps=gaps, resident=True)
