@@ -69,7 +69,6 @@ struct tl_ctx {
     std::vector<Interval> state_iv;  // sorted intervals of every state tensor
     Chunk* d_chunks = nullptr;     // segments
     int32_t* d_cbegin = nullptr;   // chunk -> first segment (nchunks + 1 entries)
-    TensorPtrs* d_tp = nullptr;
     double* d_partials = nullptr;
     double* d_norm_slots = nullptr;  // one per CTA of the second-stage reduce
     DevState* d_state = nullptr;
@@ -253,7 +252,6 @@ void free_ctx(tl_ctx* ctx) {
     if (ctx == nullptr) return;
     cudaFree(ctx->d_chunks);
     cudaFree(ctx->d_cbegin);
-    cudaFree(ctx->d_tp);
     cudaFree(ctx->d_partials);
     cudaFree(ctx->d_norm_slots);
     cudaFree(ctx->d_state);
@@ -332,7 +330,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
-    // Segments, chunks and per-tensor pointers.  A large tensor becomes one chunk
+    // Segments and chunks.  A large tensor becomes one chunk
     // per kChunk elements; small tensors (<= kSmall elements) are grouped kGroup
     // to a chunk, one per warp.  Chunks are then ordered by work, largest first
     // (stable), so every round of the persistent grid gets chunks of similar size.
@@ -342,12 +340,15 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     };
     std::vector<ChunkBuild> built;
     ChunkBuild group;
-    std::vector<TensorPtrs> tp(size_t(std::max<int64_t>(ntensors, 1)));
+    // the descriptor of elements [st, st + len) of tensor i, with its state addresses
+    auto seg = [&](int64_t i, int64_t st, int64_t len) {
+        return Chunk{acc[i] + st, master[i] + st, m[i] + st, v[i] + st,
+                     static_cast<char*>(param[i]) + st * pes, st, int32_t(i), int32_t(len), 0};
+    };
     for (int64_t i = 0; i < ntensors; ++i) {
-        tp[i] = TensorPtrs{master[i], m[i], v[i], acc[i], param[i], numel[i]};
         if (numel[i] == 0) continue;
         if (numel[i] <= kSmall) {
-            group.segs.push_back(Chunk{int32_t(i), int32_t(numel[i]), 0});
+            group.segs.push_back(seg(i, 0, numel[i]));
             group.work += numel[i];
             if (int(group.segs.size()) == kGroup) {
                 built.push_back(std::move(group));
@@ -358,7 +359,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
         for (int64_t st = 0; st < numel[i]; st += kChunk) {
             ChunkBuild one;
             const int32_t len = int32_t(std::min<int64_t>(kChunk, numel[i] - st));
-            one.segs.push_back(Chunk{int32_t(i), len, st});
+            one.segs.push_back(seg(i, st, len));
             one.work = len;
             built.push_back(std::move(one));
         }
@@ -388,7 +389,6 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     const size_t nc_alloc = size_t(std::max<int64_t>(nchunks, 1));
     if (cudaMalloc(&ctx->d_chunks, sizeof(Chunk) * std::max<size_t>(chunks.size(), 1)) != cudaSuccess ||
         cudaMalloc(&ctx->d_cbegin, sizeof(int32_t) * cbegin.size()) != cudaSuccess ||
-        cudaMalloc(&ctx->d_tp, sizeof(TensorPtrs) * tp.size()) != cudaSuccess ||
         cudaMalloc(&ctx->d_partials, sizeof(double) * nc_alloc * kGroup) != cudaSuccess ||
         cudaMalloc(&ctx->d_norm_slots, sizeof(double) * kNormBlocks) != cudaSuccess ||
         cudaMalloc(&ctx->d_state, sizeof(DevState)) != cudaSuccess) {
@@ -427,8 +427,6 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
         e = cudaMemcpyAsync(ctx->d_chunks, chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(ctx->d_cbegin, cbegin.data(), sizeof(int32_t) * cbegin.size(), cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && ntensors > 0)
-        e = cudaMemcpyAsync(ctx->d_tp, tp.data(), sizeof(TensorPtrs) * size_t(ntensors), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
@@ -480,7 +478,7 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
     if (ctx->nchunks > 0) {
         const int gdt = ctx->cfg.grad_dtype;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_accumulate(gdt, first != 0, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, inl,
+            return launch_accumulate(gdt, first != 0, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl,
                                      dtab, w, ctx->grid_acc[gdt][first][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return cuda_fail(ctx, e, "accumulate launch");
@@ -528,7 +526,7 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
     if (ctx->nchunks > 0) {
         const int gdt = ctx->cfg.grad_dtype;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_unscale(gdt, mode, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, inl, dtab, w,
+            return launch_unscale(gdt, mode, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, dtab, w,
                                   ctx->d_state, ctx->d_partials, ctx->grid_uns[gdt][mode][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return cuda_fail(ctx, e, "unscale launch");
@@ -600,7 +598,7 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
             const int vr = (f ? 1 : 0) | (l ? 2 : 0);
             const int gdt = ctx->cfg.grad_dtype;
             cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, inl, a,
+                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, a,
                                          ctx->d_state, ctx->d_partials, ctx->grid_many[gdt][vr][small ? 1 : 0], s);
             });
             if (e != cudaSuccess) return cuda_fail(ctx, e, "many-list accumulate launch");
@@ -644,11 +642,11 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
     if (ctx->nchunks == 0) {
         // no elements: still one launch, whose first CTA computes the beta powers
         // the scaler kernel commits
-        e = launch_adamw(pdt, false, ctx->d_chunks, ctx->d_cbegin, 0, 0, ctx->d_tp, ctx->d_state, h, 1, s);
+        e = launch_adamw(pdt, false, ctx->d_chunks, ctx->d_cbegin, 0, 0, ctx->d_state, h, 1, s);
         if (e == cudaSuccess) ctx->launches += 1;
     } else {
         e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_adamw(pdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_tp, ctx->d_state, h,
+            return launch_adamw(pdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_state, h,
                                 ctx->grid_adam[pdt][small ? 1 : 0], s);
         });
     }

@@ -33,22 +33,22 @@ constexpr int kF32 = 0;
 constexpr int kBF16 = 1;
 constexpr int kF16 = 2;
 
-// Per-tensor base pointers of the state lists (48 bytes).
-struct TensorPtrs {
+// One segment: elements [start, start + len) of tensor `tensor` (64 bytes).  The
+// state-list addresses of its first element are stored in the descriptor, so a
+// kernel reaches the data one load after the descriptor; the gradient lists,
+// which change from call to call, are indexed by tensor and offset by start.
+// Chunk c covers segments [cbegin[c], cbegin[c + 1]); in the whole-CTA part of
+// the table chunk c is segment c.
+struct Chunk {
+    float* acc;
     float* master;
     float* m;
     float* v;
-    float* acc;
     void* param;
-    int64_t numel;
-};
-
-// One segment: elements [start, start + len) of tensor `tensor` (16 bytes).
-// Chunk c covers segments [cbegin[c], cbegin[c + 1]).
-struct Chunk {
+    int64_t start;
     int32_t tensor;
     int32_t len;
-    int64_t start;
+    int64_t reserved;
 };
 
 // Device-resident scalars of one context.
@@ -113,18 +113,18 @@ enum UnscaleMode : int {
 // small = true for groups of small tensors (one warp per tensor).  `grid` is
 // the persistent grid size; a gtab of nullptr means the pointers are in `inl`.
 cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
-                              int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
+                              int64_t c1, const GradTable& inl, const void* const* gtab, float w,
                               int grid, cudaStream_t s);
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
-                           int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
+                           int64_t c1, const GradTable& inl, const void* const* gtab, float w,
                            DevState* st, double* partials, int grid, cudaStream_t s);
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
-                              int64_t c0, int64_t c1, const TensorPtrs* tp, const GradTableMany& inl,
+                              int64_t c0, int64_t c1, const GradTableMany& inl,
                               const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s);
 cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevState* st, float max_norm,
                         cudaStream_t s);
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
-                         const TensorPtrs* tp, DevState* st, AdamHP hp, int grid, cudaStream_t s);
+                         DevState* st, AdamHP hp, int grid, cudaStream_t s);
 cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);
 cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s);
 

@@ -283,9 +283,8 @@ __device__ __forceinline__ int ephase(const void* p) {
 }
 
 template <int NT, int GDT, bool FIRST>
-__device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
-                                                   const void* const* gp, float w) {
-    float* __restrict__ acc0 = tp[ch.tensor].acc + ch.start;
+__device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const void* const* gp, float w) {
+    float* __restrict__ acc0 = ch.acc;
     const char* g0 = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
     const int len = ch.len;
     VecPlan pl{0, false, false};
@@ -336,14 +335,17 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
 template <int NT, int GDT, bool FIRST>
 __global__ void __launch_bounds__(kThreads)
 k_accumulate(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
-             const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTable inl,
+             const __grid_constant__ GradTable inl,
              const void* const* __restrict__ gtab, float w) {
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
-        if (NT == kThreads) accumulate_segment<kThreads, GDT, FIRST>(chunks[b0], threadIdx.x, tp, gp, w);
-        else if (wi < cbegin[c + 1] - b0) accumulate_segment<32, GDT, FIRST>(chunks[b0 + wi], threadIdx.x & 31, tp, gp, w);
+        if (NT == kThreads) {
+            accumulate_segment<kThreads, GDT, FIRST>(chunks[c], threadIdx.x, gp, w);
+        } else {
+            const int b0 = cbegin[c];
+            const int wi = threadIdx.x >> 5;
+            if (wi < cbegin[c + 1] - b0) accumulate_segment<32, GDT, FIRST>(chunks[b0 + wi], threadIdx.x & 31, gp, w);
+        }
     }
 }
 
@@ -454,12 +456,11 @@ __device__ __forceinline__ void finish_warp(const SumSq& sq, bool bad, int64_t c
 }
 
 template <int NT, int GDT, int MODE>
-__device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
-                                                const void* const* gp, float w, float inv_s, SumSq& sq,
-                                                bool& bad) {
+__device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const void* const* gp, float w, float inv_s,
+                                                SumSq& sq, bool& bad) {
     constexpr bool kReadG = MODE != kAccOnly;
     constexpr bool kReadAcc = MODE != kFirstOnly;
-    float* __restrict__ acc0 = tp[ch.tensor].acc + ch.start;
+    float* __restrict__ acc0 = ch.acc;
     const char* g0 = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
     const int len = ch.len;
     VecPlan pl{0, false, false};
@@ -522,18 +523,21 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const Te
 template <int NT, int GDT, int MODE>
 __global__ void __launch_bounds__(kThreads, NT == kThreads && GDT != kF32 ? 3 : 2)
 k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
-          const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTable inl,
+          const __grid_constant__ GradTable inl,
           const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials) {
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
     const float inv_s = __fdiv_rn(1.0f, st->S);
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
         SumSq sq;
         bool bad = false;
-        if (NT == kThreads) unscale_segment<kThreads, GDT, MODE>(chunks[b0], threadIdx.x, tp, gp, w, inv_s, sq, bad);
-        else if (wi < cbegin[c + 1] - b0)
-            unscale_segment<32, GDT, MODE>(chunks[b0 + wi], threadIdx.x & 31, tp, gp, w, inv_s, sq, bad);
+        if (NT == kThreads) {
+            unscale_segment<kThreads, GDT, MODE>(chunks[c], threadIdx.x, gp, w, inv_s, sq, bad);
+        } else {
+            const int b0 = cbegin[c];
+            const int wi = threadIdx.x >> 5;
+            if (wi < cbegin[c + 1] - b0)
+                unscale_segment<32, GDT, MODE>(chunks[b0 + wi], threadIdx.x & 31, gp, w, inv_s, sq, bad);
+        }
         finish_warp(sq, bad, c, st, partials);
     }
 }
@@ -547,11 +551,10 @@ k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, 
 // with the unscale, overflow check and squared-norm partial of a3.
 // ---------------------------------------------------------------------------
 template <int NT, int GDT, bool FIRST, bool LAST>
-__device__ __forceinline__ void many_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
-                                             const GradTableMany& inl, const ManyArgs& a, float inv_s, SumSq& sq,
-                                             bool& bad) {
+__device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradTableMany& inl, const ManyArgs& a,
+                                             float inv_s, SumSq& sq, bool& bad) {
     const int kk = a.k;
-    float* __restrict__ acc0 = tp[ch.tensor].acc + ch.start;
+    float* __restrict__ acc0 = ch.acc;
     const char* g[kMaxMany];
     bool al = aligned16(acc0);
     bool same = true;
@@ -628,17 +631,20 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const Tenso
 template <int NT, int GDT, bool FIRST, bool LAST>
 __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1 : GDT == kF32 ? (TL_MINB_MANY < 2 ? TL_MINB_MANY : 2) : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
-             const TensorPtrs* __restrict__ tp, const __grid_constant__ GradTableMany inl,
+             const __grid_constant__ GradTableMany inl,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
         SumSq sq;
         bool bad = false;
-        if (NT == kThreads) many_segment<kThreads, GDT, FIRST, LAST>(chunks[b0], threadIdx.x, tp, inl, a, inv_s, sq, bad);
-        else if (wi < cbegin[c + 1] - b0)
-            many_segment<32, GDT, FIRST, LAST>(chunks[b0 + wi], threadIdx.x & 31, tp, inl, a, inv_s, sq, bad);
+        if (NT == kThreads) {
+            many_segment<kThreads, GDT, FIRST, LAST>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
+        } else {
+            const int b0 = cbegin[c];
+            const int wi = threadIdx.x >> 5;
+            if (wi < cbegin[c + 1] - b0)
+                many_segment<32, GDT, FIRST, LAST>(chunks[b0 + wi], threadIdx.x & 31, inl, a, inv_s, sq, bad);
+        }
         if (LAST) finish_warp(sq, bad, c, st, partials);
     }
 }
@@ -735,14 +741,12 @@ __device__ __forceinline__ void adamw1(float u, float& w, float& m, float& v, co
 }
 
 template <int NT, int PDT>
-__device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const TensorPtrs* __restrict__ tp,
-                                              const AdamConsts& k) {
-    const TensorPtrs tpp = tp[ch.tensor];
-    const float* __restrict__ u0 = tpp.acc + ch.start;
-    float* __restrict__ w0 = tpp.master + ch.start;
-    float* __restrict__ m0 = tpp.m + ch.start;
-    float* __restrict__ v0 = tpp.v + ch.start;
-    unsigned short* p0 = static_cast<unsigned short*>(tpp.param) + ch.start;
+__device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const AdamConsts& k) {
+    const float* __restrict__ u0 = ch.acc;
+    float* __restrict__ w0 = ch.master;
+    float* __restrict__ m0 = ch.m;
+    float* __restrict__ v0 = ch.v;
+    unsigned short* p0 = static_cast<unsigned short*>(ch.param);
     const int len = ch.len;
     VecPlan pl{0, false, false};
     if (aligned16(u0) && aligned16(w0) && aligned16(m0) && aligned16(v0) && aligned16(p0)) {
@@ -815,7 +819,6 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Tens
 template <int NT, int PDT>
 __global__ void __launch_bounds__(kThreads, TL_MINB_ADAM)
 k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
-        const TensorPtrs* __restrict__ tp,
         DevState* __restrict__ st, AdamHP hp) {
     __shared__ AdamConsts sk;
     __shared__ int skip;
@@ -844,10 +847,13 @@ k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, in
     if (skip) return;
     const AdamConsts k = sk;
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
-        if (NT == kThreads) adamw_segment<kThreads, PDT>(chunks[b0], threadIdx.x, tp, k);
-        else if (wi < cbegin[c + 1] - b0) adamw_segment<32, PDT>(chunks[b0 + wi], threadIdx.x & 31, tp, k);
+        if (NT == kThreads) {
+            adamw_segment<kThreads, PDT>(chunks[c], threadIdx.x, k);
+        } else {
+            const int b0 = cbegin[c];
+            const int wi = threadIdx.x >> 5;
+            if (wi < cbegin[c + 1] - b0) adamw_segment<32, PDT>(chunks[b0 + wi], threadIdx.x & 31, k);
+        }
     }
 }
 
@@ -897,13 +903,12 @@ __global__ void k_seed(const DevState* __restrict__ st, float w, float* __restri
 // (one warp per tensor) over whole-CTA segments; each has its own register
 // budget.
 // ---------------------------------------------------------------------------
-using AccFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, const GradTable,
-                       const void* const*, float);
-using UnsFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, const GradTable,
-                       const void* const*, float, DevState*, double*);
-using ManyFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, const GradTableMany,
-                        const ManyArgs, DevState*, double*);
-using AdamFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const TensorPtrs*, DevState*, AdamHP);
+using AccFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const GradTable, const void* const*, float);
+using UnsFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const GradTable, const void* const*, float,
+                       DevState*, double*);
+using ManyFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const GradTableMany, const ManyArgs,
+                        DevState*, double*);
+using AdamFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, DevState*, AdamHP);
 
 template <int NT>
 AccFn acc_fn_nt(int gdt, bool first) {
@@ -970,29 +975,29 @@ AdamFn adam_fn(int pdt, bool small) {
 }  // namespace
 
 cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
-                              int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
-                              int grid, cudaStream_t s) {
+                              int64_t c1, const GradTable& inl, const void* const* gtab, float w, int grid,
+                              cudaStream_t s) {
     AccFn f = acc_fn(gdt, first, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, inl, gtab, w);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, gtab, w);
     return cudaGetLastError();
 }
 
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
-                           int64_t c1, const TensorPtrs* tp, const GradTable& inl, const void* const* gtab, float w,
-                           DevState* st, double* partials, int grid, cudaStream_t s) {
+                           int64_t c1, const GradTable& inl, const void* const* gtab, float w, DevState* st,
+                           double* partials, int grid, cudaStream_t s) {
     UnsFn f = uns_fn(gdt, mode, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, inl, gtab, w, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, gtab, w, st, partials);
     return cudaGetLastError();
 }
 
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
-                              int64_t c0, int64_t c1, const TensorPtrs* tp, const GradTableMany& inl,
-                              const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s) {
+                              int64_t c0, int64_t c1, const GradTableMany& inl, const ManyArgs& a, DevState* st,
+                              double* partials, int grid, cudaStream_t s) {
     ManyFn f = many_fn(gdt, first, last, small);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, inl, a, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, a, st, partials);
     return cudaGetLastError();
 }
 
@@ -1005,10 +1010,10 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
 }
 
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
-                         const TensorPtrs* tp, DevState* st, AdamHP hp, int grid, cudaStream_t s) {
+                         DevState* st, AdamHP hp, int grid, cudaStream_t s) {
     AdamFn f = adam_fn(pdt, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, tp, st, hp);
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, st, hp);
     return cudaGetLastError();
 }
 
