@@ -79,7 +79,7 @@ struct tl_ctx {
     int grid_acc[3][2][2] = {};
     int grid_uns[3][3][2] = {};
     int grid_adam[3][2] = {};
-    int grid_many[3][4][2] = {};
+    int grid_many[3][8][2] = {};
     // the update in flight
     int phase = kIdle;
     int64_t n_sum = 0;
@@ -439,7 +439,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
             for (int md = 0; md < 3; ++md)
                 ctx->grid_uns[dt][md][part] = grid_for(ctx, blocks_per_sm(1, dt, md, small), n);
             ctx->grid_adam[dt][part] = dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(2, dt, 0, small), n);
-            for (int vr = 0; vr < 4; ++vr)
+            for (int vr = 0; vr < 8; ++vr)
                 ctx->grid_many[dt][vr][part] = grid_for(ctx, blocks_per_sm(3, dt, vr, small), n);
         }
     }
@@ -595,7 +595,7 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
         const bool f = first && j == 0;
         const bool l = last && j + kk == k;
         if (ctx->nchunks > 0) {
-            const int vr = (f ? 1 : 0) | (l ? 2 : 0);
+            const int vr = (f ? 1 : 0) | (l ? 2 : 0) | (kk <= kFewLists ? 4 : 0);
             const int gdt = ctx->cfg.grad_dtype;
             cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
                 return launch_accum_many(gdt, f, l, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, a,

@@ -75,6 +75,7 @@ struct GradTable {
 
 // Resident micro-batches read by one launch of the many-list kernel.
 constexpr int kMaxMany = 8;
+constexpr int kFewLists = 2;      // launches of at most this many lists use a kernel form of their own
 constexpr int kInlineMany = 2048;  // k * ntensors gradient pointers travel by value up to this size
 
 struct GradTableMany {
@@ -130,7 +131,7 @@ cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s)
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0
-// FIRST, bit 1 LAST).
+// FIRST, bit 1 LAST, bit 2 at most kFewLists lists).
 int blocks_per_sm(int kind, int dt, int variant, bool small);
 
 }  // namespace tl

@@ -29,9 +29,13 @@ namespace tl {
 namespace {
 
 // Minimum resident CTAs per SM requested from the compiler (register budget) for
-// the many-list and AdamW kernels.
+// the many-list kernels (TL_MINB_FEW: launches of one or two lists, whose chunks
+// are worked faster when more of them are in flight) and the AdamW kernel.
 #ifndef TL_MINB_MANY
 #define TL_MINB_MANY 3
+#endif
+#ifndef TL_MINB_FEW
+#define TL_MINB_FEW 5
 #endif
 #ifndef TL_MINB_ADAM
 #define TL_MINB_ADAM 1
@@ -550,17 +554,17 @@ k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, 
 // of once per micro-batch.  FIRST: no partial sum in acc yet.  LAST: finish
 // with the unscale, overflow check and squared-norm partial of a3.
 // ---------------------------------------------------------------------------
-template <int NT, int GDT, bool FIRST, bool LAST>
+template <int NT, int GDT, bool FIRST, bool LAST, int KM>
 __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradTableMany& inl, const ManyArgs& a,
                                              float inv_s, SumSq& sq, bool& bad) {
     const int kk = a.k;
     float* __restrict__ acc0 = ch.acc;
-    const char* g[kMaxMany];
+    const char* g[KM];
     bool al = aligned16(acc0);
     bool same = true;
     const int r = ephase<4>(acc0);
 #pragma unroll
-    for (int q = 0; q < kMaxMany; ++q) {
+    for (int q = 0; q < KM; ++q) {
         if (q < kk) {
             const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
             g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
@@ -581,21 +585,16 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         float* __restrict__ acc = acc0 + head;
         const int gofs = head * Grad<GDT>::kBytes;
         const int nv = (len - head) / kVec;
-        for (int i = t; i < nv; i += NT) {
-            // all kk loads in flight first; each stream's 8 values are unpacked
-            // inside the multiply-add chain (per element still q = 0, 1, ... in order)
-            typename GradRaw<GDT>::T raw[kMaxMany];
-#pragma unroll
-            for (int q = 0; q < kMaxMany; ++q)
-                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q] + gofs, int64_t(i) * kVec);
-            float ax[8];
-            if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
+        // acc = w_0 g_0 + w_1 g_1 + ... (per element in list order), then unscale
+        // and the overflow / squared-norm bookkeeping of the last micro-batch
+        auto mix = [&](const auto& raw, float (&ax)[8]) {
+            constexpr int kq = sizeof(raw) / sizeof(raw[0]);  // lists this form can hold
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
                               : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
 #pragma unroll
-            for (int q = 1; q < kMaxMany; ++q)
+            for (int q = 1; q < kq; ++q)
                 if (q < kk) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
@@ -608,6 +607,17 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
                 }
                 sq.vec8(ax);
             }
+        };
+        for (int i = t; i < nv; i += NT) {
+            // all kk loads in flight first; each stream's 8 values are unpacked
+            // inside the multiply-add chain (per element still q = 0, 1, ... in order)
+            typename GradRaw<GDT>::T raw[KM];
+#pragma unroll
+            for (int q = 0; q < KM; ++q)
+                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q] + gofs, int64_t(i) * kVec);
+            float ax[8];
+            if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
+            mix(raw, ax);
             st8_f32(acc + i * kVec, ax, wide);
         }
         done = head + nv * kVec;
@@ -615,7 +625,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     auto one = [&](int j) {
         float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j)) : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j), acc0[j]);
 #pragma unroll
-        for (int q = 1; q < kMaxMany; ++q)
+        for (int q = 1; q < KM; ++q)
             if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j), v);
         if (LAST) {
             v = __fmul_rn(v, inv_s);
@@ -628,8 +638,10 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
 }
 
-template <int NT, int GDT, bool FIRST, bool LAST>
-__global__ void __launch_bounds__(kThreads, NT != kThreads ? 1 : GDT == kF32 ? (TL_MINB_MANY < 2 ? TL_MINB_MANY : 2) : TL_MINB_MANY)
+template <int NT, int GDT, bool FIRST, bool LAST, int KM>
+__global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
+                                            : GDT == kF32 ? 2
+                                            : KM <= kFewLists ? TL_MINB_FEW : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
              const __grid_constant__ GradTableMany inl,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
@@ -638,12 +650,12 @@ k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegi
         SumSq sq;
         bool bad = false;
         if (NT == kThreads) {
-            many_segment<kThreads, GDT, FIRST, LAST>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
+            many_segment<kThreads, GDT, FIRST, LAST, KM>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
         } else {
             const int b0 = cbegin[c];
             const int wi = threadIdx.x >> 5;
             if (wi < cbegin[c + 1] - b0)
-                many_segment<32, GDT, FIRST, LAST>(chunks[b0 + wi], threadIdx.x & 31, inl, a, inv_s, sq, bad);
+                many_segment<32, GDT, FIRST, LAST, KM>(chunks[b0 + wi], threadIdx.x & 31, inl, a, inv_s, sq, bad);
         }
         if (LAST) finish_warp(sq, bad, c, st, partials);
     }
@@ -944,24 +956,28 @@ UnsFn uns_fn_nt(int gdt, int mode) {
 
 UnsFn uns_fn(int gdt, int mode, bool small) { return small ? uns_fn_nt<32>(gdt, mode) : uns_fn_nt<kThreads>(gdt, mode); }
 
+template <int NT, int GDT, int KM>
+ManyFn many_fn_km(bool first, bool last) {
+    if (first) return last ? k_accum_many<NT, GDT, true, true, KM> : k_accum_many<NT, GDT, true, false, KM>;
+    return last ? k_accum_many<NT, GDT, false, true, KM> : k_accum_many<NT, GDT, false, false, KM>;
+}
 template <int NT, int GDT>
-ManyFn many_fn_dt(bool first, bool last) {
-    if (first) return last ? k_accum_many<NT, GDT, true, true> : k_accum_many<NT, GDT, true, false>;
-    return last ? k_accum_many<NT, GDT, false, true> : k_accum_many<NT, GDT, false, false>;
+ManyFn many_fn_dt(bool first, bool last, bool few) {
+    return few ? many_fn_km<NT, GDT, kFewLists>(first, last) : many_fn_km<NT, GDT, kMaxMany>(first, last);
 }
 
 template <int NT>
-ManyFn many_fn_nt(int gdt, bool first, bool last) {
+ManyFn many_fn_nt(int gdt, bool first, bool last, bool few) {
     switch (gdt) {
-        case kBF16: return many_fn_dt<NT, kBF16>(first, last);
-        case kF16: return many_fn_dt<NT, kF16>(first, last);
-        case kF32: return many_fn_dt<NT, kF32>(first, last);
+        case kBF16: return many_fn_dt<NT, kBF16>(first, last, few);
+        case kF16: return many_fn_dt<NT, kF16>(first, last, few);
+        case kF32: return many_fn_dt<NT, kF32>(first, last, few);
         default: return nullptr;
     }
 }
 
-ManyFn many_fn(int gdt, bool first, bool last, bool small) {
-    return small ? many_fn_nt<32>(gdt, first, last) : many_fn_nt<kThreads>(gdt, first, last);
+ManyFn many_fn(int gdt, bool first, bool last, bool small, bool few) {
+    return small ? many_fn_nt<32>(gdt, first, last, few) : many_fn_nt<kThreads>(gdt, first, last, few);
 }
 
 AdamFn adam_fn(int pdt, bool small) {
@@ -995,7 +1011,7 @@ cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, c
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
                               int64_t c0, int64_t c1, const GradTableMany& inl, const ManyArgs& a, DevState* st,
                               double* partials, int grid, cudaStream_t s) {
-    ManyFn f = many_fn(gdt, first, last, small);
+    ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, a, st, partials);
     return cudaGetLastError();
@@ -1032,7 +1048,8 @@ int blocks_per_sm(int kind, int dt, int variant, bool small) {
     if (kind == 0) f = reinterpret_cast<const void*>(acc_fn(dt, variant != 0, small));
     else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn(dt, variant, small));
     else if (kind == 2) f = reinterpret_cast<const void*>(adam_fn(dt, small));
-    else if (kind == 3) f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0, small));
+    else if (kind == 3)
+        f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0, small, (variant & 4) != 0));
     if (f == nullptr) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess || n < 1) return 1;

@@ -35,17 +35,56 @@ def test_workloads_resident(name):
     run_parity(wl, resident=True, compare_every=5 if wl.steps > 5 else 1)
 
 
-@pytest.mark.parametrize("k", [1, 3, 8, 9, 11, 17])
+@pytest.mark.parametrize("k", [1, 2, 3, 8, 9, 10, 11, 17])
 @pytest.mark.parametrize("gaps", [False, True, "packed"], ids=["aligned", "misaligned", "packed"])
 def test_micro_batch_counts_resident(k, gaps):
     wl = custom([1, 9, 16385, 5000, 0, 77], k=k, steps=2, counts=[3 + (i * 7) % 11 for i in range(k)])
     run_parity(wl, gaps=gaps, resident=True)
 
 
+@pytest.mark.parametrize("k", [2, 4])
 @pytest.mark.parametrize("dtypes", [("f16", "f16"), ("bf16", "f32"), ("f16", "bf16")], ids=str)
-def test_dtypes_resident(dtypes):
-    wl = custom([4096, 33, 20000], pdtype=dtypes[0], gdtype=dtypes[1], k=4, steps=2, counts=[1, 2, 3, 4])
+def test_dtypes_resident(dtypes, k):
+    wl = custom([4096, 33, 20000], pdtype=dtypes[0], gdtype=dtypes[1], k=k, steps=2, counts=[1, 2, 3, 4][:k])
     run_parity(wl, gaps=True, resident=True)
+
+
+@pytest.mark.parametrize("split", [(2, 2), (1, 3), (3, 1), (2, 1, 1), (1, 1, 1, 1)], ids=str)
+@pytest.mark.parametrize("gdtype", ["bf16", "f16", "f32"])
+def test_split_resident_calls(split, gdtype):
+    """One update fed by several tl_accumulate_many calls of one to three lists (the
+    launches of at most two lists take a kernel form of their own, with and without
+    a partial sum already in the buffer, and with and without the unscale); bit for
+    bit equal to the per-micro-batch path, and within tolerance of the oracle."""
+    pdtype = "f16" if gdtype == "f16" else "bf16"
+    wl = custom([70000, 4099, 123, 8, 16384], pdtype=pdtype, gdtype=gdtype, k=4, steps=2, counts=[5, 1, 2, 9])
+    master0 = W.master_init(wl)
+    # the same layout for both: which elements a thread sums (so the last bits of
+    # the squared norm) depends on the alignment of the lists
+    a = GpuOptimizer(wl, master0, gaps="packed", key=61)
+    b = GpuOptimizer(wl, master0, gaps="packed", key=61)
+    orc = oracle_for(wl, master0)
+    hp = tl.tl_adamw_hp(**W.HP)
+    for step in (1, 2):
+        grads = [W.grad_input(wl, step, i) for i in range(wl.k)]
+        counts = wl.counts(step)
+        a.step(grads, counts, resident=False)
+        pl = [b.grad_list(i, g) for i, g in enumerate(grads)]
+        j = 0
+        for n in split:
+            tl.tl_accumulate_many(b.ctx, pl[j:j + n], counts[j:j + n], sum(counts), int(j + n == wl.k))
+            j += n
+        tl.tl_grad_norm(b.ctx, wl.max_norm)
+        tl.tl_clip_adamw_step(b.ctx, hp)
+        tl.tl_scaler_update(b.ctx)
+        res = orc.step([grad_bits(g) for g in grads], counts, wl.max_norm, **W.HP)
+        sa, sb = a.status(), b.status()
+        assert (sa.norm, sa.sumsq, sa.coef, sa.t) == (sb.norm, sb.sumsq, sb.coef, sb.t)
+        compare_scalars(sb, orc, res, f"split {split} step {step}")
+    ra, rb = a.pull(), b.pull()
+    for key in ra:
+        assert np.array_equal(ra[key], rb[key]), key
+    compare_state(rb, orc, wl, f"split {split}")
 
 
 @pytest.mark.parametrize("ntensors", [256, 257, 600])
