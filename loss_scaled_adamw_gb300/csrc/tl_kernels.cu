@@ -44,6 +44,7 @@ namespace {
 constexpr int kVec = 8;     // elements per vector access (16 B of a 16-bit stream)
 constexpr int kUnroll = 4;  // vectors in flight per thread in the accumulate/unscale kernels
 constexpr int kUnrollAdam = 2;
+constexpr int kScalar = 8;  // elements per thread in flight on the scalar path (streams of unequal phase)
 
 // ---------------------------------------------------------------------------
 // 8-element vector access
@@ -333,7 +334,20 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
         acc0[j] = FIRST ? __fmul_rn(w, gj) : __fmaf_rn(w, gj, acc0[j]);
     };
     for (int j = t; j < head; j += NT) one(j);          // head
-    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
+    // tail, or the whole segment without a vector part: kScalar elements per
+    // thread loaded before any is stored
+    int j = done + t;
+    for (; j + (kScalar - 1) * NT < len; j += kScalar * NT) {
+        float gx[kScalar], ax[kScalar];
+#pragma unroll
+        for (int q = 0; q < kScalar; ++q) {
+            gx[q] = Grad<GDT>::ld1(g0, j + q * NT);
+            if (!FIRST) ax[q] = acc0[j + q * NT];
+        }
+#pragma unroll
+        for (int q = 0; q < kScalar; ++q) acc0[j + q * NT] = FIRST ? __fmul_rn(w, gx[q]) : __fmaf_rn(w, gx[q], ax[q]);
+    }
+    for (; j < len; j += NT) one(j);
 }
 
 template <int NT, int GDT, bool FIRST>
@@ -521,7 +535,25 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
         sq.one(u);
     };
     for (int j = t; j < head; j += NT) one(j);          // head
-    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
+    // tail, or the whole segment without a vector part: kScalar elements per
+    // thread loaded first, then finished in element order
+    int j = done + t;
+    for (; j + (kScalar - 1) * NT < len; j += kScalar * NT) {
+        float ax[kScalar], gx[kScalar];
+#pragma unroll
+        for (int q = 0; q < kScalar; ++q) {
+            ax[q] = kReadAcc ? acc0[j + q * NT] : 0.0f;
+            gx[q] = kReadG ? Grad<GDT>::ld1(g0, j + q * NT) : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < kScalar; ++q) {
+            const float u = unscale1<MODE>(ax[q], gx[q], w, inv_s);
+            acc0[j + q * NT] = u;
+            bad |= !isfinite(u);
+            sq.one(u);
+        }
+    }
+    for (; j < len; j += NT) one(j);
 }
 
 template <int NT, int GDT, int MODE>
@@ -635,7 +667,35 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         acc0[j] = v;
     };
     for (int j = t; j < head; j += NT) one(j);          // head
-    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
+    // tail, or the whole segment without a vector part: with one or two lists,
+    // S elements per thread loaded first, then finished in element order (more
+    // lists already put that many loads in flight)
+    constexpr int S = KM <= kFewLists ? kScalar / 4 : 1;
+    int j = done + t;
+    for (; S > 1 && j + (S - 1) * NT < len; j += S * NT) {
+        float gx[S][KM], ax[S];
+#pragma unroll
+        for (int e = 0; e < S; ++e) {
+#pragma unroll
+            for (int q = 0; q < KM; ++q)
+                if (q < kk) gx[e][q] = Grad<GDT>::ld1(g[q], j + e * NT);
+            if (!FIRST) ax[e] = acc0[j + e * NT];
+        }
+#pragma unroll
+        for (int e = 0; e < S; ++e) {
+            float v = FIRST ? __fmul_rn(a.w[0], gx[e][0]) : __fmaf_rn(a.w[0], gx[e][0], ax[e]);
+#pragma unroll
+            for (int q = 1; q < KM; ++q)
+                if (q < kk) v = __fmaf_rn(a.w[q], gx[e][q], v);
+            if (LAST) {
+                v = __fmul_rn(v, inv_s);
+                bad |= !isfinite(v);
+                sq.one(v);
+            }
+            acc0[j + e * NT] = v;
+        }
+    }
+    for (; j < len; j += NT) one(j);
 }
 
 template <int NT, int GDT, bool FIRST, bool LAST, int KM>
@@ -825,7 +885,30 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Adam
         Param<PDT>::st1(p0, j, wj);
     };
     for (int j = t; j < head; j += NT) one(j);          // head
-    for (int j = done + t; j < len; j += NT) one(j);    // tail, or the whole segment without a vector part
+    // tail, or the whole segment without a vector part: kScalar elements per
+    // thread loaded before any is stored
+    int j = done + t;
+    for (; j + (kScalar - 1) * NT < len; j += kScalar * NT) {
+        float ux[kScalar], wx[kScalar], mx[kScalar], vx[kScalar];
+#pragma unroll
+        for (int q = 0; q < kScalar; ++q) {
+            const int o = j + q * NT;
+            ux[q] = u0[o];
+            wx[q] = w0[o];
+            mx[q] = m0[o];
+            vx[q] = v0[o];
+        }
+#pragma unroll
+        for (int q = 0; q < kScalar; ++q) {
+            const int o = j + q * NT;
+            adamw1(ux[q], wx[q], mx[q], vx[q], k);
+            w0[o] = wx[q];
+            m0[o] = mx[q];
+            v0[o] = vx[q];
+            Param<PDT>::st1(p0, o, wx[q]);
+        }
+    }
+    for (; j < len; j += NT) one(j);
 }
 
 template <int NT, int PDT>
