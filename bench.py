@@ -112,9 +112,9 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key: str):
+def recorded_traffic(kernel_key: str, workload: str, layout: str):
     """DRAM bytes per launch of a kernel from the committed ncu summary, if it was taken
-    from the current kernel source (else None)."""
+    from the current kernel source on this workload and layout (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -125,6 +125,8 @@ def recorded_traffic(kernel_key: str):
             k, v = line.split("=", 1)
             kv[k.strip()] = v.strip()
     if kv.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    if kv.get("workload") != workload or kv.get("layout") != layout:
         return None
     v = kv.get(kernel_key + ".dram_bytes_per_launch")
     return float(v) if v else None
@@ -405,7 +407,8 @@ def run_gpu(args, rank, world, local_rank):
     out = {
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; random-init masters, N(0,1e-3) bf16 grads)",
+        "vs_baseline": None, "dtype": "f32",
+        "data": f"synthetic (seeded; random-init masters, N(0,{wl.grad_std:g}) {wl.grad_dtype} grads)",
         "config": {"workload": f"{wl.name}: ~1.24B-param Llama tensor list, {len(wl.numel)} tensors, P={P}, "
                                f"bf16 params/grads, fp32 master/m/v/acc, k={k} micro-batches"
                                if wl.name == "llama_1b" else
@@ -413,13 +416,13 @@ def run_gpu(args, rank, world, local_rank):
                                f"{wl.grad_dtype} grads, k={k}",
                    "P": P, "k": k, "tensors": len(wl.numel), "counts": gw.counts, "path": args.path,
                    "layout": args.layout,
-                   "l2": ("no flush: every launch streams >= 7.4 GB, far above the 129 MB L2" if P * 6 > 10 * 129e6
-                          else "small case: the working set fits in L2 (launch-latency bound)"),
+                   "l2": (f"no flush: every launch streams >= {P * 6 / 1e9:.1f} GB, far above the 129 MB L2"
+                          if P * 6 > 10 * 129e6 else "small case: the working set fits in L2 (launch-latency bound)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm": head["hbm"],
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
                      "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_kind": peak_kind,
-                     "traffic": recorded_traffic(TRAFFIC_KEYS.get(dom, dom))},
+                     "traffic": recorded_traffic(TRAFFIC_KEYS.get(dom, dom), wl.name, args.layout)},
         "kernels": kernels,
         "gpu_launches": head["launches"],
         "paths": {args.path: {k2: head[k2] for k2 in ("value", "ms_per_step", "hbm")},
