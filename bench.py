@@ -47,12 +47,14 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama_1b")
-    ap.add_argument("--path", choices=["resident", "per_microbatch"], default="resident",
+    ap.add_argument("--path", choices=["resident", "per_microbatch", "remat"], default="resident",
                     help="resident: the k micro-batch gradient lists are read in one pass (tl_accumulate_many); "
-                         "per_microbatch: one tl_accumulate per micro-batch")
+                         "per_microbatch: one tl_accumulate per micro-batch; remat (k <= 4): the lists are "
+                         "checked without storing u (tl_unscale_check_many) and the AdamW pass recomputes u "
+                         "from them")
     ap.add_argument("--layout", choices=["aligned", "packed", "misaligned"], default="aligned",
                     help="tensor placement inside the flat buffers (see GpuWorkload)")
-    ap.add_argument("--graph", action="store_true", help="also time both sequences replayed from a CUDA graph")
+    ap.add_argument("--graph", action="store_true", help="also time every sequence replayed from a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -284,6 +286,14 @@ class GpuWorkload:
         res = [("accumulate_many", many_bytes,
                 lambda: tl.tl_accumulate_many(self.ctx, self.many, self.counts, self.N, 1))]
         self.paths = {"resident": res + tail, "per_microbatch": per + tail}
+        if k <= 4:
+            # re-materialising: the lists are read twice (check, then AdamW), u never stored
+            self.paths["remat"] = [
+                ("unscale_check_many", k * sg,
+                 lambda: tl.tl_unscale_check_many(self.ctx, self.many, self.counts, self.N)),
+                tail[0],
+                ("clip_adamw_step_remat", 12 + 12 + sp + k * sg, lambda: tl.tl_clip_adamw_step(self.ctx, self.hp)),
+                tail[2]]
 
     def step_bytes(self, path):
         return self.P * sum(b for _, b, _ in self.paths[path] if b)
@@ -395,10 +405,12 @@ def run_gpu(args, rank, world, local_rank):
     gw = GpuWorkload(wl, device, args.layout)
     P, k = wl.P, wl.k
     with ClockSampler(gpu_id(local_rank)) as clk:
-        head = time_path(args, gw, args.path, world)
-        other_name = "per_microbatch" if args.path == "resident" else "resident"
-        other = time_path(args, gw, other_name, world)
-        graphs = {p: time_graph(args, gw, p, world) for p in (args.path, other_name)} if args.graph else None
+        if args.path not in gw.paths:
+            raise SystemExit(f"--path {args.path} needs k <= 4 micro-batches ({wl.name} has k = {k})")
+        names = [args.path] + [p for p in gw.paths if p != args.path]
+        timed = {p: time_path(args, gw, p, world) for p in names}
+        head = timed[args.path]
+        graphs = {p: time_graph(args, gw, p, world) for p in names} if args.graph else None
         e2e = None if args.no_e2e else run_e2e(args, gw, world)
     st = tl.tl_read_status(gw.ctx)
     kernels = head["kernels"]
@@ -425,8 +437,8 @@ def run_gpu(args, rank, world, local_rank):
                      "traffic": recorded_traffic(TRAFFIC_KEYS.get(dom, dom), wl.name, args.layout)},
         "kernels": kernels,
         "gpu_launches": head["launches"],
-        "paths": {args.path: {k2: head[k2] for k2 in ("value", "ms_per_step", "hbm")},
-                  other_name: {k2: other[k2] for k2 in ("value", "ms_per_step", "hbm", "kernels")}},
+        "paths": {p: {k2: timed[p][k2] for k2 in (("value", "ms_per_step", "hbm") if p == args.path else
+                                                   ("value", "ms_per_step", "hbm", "kernels"))} for p in names},
         "clocks": clk.summary(),
         **({"cuda_graph": graphs} if graphs else {}),
         "status": {"S": st.S, "t": st.t, "skipped": st.skipped, "norm": st.norm},
@@ -469,15 +481,23 @@ def run_e2e(args, gw, world):
             e.record(copy_stream)
             landed[b] = e
 
+    remat = args.path == "remat"
+
     def compute_step(step):
         b = step % 2
         compute.wait_event(landed[b])
-        tl.tl_accumulate_many(gw.ctx, many[b], gw.counts, gw.N, 1)
         e = torch.cuda.Event()
-        e.record(compute)
+        if remat:
+            tl.tl_unscale_check_many(gw.ctx, many[b], gw.counts, gw.N)
+            tl.tl_grad_norm(gw.ctx, gw.wl.max_norm)
+            tl.tl_clip_adamw_step(gw.ctx, gw.hp)   # the last reader of the lists
+            e.record(compute)
+        else:
+            tl.tl_accumulate_many(gw.ctx, many[b], gw.counts, gw.N, 1)
+            e.record(compute)
+            tl.tl_grad_norm(gw.ctx, gw.wl.max_norm)
+            tl.tl_clip_adamw_step(gw.ctx, gw.hp)
         released[b] = e
-        tl.tl_grad_norm(gw.ctx, gw.wl.max_norm)
-        tl.tl_clip_adamw_step(gw.ctx, gw.hp)
         tl.tl_scaler_update(gw.ctx)
 
     def run(nsteps):

@@ -189,6 +189,25 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
 int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64_t* n, int64_t N, int last,
                        tl_stream stream);
 
+/* A whole logical update over k <= 4 resident micro-batches without storing u
+ * (a2 for each and a3, re-materialising form).  [MEG] section 8 (real
+ * implementations fuse and flatten the copy / unscale / check path).  Reads the
+ * k lists (same layout as tl_accumulate_many) once and computes, per element and
+ * in registers only, u = fma(w_k, g_k, ... fma(w_2, g_2, w_1 g_1)) * (1/S): the
+ * operations and order of tl_accumulate_many, so the same u bit for bit.  It
+ * raises the overflow flag and writes the squared-norm partials; acc is neither
+ * read nor written.  tl_grad_norm follows as usual, and tl_clip_adamw_step then
+ * recomputes u from the same k lists instead of reading it from acc.  HBM bytes
+ * per parameter for the update: 26 + 4k (16-bit grads) instead of the resident
+ * pass's 34 + 2k, fewer for k < 4.  Opens an update (none may be open) and
+ * covers all of it: the counts must total N.  The context keeps the k lists'
+ * pointers (not their data) until tl_clip_adamw_step has been enqueued; the
+ * gradients must stay unchanged in device memory until that step has run.
+ * Errors: TL_EINVAL (k outside 1..4, counts, NULL or overlapping pointers),
+ * TL_ESTATE (an update is open). */
+int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const int64_t* n, int64_t N,
+                          tl_stream stream);
+
 /* Global L2 norm and clip coefficient (a4).  [MEG] section 9: global_norm =
  * sqrt(sum ||grad||^2), clip_coef = max_norm / (global_norm + eps); the
  * coefficient is applied only when below 1 (eps = 1e-6); max_norm <= 0
@@ -207,6 +226,8 @@ int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream);
  *   g = u*coef; m = b1*m + (1-b1)*g; v = b2*v + (1-b2)*(g*g);
  *   w = w - (lr*wd)*w; w = w - (lr/(1-b1^(t+1))) * (m / (sqrt(v)/sqrt(1-b2^(t+1)) + eps));
  *   param = round-to-nearest-even(w).
+ * u is read from acc, or, after tl_unscale_check_many, recomputed from the
+ * micro-batch lists that call was given.
  * If the overflow flag is set the kernel exits without touching any tensor.
  * Errors: TL_EINVAL (hp), TL_ESTATE. */
 int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream);

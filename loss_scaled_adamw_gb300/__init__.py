@@ -29,7 +29,8 @@ LIB_PATH = os.path.join(_PKG, "libtl_gb300.so")
 TL_OK, TL_EINVAL, TL_ECUDA, TL_ESTATE, TL_ENOMEM = 0, 1, 2, 3, 4
 TL_F32, TL_BF16, TL_F16 = 0, 1, 2
 
-EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "tl_unscale_check", "tl_grad_norm",
+EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "tl_unscale_check_many",
+            "tl_unscale_check", "tl_grad_norm",
             "tl_clip_adamw_step", "tl_scaler_update", "tl_read_status", "tl_get_state", "tl_set_state",
             "tl_scale_ptr", "tl_num_params", "tl_num_chunks", "tl_launch_count", "tl_status_string",
             "tl_last_error", "tl_unscale_norm_noalloc", "tl_loss_seed")
@@ -109,6 +110,7 @@ def load_library():
         "tl_destroy": (i32, [vp]),
         "tl_accumulate": (i32, [vp, pp, i64, i64, i32, vp]),
         "tl_accumulate_many": (i32, [vp, i32, pp, ctypes.POINTER(i64), i64, i32, vp]),
+        "tl_unscale_check_many": (i32, [vp, i32, pp, ctypes.POINTER(i64), i64, vp]),
         "tl_unscale_check": (i32, [vp, pp, i64, i64, vp]),
         "tl_grad_norm": (i32, [vp, f32, vp]),
         "tl_clip_adamw_step": (i32, [vp, ctypes.POINTER(tl_adamw_hp), vp]),
@@ -240,6 +242,15 @@ def tl_accumulate_many(ctx: Context, lists, counts: Sequence[int], N: int, last:
                                                                         int(last), _stream(stream)))
 
 
+def tl_unscale_check_many(ctx: Context, lists, counts: Sequence[int], N: int, stream=None) -> None:
+    ml = lists if isinstance(lists, ManyLists) else ManyLists(lists)
+    if len(counts) != ml.k:
+        raise ValueError("one count per gradient list")
+    cnt = (ctypes.c_int64 * max(ml.k, 1))(*[int(c) for c in counts])
+    _check(ctx, "tl_unscale_check_many", load_library().tl_unscale_check_many(ctx.handle, ml.k, ml.array, cnt, int(N),
+                                                                              _stream(stream)))
+
+
 def tl_unscale_check(ctx: Context, grads, n_k: int, N: int, stream=None) -> None:
     _check(ctx, "tl_unscale_check", load_library().tl_unscale_check(ctx.handle, _ptrs(grads), int(n_k), int(N),
                                                                     _stream(stream)))
@@ -297,17 +308,21 @@ def tl_launch_count(ctx: Context) -> int:
 
 
 def logical_update(ctx: Context, micro_batches, counts, max_norm: float, hp: tl_adamw_hp, stream=None,
-                   resident: bool = False) -> None:
+                   resident=False) -> None:
     """One attempted logical update: the tl_* call sequence over k micro-batches
     (micro_batches[i] is a tensor list or PtrList; counts[i] its valid targets).
-    resident=True reads all k lists in one pass (tl_accumulate_many); micro_batches
-    may then also be a prebuilt ManyLists."""
+    resident=True reads all k lists in one pass (tl_accumulate_many); resident="remat"
+    checks them without storing u (tl_unscale_check_many, k <= 4) and lets the AdamW
+    pass recompute u from them.  With either, micro_batches may also be a prebuilt
+    ManyLists."""
     k = micro_batches.k if isinstance(micro_batches, ManyLists) else len(micro_batches)
     if k < 1 or len(counts) != k:
         raise ValueError("need one count per micro-batch and at least one micro-batch")
     N = int(sum(int(c) for c in counts))
     s = _stream(stream)
-    if resident:
+    if resident == "remat":
+        tl_unscale_check_many(ctx, micro_batches, counts, N, s)
+    elif resident:
         tl_accumulate_many(ctx, micro_batches, counts, N, 1, s)
     else:
         for i in range(k - 1):

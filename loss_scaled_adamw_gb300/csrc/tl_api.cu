@@ -80,11 +80,19 @@ struct tl_ctx {
     int grid_uns[3][3][2] = {};
     int grid_adam[3][2] = {};
     int grid_many[3][8][2] = {};
+    int grid_check[3][2][2] = {};   // [grad dtype][few lists][part]
+    int grid_remat[3][3][2][2] = {};   // [param dtype][grad dtype][few lists][part]
     // the update in flight
     int phase = kIdle;
     int64_t n_sum = 0;
     int64_t N_update = 0;
     bool accumulated = false;
+    // a re-materialising update: u was never stored; the step recomputes it from
+    // these lists (list-major, ntensors pointers each) and counts
+    bool remat = false;
+    int remat_k = 0;
+    std::vector<const void*> remat_grads;
+    int64_t remat_n[kRematLists] = {};
     int64_t launches = 0;
     std::string last_error;
 };
@@ -246,6 +254,39 @@ cudaError_t over_parts(tl_ctx* ctx, Launch launch) {
         ctx->launches += 1;
     }
     return cudaSuccess;
+}
+
+// Resolve (and validate) k gradient lists (list-major, ntensors pointers each)
+// before any launch: a table by value when k lists fit in it, else one cached
+// device table per list.
+int resolve_lists(tl_ctx* ctx, int k, const void* const* grads, cudaStream_t s, bool* by_value,
+                  std::vector<const void* const*>& tabs, std::vector<GradSlot*>& slots) {
+    const int64_t nt = ctx->ntensors;
+    *by_value = nt <= kInlineMany / kMaxMany;
+    tabs.assign(size_t(k), nullptr);
+    slots.assign(size_t(k), nullptr);
+    if (nt == 0) return TL_OK;
+    for (int i = 0; i < k; ++i) {
+        const void* const* gi = grads + int64_t(i) * nt;
+        int rc = *by_value ? check_grads(ctx, gi) : resolve_device_table(ctx, gi, s, &tabs[size_t(i)], &slots[size_t(i)]);
+        if (rc != TL_OK) return rc;
+    }
+    return TL_OK;
+}
+
+// The kernel arguments of lists [j, j + kk) of a resolved set.
+void fill_many_args(const tl_ctx* ctx, const void* const* grads, const int64_t* n, int64_t N, int j, int kk,
+                    bool by_value, const std::vector<const void* const*>& tabs, ManyArgs& a, GradTableMany& inl) {
+    const int64_t nt = ctx->ntensors;
+    a = ManyArgs{};
+    a.k = kk;
+    a.ntensors = static_cast<int32_t>(nt);
+    for (int i = 0; i < kk; ++i) {
+        a.w[i] = static_cast<float>(static_cast<double>(n[j + i]) / static_cast<double>(N));
+        a.tabs[i] = by_value ? nullptr : tabs[size_t(j + i)];
+        if (by_value)
+            for (int64_t t = 0; t < nt; ++t) inl.p[int64_t(i) * nt + t] = grads[int64_t(j + i) * nt + t];
+    }
 }
 
 void free_ctx(tl_ctx* ctx) {
@@ -441,6 +482,12 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
             ctx->grid_adam[dt][part] = dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(2, dt, 0, small), n);
             for (int vr = 0; vr < 8; ++vr)
                 ctx->grid_many[dt][vr][part] = grid_for(ctx, blocks_per_sm(3, dt, vr, small), n);
+            for (int few = 0; few < 2; ++few)
+                ctx->grid_check[dt][few][part] = grid_for(ctx, blocks_per_sm(4, dt, few ? 4 : 0, small), n);
+            for (int gdt = 0; gdt < 3; ++gdt)
+                for (int few = 0; few < 2; ++few)
+                    ctx->grid_remat[dt][gdt][few][part] =
+                        dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(5, dt, gdt | (few ? 4 : 0), small), n);
         }
     }
     *out = ctx;
@@ -567,31 +614,17 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
     if (last && total != N) return fail(ctx, TL_EINVAL, "the counts do not add up to N");
     if ((rc = check_device(ctx)) != TL_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t nt = ctx->ntensors;
-    const bool by_value = nt <= kInlineMany / kMaxMany;
     static thread_local GradTableMany inl;
     // Resolve (and validate) every list before the first launch, so that an
     // error leaves nothing enqueued.
-    std::vector<const void* const*> tabs(size_t(k), nullptr);
-    std::vector<GradSlot*> slots(size_t(k), nullptr);
-    if (nt > 0) {
-        for (int i = 0; i < k; ++i) {
-            const void* const* gi = grads + int64_t(i) * nt;
-            rc = by_value ? check_grads(ctx, gi) : resolve_device_table(ctx, gi, s, &tabs[i], &slots[i]);
-            if (rc != TL_OK) return rc;
-        }
-    }
+    bool by_value = true;
+    std::vector<const void* const*> tabs;
+    std::vector<GradSlot*> slots;
+    if ((rc = resolve_lists(ctx, k, grads, s, &by_value, tabs, slots)) != TL_OK) return rc;
     for (int j = 0; j < k; j += kMaxMany) {
         const int kk = std::min(kMaxMany, k - j);
-        ManyArgs a{};
-        a.k = kk;
-        a.ntensors = static_cast<int32_t>(nt);
-        for (int i = 0; i < kk; ++i) {
-            a.w[i] = static_cast<float>(static_cast<double>(n[j + i]) / static_cast<double>(N));
-            a.tabs[i] = by_value ? nullptr : tabs[j + i];
-            if (by_value)
-                for (int64_t t = 0; t < nt; ++t) inl.p[int64_t(i) * nt + t] = grads[int64_t(j + i) * nt + t];
-        }
+        ManyArgs a;
+        fill_many_args(ctx, grads, n, N, j, kk, by_value, tabs, a, inl);
         const bool f = first && j == 0;
         const bool l = last && j + kk == k;
         if (ctx->nchunks > 0) {
@@ -609,6 +642,52 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
     ctx->n_sum = total;
     ctx->accumulated = true;
     ctx->phase = last ? kUnscaled : kAccum;
+    return TL_OK;
+}
+
+int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const int64_t* n, int64_t N,
+                          tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (k < 1 || k > kRematLists || n == nullptr)
+        return fail(ctx, TL_EINVAL, "need 1 <= k <= " + std::to_string(kRematLists) + " micro-batches and their counts");
+    if (grads == nullptr && ctx->ntensors > 0) return fail(ctx, TL_EINVAL, "grads must not be NULL");
+    if (ctx->phase != kIdle)
+        return fail(ctx, TL_ESTATE, "tl_unscale_check_many opens an update: finish the open one with tl_scaler_update");
+    int rc;
+    int64_t sum = 0;
+    for (int i = 0; i < k; ++i) {
+        if ((rc = check_counts(ctx, n[i], N)) != TL_OK) return rc;
+        sum += n[i];
+        if (sum > N) return fail(ctx, TL_EINVAL, "the counts exceed N");
+    }
+    if (sum != N) return fail(ctx, TL_EINVAL, "the counts do not add up to N");
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    static thread_local GradTableMany inl;
+    bool by_value = true;
+    std::vector<const void* const*> tabs;
+    std::vector<GradSlot*> slots;
+    if ((rc = resolve_lists(ctx, k, grads, s, &by_value, tabs, slots)) != TL_OK) return rc;
+    if (ctx->nchunks > 0) {
+        ManyArgs a;
+        fill_many_args(ctx, grads, n, N, 0, k, by_value, tabs, a, inl);
+        const int gdt = ctx->cfg.grad_dtype;
+        const int few = k <= kFewLists ? 1 : 0;
+        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+            return launch_check_many(gdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, a, ctx->d_state,
+                                     ctx->d_partials, ctx->grid_check[gdt][few][small ? 1 : 0], s);
+        });
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "many-list check launch");
+        for (int i = 0; i < k; ++i) mark_used(slots[size_t(i)], s);
+    }
+    ctx->remat = true;
+    ctx->remat_k = k;
+    ctx->remat_grads.assign(grads, grads + int64_t(k) * ctx->ntensors);
+    for (int i = 0; i < k; ++i) ctx->remat_n[i] = n[i];
+    ctx->N_update = N;
+    ctx->n_sum = N;
+    ctx->accumulated = true;
+    ctx->phase = kUnscaled;
     return TL_OK;
 }
 
@@ -644,6 +723,24 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         // the scaler kernel commits
         e = launch_adamw(pdt, false, ctx->d_chunks, ctx->d_cbegin, 0, 0, ctx->d_state, h, 1, s);
         if (e == cudaSuccess) ctx->launches += 1;
+    } else if (ctx->remat) {
+        // u recomputed from the lists the update was checked on (the same device
+        // tables: nothing else has used the cache since)
+        static thread_local GradTableMany inl;
+        bool by_value = true;
+        std::vector<const void* const*> tabs;
+        std::vector<GradSlot*> slots;
+        const int k = ctx->remat_k;
+        if ((rc = resolve_lists(ctx, k, ctx->remat_grads.data(), s, &by_value, tabs, slots)) != TL_OK) return rc;
+        ManyArgs a;
+        fill_many_args(ctx, ctx->remat_grads.data(), ctx->remat_n, ctx->N_update, 0, k, by_value, tabs, a, inl);
+        const int gdt = ctx->cfg.grad_dtype;
+        e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+            return launch_adamw_remat(pdt, gdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_state, h, inl, a,
+                                      ctx->grid_remat[pdt][gdt][k <= kFewLists ? 1 : 0][small ? 1 : 0], s);
+        });
+        if (e == cudaSuccess)
+            for (int i = 0; i < k; ++i) mark_used(slots[size_t(i)], s);
     } else {
         e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
             return launch_adamw(pdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_state, h,
@@ -669,6 +766,9 @@ int tl_scaler_update(tl_ctx* ctx, tl_stream stream) {
     ctx->n_sum = 0;
     ctx->N_update = 0;
     ctx->accumulated = false;
+    ctx->remat = false;
+    ctx->remat_k = 0;
+    ctx->remat_grads.clear();
     return TL_OK;
 }
 

@@ -76,6 +76,7 @@ struct GradTable {
 // Resident micro-batches read by one launch of the many-list kernel.
 constexpr int kMaxMany = 8;
 constexpr int kFewLists = 2;      // launches of at most this many lists use a kernel form of their own
+constexpr int kRematLists = 4;    // lists an update may re-materialise u from (beyond, the resident pass moves fewer bytes)
 constexpr int kInlineMany = 2048;  // k * ntensors gradient pointers travel by value up to this size
 
 struct GradTableMany {
@@ -122,6 +123,14 @@ cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, c
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
                               int64_t c0, int64_t c1, const GradTableMany& inl,
                               const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s);
+// The many-list pass without the store of u (all lists of the update at once),
+// and the AdamW pass that recomputes u from the same lists.
+cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+                              const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
+                              cudaStream_t s);
+cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+                               int64_t c1, DevState* st, AdamHP hp, const GradTableMany& inl, const ManyArgs& a,
+                               int grid, cudaStream_t s);
 cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevState* st, float max_norm,
                         cudaStream_t s);
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
@@ -131,7 +140,9 @@ cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s)
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0
-// FIRST, bit 1 LAST, bit 2 at most kFewLists lists).
+// FIRST, bit 1 LAST, bit 2 at most kFewLists lists), 4 many-list pass without the
+// store (variant bit 2 as for kind 3), 5 re-materialising adamw (dt = param dtype,
+// variant bits 0-1 = grad dtype, bit 2 at most kFewLists lists).
 int blocks_per_sm(int kind, int dt, int variant, bool small);
 
 }  // namespace tl

@@ -30,20 +30,35 @@ namespace {
 
 // Minimum resident CTAs per SM requested from the compiler (register budget) for
 // the many-list kernels (TL_MINB_FEW: launches of one or two lists, whose chunks
-// are worked faster when more of them are in flight) and the AdamW kernel.
+// are worked faster when more of them are in flight), the AdamW kernel and its
+// re-materialising form; *_UNROLL: 8-element vectors per thread per trip of the
+// AdamW loops.  The defaults are the fastest measured (one vector per thread at
+// 2 CTAs/SM equals two at 1 CTA/SM on the 1.24B list, 2-4 % faster on the
+// ragged 100k list, whose segments are mostly partial).
 #ifndef TL_MINB_MANY
 #define TL_MINB_MANY 3
 #endif
 #ifndef TL_MINB_FEW
 #define TL_MINB_FEW 5
 #endif
+#ifndef TL_REMAT_UNROLL
+#define TL_REMAT_UNROLL 1
+#endif
+#ifndef TL_MINB_REMAT_FEW
+#define TL_MINB_REMAT_FEW 3
+#endif
+#ifndef TL_MINB_REMAT
+#define TL_MINB_REMAT 2
+#endif
+#ifndef TL_ADAM_UNROLL
+#define TL_ADAM_UNROLL 1
+#endif
 #ifndef TL_MINB_ADAM
-#define TL_MINB_ADAM 1
+#define TL_MINB_ADAM 2
 #endif
 
 constexpr int kVec = 8;     // elements per vector access (16 B of a 16-bit stream)
 constexpr int kUnroll = 4;  // vectors in flight per thread in the accumulate/unscale kernels
-constexpr int kUnrollAdam = 2;
 constexpr int kScalar = 8;  // elements per thread in flight on the scalar path (streams of unequal phase)
 
 // ---------------------------------------------------------------------------
@@ -586,20 +601,23 @@ k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, 
 // of once per micro-batch.  FIRST: no partial sum in acc yet.  LAST: finish
 // with the unscale, overflow check and squared-norm partial of a3.
 // ---------------------------------------------------------------------------
-template <int NT, int GDT, bool FIRST, bool LAST, int KM>
+template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
 __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradTableMany& inl, const ManyArgs& a,
                                              float inv_s, SumSq& sq, bool& bad) {
     const int kk = a.k;
     float* __restrict__ acc0 = ch.acc;
     const char* g[KM];
-    bool al = aligned16(acc0);
+    // without the store of u the accumulation buffer is not touched: the lists
+    // alone decide the vector plan
+    bool al = !STORE || aligned16(acc0);
     bool same = true;
-    const int r = ephase<4>(acc0);
+    int r = STORE ? ephase<4>(acc0) : 0;
 #pragma unroll
     for (int q = 0; q < KM; ++q) {
         if (q < kk) {
             const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
             g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
+            if (!STORE && q == 0) r = ephase<Grad<GDT>::kBytes>(g[0]);
             al = al && aligned16(g[q]);
             same = same && ephase<Grad<GDT>::kBytes>(g[q]) == r;
         } else {
@@ -608,7 +626,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     }
     const int len = ch.len;
     VecPlan pl{0, false, false};
-    if (al) pl = VecPlan{0, true, aligned32(acc0)};
+    if (al) pl = VecPlan{0, true, !STORE || aligned32(acc0)};
     else if (same) pl = VecPlan{(8 - r) & 7, true, true};
     int head = 0, done = 0;
     if (pl.vec) {
@@ -650,7 +668,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
             float ax[8];
             if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
             mix(raw, ax);
-            st8_f32(acc + i * kVec, ax, wide);
+            if (STORE) st8_f32(acc + i * kVec, ax, wide);
         }
         done = head + nv * kVec;
     }
@@ -664,7 +682,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
             bad |= !isfinite(v);
             sq.one(v);
         }
-        acc0[j] = v;
+        if (STORE) acc0[j] = v;
     };
     for (int j = t; j < head; j += NT) one(j);          // head
     // tail, or the whole segment without a vector part: with one or two lists,
@@ -692,13 +710,13 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
                 bad |= !isfinite(v);
                 sq.one(v);
             }
-            acc0[j + e * NT] = v;
+            if (STORE) acc0[j + e * NT] = v;
         }
     }
     for (; j < len; j += NT) one(j);
 }
 
-template <int NT, int GDT, bool FIRST, bool LAST, int KM>
+template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
 __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
                                             : GDT == kF32 ? 2
                                             : KM <= kFewLists ? TL_MINB_FEW : TL_MINB_MANY)
@@ -710,12 +728,12 @@ k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegi
         SumSq sq;
         bool bad = false;
         if (NT == kThreads) {
-            many_segment<kThreads, GDT, FIRST, LAST, KM>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
+            many_segment<kThreads, GDT, FIRST, LAST, KM, STORE>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
         } else {
             const int b0 = cbegin[c];
             const int wi = threadIdx.x >> 5;
             if (wi < cbegin[c + 1] - b0)
-                many_segment<32, GDT, FIRST, LAST, KM>(chunks[b0 + wi], threadIdx.x & 31, inl, a, inv_s, sq, bad);
+                many_segment<32, GDT, FIRST, LAST, KM, STORE>(chunks[b0 + wi], threadIdx.x & 31, inl, a, inv_s, sq, bad);
         }
         if (LAST) finish_warp(sq, bad, c, st, partials);
     }
@@ -812,73 +830,160 @@ __device__ __forceinline__ void adamw1(float u, float& w, float& m, float& v, co
     w = __fsub_rn(wd, __fmul_rn(k.step, __fdiv_rn(m, denom)));
 }
 
-template <int NT, int PDT>
-__device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const AdamConsts& k) {
-    const float* __restrict__ u0 = ch.acc;
+// Where a segment's u comes from.  UFromAcc: the accumulation buffer holds u
+// (written by the unscale or many-list pass).  UFromLists: u is recomputed from
+// the resident micro-batch gradient lists in the operations of the many-list
+// pass (w_1 g_1, then fma(w_q, g_q, .) in list order, then times 1/S), so it is
+// the same value bit for bit; nothing is read from the accumulation buffer.
+struct UFromAcc {
+    static constexpr int kUnroll = TL_ADAM_UNROLL;
+    struct Raw {
+        float x[8];
+    };
+    const float* __restrict__ u0;
+    __device__ __forceinline__ explicit UFromAcc(const Chunk& ch) : u0(ch.acc) {}
+    __device__ __forceinline__ bool aligned16_all() const { return aligned16(u0); }
+    __device__ __forceinline__ bool aligned32_all() const { return aligned32(u0); }
+    __device__ __forceinline__ bool phase_is(int r) const { return ephase<4>(u0) == r; }
+    __device__ __forceinline__ void load(Raw& r, int o, bool wide) const { ld8_f32(u0 + o, r.x, wide); }
+    __device__ __forceinline__ void value(const Raw& r, float (&u)[8]) const {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = r.x[e];
+    }
+    __device__ __forceinline__ float at(int j) const { return u0[j]; }
+};
+
+template <int GDT, int KM>
+struct UFromLists {
+    static constexpr int kUnroll = TL_REMAT_UNROLL;
+    struct Raw {
+        typename GradRaw<GDT>::T r[KM];
+    };
+    const char* g[KM];
+    const float* w;  // micro-batch weights n_q / N
+    int kk;
+    float inv_s;
+    __device__ __forceinline__ UFromLists(const Chunk& ch, const GradTableMany& inl, const ManyArgs& a, float is)
+        : w(a.w), kk(a.k), inv_s(is) {
+#pragma unroll
+        for (int q = 0; q < KM; ++q) {
+            if (q < kk) {
+                const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
+                g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
+            } else {
+                g[q] = nullptr;
+            }
+        }
+    }
+    __device__ __forceinline__ bool aligned16_all() const {
+        bool al = true;
+#pragma unroll
+        for (int q = 0; q < KM; ++q)
+            if (q < kk) al = al && aligned16(g[q]);
+        return al;
+    }
+    __device__ __forceinline__ bool aligned32_all() const { return true; }  // 16-byte accesses only
+    __device__ __forceinline__ bool phase_is(int r) const {
+        bool same = true;
+#pragma unroll
+        for (int q = 0; q < KM; ++q)
+            if (q < kk) same = same && ephase<Grad<GDT>::kBytes>(g[q]) == r;
+        return same;
+    }
+    __device__ __forceinline__ void load(Raw& r, int o, bool) const {
+#pragma unroll
+        for (int q = 0; q < KM; ++q)
+            if (q < kk) r.r[q] = GradRaw<GDT>::ld(g[q], o);
+    }
+    __device__ __forceinline__ void value(const Raw& r, float (&u)[8]) const {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = __fmul_rn(w[0], GradRaw<GDT>::at(r.r[0], e));
+#pragma unroll
+        for (int q = 1; q < KM; ++q)
+            if (q < kk) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) u[e] = __fmaf_rn(w[q], GradRaw<GDT>::at(r.r[q], e), u[e]);
+            }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = __fmul_rn(u[e], inv_s);
+    }
+    __device__ __forceinline__ float at(int j) const {
+        float v = __fmul_rn(w[0], Grad<GDT>::ld1(g[0], j));
+#pragma unroll
+        for (int q = 1; q < KM; ++q)
+            if (q < kk) v = __fmaf_rn(w[q], Grad<GDT>::ld1(g[q], j), v);
+        return __fmul_rn(v, inv_s);
+    }
+};
+
+template <int NT, int PDT, class Src>
+__device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const AdamConsts& k, const Src& src) {
     float* __restrict__ w0 = ch.master;
     float* __restrict__ m0 = ch.m;
     float* __restrict__ v0 = ch.v;
     unsigned short* p0 = static_cast<unsigned short*>(ch.param);
     const int len = ch.len;
     VecPlan pl{0, false, false};
-    if (aligned16(u0) && aligned16(w0) && aligned16(m0) && aligned16(v0) && aligned16(p0)) {
-        pl = VecPlan{0, true, aligned32(u0) && aligned32(w0) && aligned32(m0) && aligned32(v0)};
+    if (src.aligned16_all() && aligned16(w0) && aligned16(m0) && aligned16(v0) && aligned16(p0)) {
+        pl = VecPlan{0, true, src.aligned32_all() && aligned32(w0) && aligned32(m0) && aligned32(v0)};
     } else {
-        const int r = ephase<4>(u0);
-        if (ephase<4>(w0) == r && ephase<4>(m0) == r && ephase<4>(v0) == r && ephase<2>(p0) == r)
+        const int r = ephase<4>(w0);
+        if (src.phase_is(r) && ephase<4>(m0) == r && ephase<4>(v0) == r && ephase<2>(p0) == r)
             pl = VecPlan{(8 - r) & 7, true, true};
     }
     int head = 0, done = 0;
     if (pl.vec) {
         head = min(pl.head, len);
         const bool wide = pl.wide;
-        const float* __restrict__ u = u0 + head;
-        float* __restrict__ w = w0 + head;
-        float* __restrict__ m = m0 + head;
-        float* __restrict__ v = v0 + head;
         void* p = p0 + head;
         const int nv = (len - head) / kVec;
+        constexpr int U = Src::kUnroll;
         int i = t;
-        for (; i + (kUnrollAdam - 1) * NT < nv; i += kUnrollAdam * NT) {
-            float ux[kUnrollAdam][8], wx[kUnrollAdam][8], mx[kUnrollAdam][8], vx[kUnrollAdam][8];
+        for (; i + (U - 1) * NT < nv; i += U * NT) {
+            typename Src::Raw ur[U];
+            float wx[U][8], mx[U][8], vx[U][8];
 #pragma unroll
-            for (int q = 0; q < kUnrollAdam; ++q) {
-                const int o = (i + q * NT) * kVec;
-                ld8_f32(u + o, ux[q], wide);
-                ld8_f32(w + o, wx[q], wide);
-                ld8_f32(m + o, mx[q], wide);
-                ld8_f32(v + o, vx[q], wide);
+            for (int q = 0; q < U; ++q) {
+                const int o = head + (i + q * NT) * kVec;
+                src.load(ur[q], o, wide);
+                ld8_f32(w0 + o, wx[q], wide);
+                ld8_f32(m0 + o, mx[q], wide);
+                ld8_f32(v0 + o, vx[q], wide);
             }
 #pragma unroll
-            for (int q = 0; q < kUnrollAdam; ++q) {
+            for (int q = 0; q < U; ++q) {
+                float ux[8];
+                src.value(ur[q], ux);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) adamw1(ux[q][e], wx[q][e], mx[q][e], vx[q][e], k);
-                const int o = (i + q * NT) * kVec;
-                st8_f32(w + o, wx[q], wide);
-                st8_f32(m + o, mx[q], wide);
-                st8_f32(v + o, vx[q], wide);
-                st8_param<PDT>(p, o, wx[q]);
+                for (int e = 0; e < 8; ++e) adamw1(ux[e], wx[q][e], mx[q][e], vx[q][e], k);
+                const int o = head + (i + q * NT) * kVec;
+                st8_f32(w0 + o, wx[q], wide);
+                st8_f32(m0 + o, mx[q], wide);
+                st8_f32(v0 + o, vx[q], wide);
+                st8_param<PDT>(p, (i + q * NT) * kVec, wx[q]);
             }
         }
         for (; i < nv; i += NT) {
+            typename Src::Raw ur;
             float ux[8], wx[8], mx[8], vx[8];
-            const int o = i * kVec;
-            ld8_f32(u + o, ux, wide);
-            ld8_f32(w + o, wx, wide);
-            ld8_f32(m + o, mx, wide);
-            ld8_f32(v + o, vx, wide);
+            const int o = head + i * kVec;
+            src.load(ur, o, wide);
+            ld8_f32(w0 + o, wx, wide);
+            ld8_f32(m0 + o, mx, wide);
+            ld8_f32(v0 + o, vx, wide);
+            src.value(ur, ux);
 #pragma unroll
             for (int e = 0; e < 8; ++e) adamw1(ux[e], wx[e], mx[e], vx[e], k);
-            st8_f32(w + o, wx, wide);
-            st8_f32(m + o, mx, wide);
-            st8_f32(v + o, vx, wide);
-            st8_param<PDT>(p, o, wx);
+            st8_f32(w0 + o, wx, wide);
+            st8_f32(m0 + o, mx, wide);
+            st8_f32(v0 + o, vx, wide);
+            st8_param<PDT>(p, i * kVec, wx);
         }
         done = head + nv * kVec;
     }
     auto one = [&](int j) {
         float wj = w0[j], mj = m0[j], vj = v0[j];
-        adamw1(u0[j], wj, mj, vj, k);
+        adamw1(src.at(j), wj, mj, vj, k);
         w0[j] = wj;
         m0[j] = mj;
         v0[j] = vj;
@@ -893,7 +998,7 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Adam
 #pragma unroll
         for (int q = 0; q < kScalar; ++q) {
             const int o = j + q * NT;
-            ux[q] = u0[o];
+            ux[q] = src.at(o);
             wx[q] = w0[o];
             mx[q] = m0[o];
             vx[q] = v0[o];
@@ -911,10 +1016,11 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Adam
     for (; j < len; j += NT) one(j);
 }
 
-template <int NT, int PDT>
-__global__ void __launch_bounds__(kThreads, TL_MINB_ADAM)
-k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
-        DevState* __restrict__ st, AdamHP hp) {
+// The per-step AdamW scalars (fp64 beta powers, bias corrections rounded to fp32
+// once), computed by one thread and shared through shared memory; CTA 0 also
+// records the beta powers of the update in flight for the scaler kernel to
+// commit.  Returns true when the update is skipped (overflow flag set).
+__device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const AdamHP& hp, AdamConsts& out) {
     __shared__ AdamConsts sk;
     __shared__ int skip;
     if (threadIdx.x == 0) {
@@ -939,15 +1045,52 @@ k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, in
         }
     }
     __syncthreads();
-    if (skip) return;
-    const AdamConsts k = sk;
+    out = sk;
+    return skip != 0;
+}
+
+template <int NT, int PDT>
+__global__ void __launch_bounds__(kThreads, TL_MINB_ADAM)
+k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+        DevState* __restrict__ st, AdamHP hp) {
+    AdamConsts k;
+    if (adam_consts(st, hp, k)) return;
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         if (NT == kThreads) {
-            adamw_segment<kThreads, PDT>(chunks[c], threadIdx.x, k);
+            const Chunk& ch = chunks[c];
+            adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromAcc(ch));
         } else {
             const int b0 = cbegin[c];
             const int wi = threadIdx.x >> 5;
-            if (wi < cbegin[c + 1] - b0) adamw_segment<32, PDT>(chunks[b0 + wi], threadIdx.x & 31, k);
+            if (wi < cbegin[c + 1] - b0) {
+                const Chunk& ch = chunks[b0 + wi];
+                adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromAcc(ch));
+            }
+        }
+    }
+}
+
+// The re-materialising AdamW pass: u of every element recomputed from the
+// resident gradient lists (at most KM <= kRematLists of them) instead of read.
+template <int NT, int PDT, int GDT, int KM>
+__global__ void __launch_bounds__(kThreads, KM <= kFewLists && GDT != kF32 ? TL_MINB_REMAT_FEW : TL_MINB_REMAT)
+k_adamw_remat(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+              DevState* __restrict__ st, AdamHP hp, const __grid_constant__ GradTableMany inl,
+              const __grid_constant__ ManyArgs a) {
+    AdamConsts k;
+    if (adam_consts(st, hp, k)) return;
+    const float inv_s = __fdiv_rn(1.0f, st->S);
+    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+        if (NT == kThreads) {
+            const Chunk& ch = chunks[c];
+            adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
+        } else {
+            const int b0 = cbegin[c];
+            const int wi = threadIdx.x >> 5;
+            if (wi < cbegin[c + 1] - b0) {
+                const Chunk& ch = chunks[b0 + wi];
+                adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
+            }
         }
     }
 }
@@ -1041,8 +1184,8 @@ UnsFn uns_fn(int gdt, int mode, bool small) { return small ? uns_fn_nt<32>(gdt, 
 
 template <int NT, int GDT, int KM>
 ManyFn many_fn_km(bool first, bool last) {
-    if (first) return last ? k_accum_many<NT, GDT, true, true, KM> : k_accum_many<NT, GDT, true, false, KM>;
-    return last ? k_accum_many<NT, GDT, false, true, KM> : k_accum_many<NT, GDT, false, false, KM>;
+    if (first) return last ? k_accum_many<NT, GDT, true, true, KM, true> : k_accum_many<NT, GDT, true, false, KM, true>;
+    return last ? k_accum_many<NT, GDT, false, true, KM, true> : k_accum_many<NT, GDT, false, false, KM, true>;
 }
 template <int NT, int GDT>
 ManyFn many_fn_dt(bool first, bool last, bool few) {
@@ -1061,6 +1204,49 @@ ManyFn many_fn_nt(int gdt, bool first, bool last, bool few) {
 
 ManyFn many_fn(int gdt, bool first, bool last, bool small, bool few) {
     return small ? many_fn_nt<32>(gdt, first, last, few) : many_fn_nt<kThreads>(gdt, first, last, few);
+}
+
+// the many-list pass without the store of u (first and last micro-batch at once)
+template <int NT>
+ManyFn check_fn_nt(int gdt, bool few) {
+    switch (gdt) {
+        case kBF16: return few ? k_accum_many<NT, kBF16, true, true, kFewLists, false>
+                               : k_accum_many<NT, kBF16, true, true, kMaxMany, false>;
+        case kF16: return few ? k_accum_many<NT, kF16, true, true, kFewLists, false>
+                              : k_accum_many<NT, kF16, true, true, kMaxMany, false>;
+        case kF32: return few ? k_accum_many<NT, kF32, true, true, kFewLists, false>
+                              : k_accum_many<NT, kF32, true, true, kMaxMany, false>;
+        default: return nullptr;
+    }
+}
+ManyFn check_fn(int gdt, bool small, bool few) { return small ? check_fn_nt<32>(gdt, few) : check_fn_nt<kThreads>(gdt, few); }
+
+using RematFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, DevState*, AdamHP, const GradTableMany,
+                         const ManyArgs);
+
+template <int NT, int PDT, int GDT>
+RematFn remat_fn_gdt(bool few) {
+    return few ? k_adamw_remat<NT, PDT, GDT, kFewLists> : k_adamw_remat<NT, PDT, GDT, kRematLists>;
+}
+template <int NT, int PDT>
+RematFn remat_fn_pdt(int gdt, bool few) {
+    switch (gdt) {
+        case kBF16: return remat_fn_gdt<NT, PDT, kBF16>(few);
+        case kF16: return remat_fn_gdt<NT, PDT, kF16>(few);
+        case kF32: return remat_fn_gdt<NT, PDT, kF32>(few);
+        default: return nullptr;
+    }
+}
+template <int NT>
+RematFn remat_fn_nt(int pdt, int gdt, bool few) {
+    switch (pdt) {
+        case kBF16: return remat_fn_pdt<NT, kBF16>(gdt, few);
+        case kF16: return remat_fn_pdt<NT, kF16>(gdt, few);
+        default: return nullptr;
+    }
+}
+RematFn remat_fn(int pdt, int gdt, bool small, bool few) {
+    return small ? remat_fn_nt<32>(pdt, gdt, few) : remat_fn_nt<kThreads>(pdt, gdt, few);
 }
 
 AdamFn adam_fn(int pdt, bool small) {
@@ -1108,6 +1294,24 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
     return cudaGetLastError();
 }
 
+cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+                              const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
+                              cudaStream_t s) {
+    ManyFn f = check_fn(gdt, small, a.k <= kFewLists);
+    if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, a, st, partials);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+                               int64_t c1, DevState* st, AdamHP hp, const GradTableMany& inl, const ManyArgs& a,
+                               int grid, cudaStream_t s) {
+    RematFn f = remat_fn(pdt, gdt, small, a.k <= kFewLists);
+    if (f == nullptr || a.k < 1 || a.k > kRematLists) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, st, hp, inl, a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
                          DevState* st, AdamHP hp, int grid, cudaStream_t s) {
     AdamFn f = adam_fn(pdt, small);
@@ -1133,6 +1337,8 @@ int blocks_per_sm(int kind, int dt, int variant, bool small) {
     else if (kind == 2) f = reinterpret_cast<const void*>(adam_fn(dt, small));
     else if (kind == 3)
         f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0, small, (variant & 4) != 0));
+    else if (kind == 4) f = reinterpret_cast<const void*>(check_fn(dt, small, (variant & 4) != 0));
+    else if (kind == 5) f = reinterpret_cast<const void*>(remat_fn(dt, variant & 3, small, (variant & 4) != 0));
     if (f == nullptr) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess || n < 1) return 1;
