@@ -24,8 +24,15 @@ _SRC = os.path.join(_HERE, "tlo.c")
 _LIB_PATH = os.path.join(_HERE, "libtlo.so")
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
-DT_F32, DT_BF16, DT_F16 = 0, 1, 2
-_DT_BY_NAME = {"f32": DT_F32, "bf16": DT_BF16, "f16": DT_F16}
+DT_F32, DT_BF16, DT_F16, DT_E4M3B16 = 0, 1, 2, 3
+_DT_BY_NAME = {"f32": DT_F32, "bf16": DT_BF16, "f16": DT_F16, "e4m3b16": DT_E4M3B16}
+
+
+class E4M3List(ctypes.Structure):
+    """One micro-batch of 8-bit gradients: E4M3 codes of every tensor back to back and
+    each tensor's ceil(numel/16) fp32 block scales back to back."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("numel", ctypes.c_void_p),
+                ("ntensors", ctypes.c_int64)]
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +89,8 @@ def _bind(lib):
         "tlo_f32_to_bf16": (u16, [f32]),
         "tlo_f32_to_f16": (u16, [f32]),
         "tlo_decode16": (None, [vp, vp, i64, i32]),
+        "tlo_e4m3_to_f32": (f32, [ctypes.c_uint8]),
+        "tlo_dequant_e4m3b16": (None, [ctypes.POINTER(E4M3List), vp]),
         "tlo_recast": (None, [vp, vp, i64, i32]),
         "tlo_microbatch_weight": (f32, [i64, i64]),
         "tlo_accumulate": (None, [vp, vp, i32, i64, f32, i32]),
@@ -132,8 +141,10 @@ class Oracle:
     def __init__(self, master: np.ndarray, param_bits: np.ndarray, param_dtype: str = "bf16",
                  grad_dtype: str = "bf16", scaler_enabled: bool = False, init_scale: float = 1.0,
                  growth: float = 2.0, backoff: float = 0.5, interval: int = 2000,
-                 min_scale: float = 1.0, max_scale: float = 2.0 ** 127, lib=None):
+                 min_scale: float = 1.0, max_scale: float = 2.0 ** 127, lib=None, numel=None):
         self.lib = lib if lib is not None else load()
+        # the tensor sizes, needed to place the block scales of 8-bit gradients
+        self.numel = None if numel is None else np.ascontiguousarray(numel, dtype=np.int64)
         self.w = np.ascontiguousarray(master, dtype=np.float32).copy()
         self.m = np.zeros_like(self.w)
         self.v = np.zeros_like(self.w)
@@ -152,12 +163,24 @@ class Oracle:
     def step(self, grads, counts, max_norm: float, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8,
              weight_decay=0.1) -> Result:
         """One attempted logical update over k micro-batches (grads[i] is a flat
-        array of P gradient values: uint16 bits for bf16/f16, float32 for f32)."""
+        array of P gradient values: uint16 bits for bf16/f16, float32 for f32; for
+        e4m3b16 a pair (uint8 codes of P elements, float32 block scales))."""
         k = len(grads)
-        gs = [np.ascontiguousarray(g) for g in grads]
-        for g in gs:
-            assert g.size == self.P
-        gptrs = (ctypes.c_void_p * k)(*[g.ctypes.data for g in gs])
+        if self.gdtype == DT_E4M3B16:
+            assert self.numel is not None and int(self.numel.sum()) == self.P
+            keep = []
+            for codes, scales in grads:
+                c = np.ascontiguousarray(codes, dtype=np.uint8)
+                sc = np.ascontiguousarray(scales, dtype=np.float32)
+                assert c.size == self.P and sc.size == int(((self.numel + 15) // 16).sum())
+                keep.append((c, sc, E4M3List(c.ctypes.data, sc.ctypes.data, self.numel.ctypes.data,
+                                              self.numel.size)))
+            gptrs = (ctypes.c_void_p * k)(*[ctypes.addressof(x[2]) for x in keep])
+        else:
+            gs = [np.ascontiguousarray(g) for g in grads]
+            for g in gs:
+                assert g.size == self.P
+            gptrs = (ctypes.c_void_p * k)(*[g.ctypes.data for g in gs])
         cnts = (ctypes.c_int64 * k)(*[int(c) for c in counts])
         hp = AdamWHP(lr, beta1, beta2, eps, weight_decay)
         res = Result()
@@ -190,4 +213,22 @@ def decode16(bits: np.ndarray, dtype: str) -> np.ndarray:
     bits = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
     out = np.empty(bits.size, dtype=np.float32)
     load().tlo_decode16(_ptr(bits), _ptr(out), bits.size, _DT_BY_NAME[dtype])
+    return out
+
+
+def e4m3_to_f32(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes -> fp32 (exact)."""
+    lib = load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.tlo_e4m3_to_f32(int(c)) for c in codes], dtype=np.float32)
+
+
+def dequant_e4m3b16(codes: np.ndarray, scales: np.ndarray, numel) -> np.ndarray:
+    """8-bit gradients of a tensor list -> fp32 values code * block scale."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8).ravel()
+    sc = np.ascontiguousarray(scales, dtype=np.float32).ravel()
+    n = np.ascontiguousarray(numel, dtype=np.int64)
+    out = np.empty(c.size, dtype=np.float32)
+    lst = E4M3List(c.ctypes.data, sc.ctypes.data, n.ctypes.data, n.size)
+    load().tlo_dequant_e4m3b16(ctypes.byref(lst), _ptr(out))
     return out

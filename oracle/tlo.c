@@ -43,15 +43,24 @@
  *   R6  AdamW: eps outside the square root, decoupled decay lr*wd applied to
  *       the pre-update master, bias corrections from fp64 beta powers;
  *   R7  with the scaler disabled (bf16), S stays fixed, count stays 0, and the
- *       finite check still gates the step.
+ *       finite check still gates the step;
+ *   R17 8-bit gradients: [T41] section 41.5 names E4M3 but does not print its
+ *       emulator; the OCP E4M3 layout is taken (bias 7, 3 mantissa bits,
+ *       subnormals, no infinity, S.1111.111 is NaN, largest finite 448);
+ *   R18 block scales run over each tensor's flattened elements in blocks of 16
+ *       (the section's block_size), and a tensor's last block may hold fewer
+ *       than 16 elements.
  */
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
 
+#include <stdlib.h>
+
 #define TLO_DT_F32 0
 #define TLO_DT_BF16 1
 #define TLO_DT_F16 2
+#define TLO_DT_E4M3B16 3
 
 /* ------------------------------------------------------------------------ */
 /* 16-bit formats.  [MP] section 2 "Two 16-bit formats": bf16 keeps fp32's   */
@@ -145,6 +154,45 @@ void tlo_decode16(const uint16_t* h, float* out, int64_t n, int dtype) {
 void tlo_recast(const float* x, uint16_t* out, int64_t n, int dtype) {
     for (int64_t j = 0; j < n; ++j)
         out[j] = (dtype == TLO_DT_F16) ? tlo_f32_to_f16(x[j]) : tlo_f32_to_bf16(x[j]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* 8-bit gradients with fine-grained scaling.  [T41] section 41.5 "FP8       */
+/* training with fine-grained scaling": one scale per block of values, the   */
+/* values stored in E4M3 relative to that scale and dequantized (code value  */
+/* times block scale) before accumulation.  READING R17 fixes the format.    */
+/* ------------------------------------------------------------------------ */
+float tlo_e4m3_to_f32(uint8_t c) {
+    const uint32_t sign = (uint32_t)(c >> 7) << 31;
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    if (e == 15u && m == 7u) return bits_f32(sign | 0x7FC00000u);    /* NaN */
+    if (e == 0u) {
+        /* subnormal: m * 2^-9, an exact product of a small integer and a power of two */
+        const float mag = (float)m * (1.0f / 512.0f);
+        return bits_f32(sign | f32_bits(mag));
+    }
+    /* normal: (1 + m/8) * 2^(e-7); binary32 exponent field e - 7 + 127, mantissa m in its top 3 bits */
+    return bits_f32(sign | ((e + 120u) << 23) | (m << 20));
+}
+
+/* The gradients of one micro-batch as E4M3 codes plus fp32 block scales: the
+ * codes of every tensor back to back (tensor order), and each tensor's
+ * ceil(numel/16) scales back to back (READING R18). */
+typedef struct {
+    const uint8_t* codes;
+    const float* scales;
+    const int64_t* numel;
+    int64_t ntensors;
+} tlo_e4m3_list;
+
+/* g[j] = fl32(e4m3(code[j]) * scale of j's block) over the whole list. */
+void tlo_dequant_e4m3b16(const tlo_e4m3_list* g, float* out) {
+    int64_t j = 0, b = 0;
+    for (int64_t t = 0; t < g->ntensors; ++t) {
+        for (int64_t e = 0; e < g->numel[t]; ++e, ++j)
+            out[j] = tlo_e4m3_to_f32(g->codes[j]) * g->scales[b + e / 16];
+        b += (g->numel[t] + 15) / 16;
+    }
 }
 
 static float load_grad(const void* g, int dtype, int64_t j) {
@@ -343,8 +391,22 @@ int tlo_step(float* w, float* m, float* v, uint16_t* p, int pdtype, float* acc, 
         N += counts[i];
     }
     if (N > ((int64_t)1 << 53)) return -1;
-    for (int i = 0; i < k; ++i)
-        tlo_accumulate(acc, grads[i], gdtype, P, tlo_microbatch_weight(counts[i], N), i == 0);
+    float* deq = NULL;
+    if (gdtype == TLO_DT_E4M3B16) {
+        deq = (float*)malloc(sizeof(float) * (size_t)(P > 0 ? P : 1));
+        if (deq == NULL) return -1;
+    }
+    for (int i = 0; i < k; ++i) {
+        const void* gi = grads[i];
+        int gdt = gdtype;
+        if (deq != NULL) {  /* 8-bit gradients: dequantize, then accumulate the fp32 values */
+            tlo_dequant_e4m3b16((const tlo_e4m3_list*)grads[i], deq);
+            gi = deq;
+            gdt = TLO_DT_F32;
+        }
+        tlo_accumulate(acc, gi, gdt, P, tlo_microbatch_weight(counts[i], N), i == 0);
+    }
+    free(deq);
     int found_inf = tlo_unscale_check(acc, P, st->S);
     double sumsq = 0.0;
     float norm = 0.0f, coef = 1.0f;

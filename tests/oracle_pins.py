@@ -550,4 +550,122 @@ def pin_state_bytes_per_param(lib):
     assert sum(parts.values()) + o.acc.itemsize == 20
 
 
+# ---- 8-bit gradients with fine-grained scaling ([T41] section 41.5) --------
+
+def _torch_e4m3(codes):
+    """Library decode of E4M3 codes: torch.float8_e4m3fn."""
+    import torch
+    return torch.tensor(np.asarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).float().numpy()
+
+
+def pin_e4m3_decode_matches_torch(lib):
+    """Library pin: every one of the 256 E4M3 codes decodes as torch.float8_e4m3fn does
+    (values bit for bit, signed zeros, NaN exactly at S.1111.111, no infinity)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ours = np.array([lib.tlo_e4m3_to_f32(int(c)) for c in codes], dtype=np.float32)
+    ref = _torch_e4m3(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert set(np.nonzero(nan)[0].tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+    assert not np.isinf(ours).any()
+
+
+def pin_e4m3_closed_forms(lib):
+    """R17's layout in closed form: largest finite 1.75 * 2^8 = 448, smallest subnormal
+    2^-9, smallest normal 2^-6, 0x38 = 1; the 127 non-negative finite codes increase."""
+    d = lambda c: lib.tlo_e4m3_to_f32(c)
+    assert d(0x7E) == 448.0 and d(0xFE) == -448.0
+    assert d(0x01) == 2.0 ** -9 and d(0x07) == 7 * 2.0 ** -9
+    assert d(0x08) == 2.0 ** -6 and d(0x38) == 1.0 and d(0x39) == 1.125
+    assert math.copysign(1.0, d(0x80)) == -1.0 and d(0x80) == 0.0
+    vals = [d(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(vals, vals[1:]))
+
+
+def _quantize_blocks(x, numel):
+    """[T41] section 41.5 recipe (block 16, per-block scale max|x|/448, 1 where the block
+    is zero, values coded relative to the scale), per tensor, with torch's RNE cast."""
+    import torch
+    codes, scales, o = [], [], 0
+    for n in numel:
+        t = torch.tensor(x[o:o + n], dtype=torch.float32)
+        nb = (n + 15) // 16
+        pad = torch.zeros(nb * 16, dtype=torch.float32)
+        pad[:n] = t
+        amax = pad.view(nb, 16).abs().amax(dim=1)
+        sc = amax / 448.0
+        sc = torch.where(sc == 0, torch.ones_like(sc), sc)
+        q = (pad.view(nb, 16) / sc[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(-1)[:n]
+        codes.append(q.numpy())
+        scales.append(sc.numpy())
+        o += n
+    return np.concatenate(codes), np.concatenate(scales).astype(np.float32)
+
+
+def pin_block_dequant_roundtrip(lib):
+    """[T41] section 41.5: a block's largest magnitude codes as 448 and dequantizes back to
+    itself within one fp32 rounding; every value of the normal E4M3 range comes back within
+    half an E4M3 step (relative 2^-4), every subnormal within 2^-10 of the block scale."""
+    rng = np.random.default_rng(41)
+    numel = [16, 5, 17, 33, 64]
+    x = (rng.standard_normal(sum(numel)) * np.exp(rng.uniform(-6, 6, sum(numel)))).astype(np.float32)
+    codes, scales = _quantize_blocks(x, numel)
+    dq = oracle.dequant_e4m3b16(codes, scales, numel)
+    o, b = 0, 0
+    for n in numel:
+        for blk in range(0, n, 16):
+            xs = x[o + blk:o + min(blk + 16, n)].astype(np.float64)
+            ds = dq[o + blk:o + min(blk + 16, n)].astype(np.float64)
+            s = float(scales[b])
+            i = int(np.argmax(np.abs(xs)))
+            assert abs(ds[i] - xs[i]) <= ulp32(xs[i]), (ds[i], xs[i])
+            rel = np.abs(xs) / s
+            normal = rel >= 2.0 ** -6
+            assert np.all(np.abs(ds - xs)[normal] <= 2.0 ** -4 * np.abs(xs)[normal] * (1 + 1e-6))
+            assert np.all(np.abs(ds - xs)[~normal] <= 2.0 ** -10 * s * (1 + 1e-6))
+            b += 1
+        o += n
+
+
+def pin_block_scales_follow_tensors(lib):
+    """R18: block scales run over each tensor separately (blocks of 16, a partial last
+    block per tensor): with every code 1.0 the dequantized list is each tensor's scales
+    repeated 16 times and cut to its size."""
+    numel = [5, 16, 17, 33, 1, 40]
+    nb = [(n + 15) // 16 for n in numel]
+    scales = (2.0 ** np.arange(1, sum(nb) + 1)).astype(np.float32)
+    codes = np.full(sum(numel), 0x38, dtype=np.uint8)
+    dq = oracle.dequant_e4m3b16(codes, scales, numel)
+    expect, b = [], 0
+    for n, k in zip(numel, nb):
+        expect.append(np.repeat(scales[b:b + k], 16)[:n])
+        b += k
+    assert np.array_equal(dq, np.concatenate(expect))
+
+
+def pin_e4m3_step_equals_step_on_dequantized(lib):
+    """The 8-bit path is the fp32 path on the dequantized values: one update with E4M3
+    gradients equals, bit for bit, the update with fp32 gradients code * scale."""
+    rng = np.random.default_rng(7)
+    numel = [40, 17, 3]
+    P = sum(numel)
+    master = rng.standard_normal(P).astype(np.float32) * 0.02
+    grads = [rng.standard_normal(P).astype(np.float32) * 1e-2 for _ in range(3)]
+    q = [_quantize_blocks(g, numel) for g in grads]
+    a = make_oracle(lib, master, pdtype="bf16", gdtype="f32")
+    b = oracle.Oracle(master, oracle.recast(master, "bf16"), param_dtype="bf16", grad_dtype="e4m3b16",
+                      lib=lib, numel=numel)
+    for _ in range(2):
+        ra = a.step([oracle.dequant_e4m3b16(c, s, numel) for c, s in q], [3, 1, 2], 1.0)
+        rb = b.step(q, [3, 1, 2], 1.0)
+        assert (ra.norm, ra.sumsq, ra.skipped) == (rb.norm, rb.sumsq, rb.skipped)
+    for f in ("w", "m", "v", "p"):
+        assert np.array_equal(getattr(a, f), getattr(b, f)), f
+    bad = [(c.copy(), s) for c, s in q]
+    bad[1][0][20] = 0x7F                                   # a NaN code flags the update
+    r = b.step(bad, [3, 1, 2], 1.0)
+    assert r.skipped == 1
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

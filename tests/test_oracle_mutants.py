@@ -66,6 +66,16 @@ MUTANTS = [
     ("f16_bias_off", "mag = ldexpf((float)(1024 + man), exp - 25);", "mag = ldexpf((float)(1024 + man), exp - 24);"),
     ("f16_subnormal_scale", "mag = ldexpf((float)man, -24);", "mag = ldexpf((float)man, -25);"),
     ("param_not_recast", "p[j] = (pdtype == TLO_DT_F16) ? tlo_f32_to_f16(wj) : tlo_f32_to_bf16(wj);", "(void)p;"),
+    # 8-bit gradients: E4M3 layout and block scales
+    ("e4m3_bias_off", "((e + 120u) << 23)", "((e + 121u) << 23)"),
+    ("e4m3_mantissa_shift", "| (m << 20));", "| (m << 21));"),
+    ("e4m3_subnormal_scale", "(float)m * (1.0f / 512.0f);", "(float)m * (1.0f / 1024.0f);"),
+    ("e4m3_no_nan", "if (e == 15u && m == 7u) return bits_f32(sign | 0x7FC00000u);", ";"),
+    ("e4m3_sign_dropped", "const uint32_t sign = (uint32_t)(c >> 7) << 31;", "const uint32_t sign = 0u;"),
+    ("block_index_over_list", "g->scales[b + e / 16];", "g->scales[j / 16];"),
+    ("block_size_8", "g->scales[b + e / 16];", "g->scales[b + e / 8];"),
+    ("scale_not_applied", "out[j] = tlo_e4m3_to_f32(g->codes[j]) * g->scales[b + e / 16];",
+     "out[j] = tlo_e4m3_to_f32(g->codes[j]);"),
 ]
 
 
