@@ -241,15 +241,35 @@ class GpuWorkload:
         self.m = torch.zeros(offsets(keys["m"])[1] + 16, dtype=torch.float32, device=device)
         self.v = torch.zeros(offsets(keys["v"])[1] + 16, dtype=torch.float32, device=device)
         self.acc = torch.empty(offsets(keys["acc"])[1] + 16, dtype=torch.float32, device=device)
+        fp8 = wl.grad_dtype == "e4m3b16"
+
+        def e4m3_buffer(pair, key):
+            # every tensor on a 16-byte boundary: codes padded to 16 bytes, then block scales
+            offs, soffs, total = W.e4m3_layout(wl.numel, layout == "misaligned", key)
+            codes, scales = pair
+            buf = torch.zeros(total + 16, dtype=torch.uint8, device=device)
+            n = torch.tensor(wl.numel, dtype=torch.int64)
+            nb = (n + 15) // 16
+            ci = torch.arange(P, dtype=torch.int64) + torch.repeat_interleave(
+                torch.tensor(offs, dtype=torch.int64) - (torch.cumsum(n, 0) - n), n)
+            si = torch.arange(int(nb.sum()), dtype=torch.int64) + torch.repeat_interleave(
+                torch.tensor(soffs, dtype=torch.int64) // 4 - (torch.cumsum(nb, 0) - nb), nb)
+            buf[ci.to(device)] = codes.to(device)
+            buf.view(torch.float32)[si.to(device)] = scales.to(device)
+            return buf
+
         self.grads = []
         for i in range(wl.k):
             g = W.grad_input(wl, 1, i, scale=gscale, device=device)
-            self.grads.append(spread(g, g.dtype, 10 + i))
+            self.grads.append(e4m3_buffer(g, 10 + i) if fp8 else spread(g, g.dtype, 10 + i))
             del g
 
         def plist(t, key):
             es, base = t.element_size(), t.data_ptr()
-            p = tl.PtrList([base + o * es for o in offsets(key)[0]])
+            if fp8 and key >= 10:   # a gradient list of 8-bit tensors: byte offsets of the layout above
+                p = tl.PtrList([base + o for o in W.e4m3_layout(wl.numel, layout == "misaligned", key)[0]])
+            else:
+                p = tl.PtrList([base + o * es for o in offsets(key)[0]])
             p.keep = t
             return p
 
@@ -257,7 +277,7 @@ class GpuWorkload:
         self.plists = {n: plist(getattr(self, n), keys[n]) for n in keys}
         self.gplists = [plist(g, 10 + i) for i, g in enumerate(self.grads)]
         self.many = tl.ManyLists(self.gplists)
-        dt = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32}
+        dt = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32, "e4m3b16": tl.TL_E4M3B16}
         cfg = tl.make_config(dt[wl.param_dtype], dt[wl.grad_dtype], wl.scaler_enabled,
                              wl.init_scale if wl.scaler_enabled else 1.0, interval=wl.interval)
         L = self.plists
@@ -265,7 +285,8 @@ class GpuWorkload:
         self.counts = wl.counts(1)
         self.N = sum(self.counts)
         self.hp = tl.tl_adamw_hp(1e-3, 0.9, 0.95, 1e-8, 0.1)
-        sg = {"bf16": 2, "f16": 2, "f32": 4}[wl.grad_dtype]
+        # gradient bytes per parameter (8-bit: the code and a quarter of a 4-byte scale)
+        sg = {"bf16": 2, "f16": 2, "f32": 4, "e4m3b16": 1.25}[wl.grad_dtype]
         sp = {"bf16": 2, "f16": 2}[wl.param_dtype]
         self.adam_bytes = 16 + 12 + sp
 

@@ -70,6 +70,16 @@ extern "C" {
 #define TL_F32 0
 #define TL_BF16 1
 #define TL_F16 2
+/* 8-bit gradients with fine-grained scaling ("Training at Scale", section 41.5:
+ * one scale per block of values, the values stored in E4M3 relative to it and
+ * dequantized before accumulation).  A gradient tensor of numel elements is one
+ * buffer that starts on a 16-byte boundary: numel E4M3 codes (OCP layout: 1
+ * sign, 4 exponent bits with bias 7, 3 mantissa bits; S.1111.111 is NaN),
+ * padded to a multiple of 16 bytes, then ceil(numel / 16) fp32 block scales.
+ * Element j of the tensor is the product, rounded to fp32, of the value of code
+ * j and scale j / 16 (integer division); a tensor's last block may hold fewer
+ * than 16 elements.  Gradient dtype only. */
+#define TL_E4M3B16 3
 
 typedef struct tl_ctx tl_ctx;
 
@@ -86,7 +96,7 @@ typedef void* tl_stream;
  * gates every update. */
 typedef struct {
     int32_t param_dtype;    /* TL_BF16 or TL_F16: the model copy */
-    int32_t grad_dtype;     /* TL_BF16, TL_F16 or TL_F32: the micro-batch gradients */
+    int32_t grad_dtype;     /* TL_BF16, TL_F16, TL_F32 or TL_E4M3B16: the micro-batch gradients */
     int32_t scaler_enabled; /* 1: dynamic loss scaling; 0: S = 1 fixed */
     float init_scale;       /* S0 > 0, a power of two (e.g. 65536) */
     float growth;           /* > 1, a power of two (2) */

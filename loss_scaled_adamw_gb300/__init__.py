@@ -27,7 +27,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtl_gb300.so")
 
 TL_OK, TL_EINVAL, TL_ECUDA, TL_ESTATE, TL_ENOMEM = 0, 1, 2, 3, 4
-TL_F32, TL_BF16, TL_F16 = 0, 1, 2
+TL_F32, TL_BF16, TL_F16, TL_E4M3B16 = 0, 1, 2, 3
 
 EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "tl_unscale_check_many",
             "tl_unscale_check", "tl_grad_norm",

@@ -22,7 +22,14 @@ namespace {
 
 enum Phase { kIdle = 0, kAccum = 1, kUnscaled = 2, kNormed = 3, kStepped = 4 };
 
-int elem_size(int dt) { return dt == TL_F32 ? 4 : 2; }
+int elem_size(int dt) { return dt == TL_F32 ? 4 : dt == TL_E4M3B16 ? 1 : 2; }
+
+// Bytes of one gradient tensor of n elements (8-bit: codes padded to 16 bytes,
+// then one fp32 scale per block of 16).
+uintptr_t grad_bytes(int dt, int64_t n) {
+    if (dt == TL_E4M3B16) return uintptr_t((n + 15) / 16 * 16 + (n + 15) / 16 * 4);
+    return uintptr_t(n) * uintptr_t(elem_size(dt));
+}
 
 bool is_pow2(float x) {
     if (!(x > 0.0f) || !std::isfinite(x)) return false;
@@ -76,12 +83,12 @@ struct tl_ctx {
     uint64_t clock = 0;
     int64_t nbig = 0;              // chunks [0, nbig) are whole-CTA segments, [nbig, nchunks) small-tensor groups
     // persistent grid sizes per kernel variant, [..][0] for the whole-CTA part, [..][1] for the groups
-    int grid_acc[3][2][2] = {};
-    int grid_uns[3][3][2] = {};
+    int grid_acc[kGradTypes][2][2] = {};
+    int grid_uns[kGradTypes][3][2] = {};
     int grid_adam[3][2] = {};
-    int grid_many[3][8][2] = {};
-    int grid_check[3][2][2] = {};   // [grad dtype][few lists][part]
-    int grid_remat[3][3][2][2] = {};   // [param dtype][grad dtype][few lists][part]
+    int grid_many[kGradTypes][8][2] = {};
+    int grid_check[kGradTypes][2][2] = {};        // [grad dtype][few lists][part]
+    int grid_remat[3][kGradTypes][2][2] = {};     // [param dtype][grad dtype][few lists][part]
     // the update in flight
     int phase = kIdle;
     int64_t n_sum = 0;
@@ -120,7 +127,7 @@ bool overlaps_any(const std::vector<Interval>& sorted, uintptr_t lo, uintptr_t h
 
 int check_config(const tl_config* c, std::string& why) {
     if (c->param_dtype != TL_BF16 && c->param_dtype != TL_F16) { why = "param_dtype must be TL_BF16 or TL_F16"; return TL_EINVAL; }
-    if (c->grad_dtype != TL_BF16 && c->grad_dtype != TL_F16 && c->grad_dtype != TL_F32) { why = "grad_dtype must be TL_BF16, TL_F16 or TL_F32"; return TL_EINVAL; }
+    if (c->grad_dtype != TL_BF16 && c->grad_dtype != TL_F16 && c->grad_dtype != TL_F32 && c->grad_dtype != TL_E4M3B16) { why = "grad_dtype must be TL_BF16, TL_F16, TL_F32 or TL_E4M3B16"; return TL_EINVAL; }
     if (c->scaler_enabled != 0 && c->scaler_enabled != 1) { why = "scaler_enabled must be 0 or 1"; return TL_EINVAL; }
     if (c->scaler_enabled) {
         if (!is_pow2(c->init_scale)) { why = "init_scale must be a positive power of two"; return TL_EINVAL; }
@@ -152,13 +159,17 @@ int check_device(tl_ctx* ctx) {
 // Validate a gradient list against the context (sizes implied, alignment, no
 // overlap with anything the kernels write).
 int check_grads(tl_ctx* ctx, const void* const* grads) {
-    const int es = elem_size(ctx->cfg.grad_dtype);
+    const int dt = ctx->cfg.grad_dtype;
+    // 8-bit gradients: each tensor's codes start on a 16-byte boundary, so its
+    // segments (multiples of 16 elements apart) never split an 8-element vector
+    // across two scale blocks
+    const uintptr_t align = dt == TL_E4M3B16 ? 16 : uintptr_t(elem_size(dt));
     for (int64_t i = 0; i < ctx->ntensors; ++i) {
         if (ctx->numel[i] == 0) continue;
         const uintptr_t a = reinterpret_cast<uintptr_t>(grads[i]);
         if (a == 0) return fail(ctx, TL_EINVAL, "NULL gradient pointer for tensor " + std::to_string(i));
-        if (a % es != 0) return fail(ctx, TL_EINVAL, "misaligned gradient pointer for tensor " + std::to_string(i));
-        if (overlaps_any(ctx->state_iv, a, a + uintptr_t(ctx->numel[i]) * es))
+        if (a % align != 0) return fail(ctx, TL_EINVAL, "misaligned gradient pointer for tensor " + std::to_string(i));
+        if (overlaps_any(ctx->state_iv, a, a + grad_bytes(dt, ctx->numel[i])))
             return fail(ctx, TL_EINVAL, "gradient tensor " + std::to_string(i) + " overlaps a state tensor");
     }
     return TL_OK;
@@ -384,7 +395,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     // the descriptor of elements [st, st + len) of tensor i, with its state addresses
     auto seg = [&](int64_t i, int64_t st, int64_t len) {
         return Chunk{acc[i] + st, master[i] + st, m[i] + st, v[i] + st,
-                     static_cast<char*>(param[i]) + st * pes, st, int32_t(i), int32_t(len), 0};
+                     static_cast<char*>(param[i]) + st * pes, st, int32_t(i), int32_t(len), (numel[i] + 15) / 16 * 16};
     };
     for (int64_t i = 0; i < ntensors; ++i) {
         if (numel[i] == 0) continue;
@@ -471,23 +482,22 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
-    // Persistent grid sizes from the occupancy of each kernel variant.
+    // Persistent grid sizes from the occupancy of each kernel variant the
+    // context's dtypes can launch.
+    const int gdt = cfg->grad_dtype, pdt = cfg->param_dtype;
     for (int part = 0; part < 2; ++part) {
         const bool small = part == 1;
         const int64_t n = small ? nchunks - nbig : nbig;
-        for (int dt = 0; dt < 3; ++dt) {
-            for (int f = 0; f < 2; ++f) ctx->grid_acc[dt][f][part] = grid_for(ctx, blocks_per_sm(0, dt, f, small), n);
-            for (int md = 0; md < 3; ++md)
-                ctx->grid_uns[dt][md][part] = grid_for(ctx, blocks_per_sm(1, dt, md, small), n);
-            ctx->grid_adam[dt][part] = dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(2, dt, 0, small), n);
-            for (int vr = 0; vr < 8; ++vr)
-                ctx->grid_many[dt][vr][part] = grid_for(ctx, blocks_per_sm(3, dt, vr, small), n);
-            for (int few = 0; few < 2; ++few)
-                ctx->grid_check[dt][few][part] = grid_for(ctx, blocks_per_sm(4, dt, few ? 4 : 0, small), n);
-            for (int gdt = 0; gdt < 3; ++gdt)
-                for (int few = 0; few < 2; ++few)
-                    ctx->grid_remat[dt][gdt][few][part] =
-                        dt == TL_F32 ? 1 : grid_for(ctx, blocks_per_sm(5, dt, gdt | (few ? 4 : 0), small), n);
+        for (int f = 0; f < 2; ++f) ctx->grid_acc[gdt][f][part] = grid_for(ctx, blocks_per_sm(0, gdt, f, small), n);
+        for (int md = 0; md < 3; ++md)
+            ctx->grid_uns[gdt][md][part] = grid_for(ctx, blocks_per_sm(1, gdt, md, small), n);
+        ctx->grid_adam[pdt][part] = grid_for(ctx, blocks_per_sm(2, pdt, 0, small), n);
+        for (int vr = 0; vr < 8; ++vr)
+            ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr, small), n);
+        for (int few = 0; few < 2; ++few) {
+            ctx->grid_check[gdt][few][part] = grid_for(ctx, blocks_per_sm(4, gdt, few ? 4 : 0, small), n);
+            ctx->grid_remat[pdt][gdt][few][part] =
+                grid_for(ctx, blocks_per_sm(5, pdt, gdt | (few ? 4 : 0), small), n);
         }
     }
     *out = ctx;

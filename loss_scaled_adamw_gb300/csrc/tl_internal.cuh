@@ -32,11 +32,15 @@ constexpr int kInlineGrads = 512;    // gradient pointer tables up to this size 
 constexpr int kF32 = 0;
 constexpr int kBF16 = 1;
 constexpr int kF16 = 2;
+constexpr int kE4M3 = 3;   // 8-bit codes + fp32 scale per block of 16 (gradients only)
+constexpr int kGradTypes = 4;
 
 // One segment: elements [start, start + len) of tensor `tensor` (64 bytes).  The
 // state-list addresses of its first element are stored in the descriptor, so a
 // kernel reaches the data one load after the descriptor; the gradient lists,
 // which change from call to call, are indexed by tensor and offset by start.
+// gscale is the byte offset from a tensor's gradient pointer to its block
+// scales (8-bit gradients: the codes rounded up to 16 bytes).
 // Chunk c covers segments [cbegin[c], cbegin[c + 1]); in the whole-CTA part of
 // the table chunk c is segment c.
 struct Chunk {
@@ -48,7 +52,7 @@ struct Chunk {
     int64_t start;
     int32_t tensor;
     int32_t len;
-    int64_t reserved;
+    int64_t gscale;
 };
 
 // Device-resident scalars of one context.

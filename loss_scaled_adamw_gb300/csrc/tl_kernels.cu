@@ -24,6 +24,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 namespace tl {
 namespace {
@@ -154,29 +155,40 @@ __device__ __forceinline__ void unpack_f16x2(uint32_t r, float& lo, float& hi) {
     hi = f.y;
 }
 
+// Two E4M3 codes (the low byte first) to fp32, exactly: the hardware converts
+// E4M3 pairs to fp16 pairs (every E4M3 value, NaN included, is an fp16 value).
+__device__ __forceinline__ void unpack_e4m3x2(uint32_t codes2, float& lo, float& hi) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes2 & 0xffffu), __NV_E4M3);
+    unpack_f16x2(static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16), lo, hi);
+}
+
 // Micro-batch gradient streams: read once per kernel, through the read-only path.
+// Element i of a segment's stream `base`; `sc` points at the segment's block
+// scales (8-bit gradients only; the other types ignore it).  A segment starts
+// on a multiple of 16 elements and 8-bit vectors sit on multiples of 8, so the
+// 8 elements of one vector share one scale.
 template <int DT> struct Grad;
 
 template <> struct Grad<kBF16> {
     static constexpr int kBytes = 2;
-    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8]) {
+    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8], const float*) {
         const uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
         unpack_bf16x2(r.x, x[0], x[1]); unpack_bf16x2(r.y, x[2], x[3]);
         unpack_bf16x2(r.z, x[4], x[5]); unpack_bf16x2(r.w, x[6], x[7]);
     }
-    __device__ static __forceinline__ float ld1(const void* base, int64_t i) {
+    __device__ static __forceinline__ float ld1(const void* base, int64_t i, const float*) {
         return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(base) + i)) << 16);
     }
 };
 
 template <> struct Grad<kF16> {
     static constexpr int kBytes = 2;
-    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8]) {
+    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8], const float*) {
         const uint4 r = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
         unpack_f16x2(r.x, x[0], x[1]); unpack_f16x2(r.y, x[2], x[3]);
         unpack_f16x2(r.z, x[4], x[5]); unpack_f16x2(r.w, x[6], x[7]);
     }
-    __device__ static __forceinline__ float ld1(const void* base, int64_t i) {
+    __device__ static __forceinline__ float ld1(const void* base, int64_t i, const float*) {
         const unsigned short b = __ldg(static_cast<const unsigned short*>(base) + i);
         return __half2float(__ushort_as_half(b));
     }
@@ -184,16 +196,42 @@ template <> struct Grad<kF16> {
 
 template <> struct Grad<kF32> {
     static constexpr int kBytes = 4;
-    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8]) {
+    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8], const float*) {
         const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
         const float4 a = __ldg(p), b = __ldg(p + 1);
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     }
-    __device__ static __forceinline__ float ld1(const void* base, int64_t i) {
+    __device__ static __forceinline__ float ld1(const void* base, int64_t i, const float*) {
         return __ldg(static_cast<const float*>(base) + i);
     }
 };
+
+// 8-bit gradients: element value = fl32(code value * block scale) ("Training at
+// Scale", section 41.5: dequantize before accumulation).
+template <> struct Grad<kE4M3> {
+    static constexpr int kBytes = 1;
+    __device__ static __forceinline__ void ld8(const void* base, int64_t i, float (&x)[8], const float* sc) {
+        const uint2 c = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(base) + i));
+        const float s = __ldg(sc + (i >> 4));
+        unpack_e4m3x2(c.x, x[0], x[1]); unpack_e4m3x2(c.x >> 16, x[2], x[3]);
+        unpack_e4m3x2(c.y, x[4], x[5]); unpack_e4m3x2(c.y >> 16, x[6], x[7]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], s);
+    }
+    __device__ static __forceinline__ float ld1(const void* base, int64_t i, const float* sc) {
+        float lo, hi;
+        unpack_e4m3x2(__ldg(static_cast<const unsigned char*>(base) + i), lo, hi);
+        return __fmul_rn(lo, __ldg(sc + (i >> 4)));
+    }
+};
+
+// The block scales of a segment's 8-bit gradient stream (nullptr for the other types).
+template <int GDT>
+__device__ __forceinline__ const float* grad_scales(const void* base, const Chunk& ch) {
+    if (GDT != kE4M3) return nullptr;
+    return reinterpret_cast<const float*>(static_cast<const char*>(base) + ch.gscale) + (ch.start >> 4);
+}
 
 // Raw 16-byte loads of 8 gradient elements and the exact conversion of element e
 // (for the many-list kernel, which keeps only the raw words live).
@@ -201,7 +239,7 @@ template <int DT> struct GradRaw;
 
 template <> struct GradRaw<kBF16> {
     using T = uint4;
-    __device__ static __forceinline__ T ld(const void* base, int64_t i) {
+    __device__ static __forceinline__ T ld(const void* base, int64_t i, const float*) {
         return __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
     }
     __device__ static __forceinline__ float at(const T& r, int e) {
@@ -212,7 +250,7 @@ template <> struct GradRaw<kBF16> {
 
 template <> struct GradRaw<kF16> {
     using T = uint4;
-    __device__ static __forceinline__ T ld(const void* base, int64_t i) {
+    __device__ static __forceinline__ T ld(const void* base, int64_t i, const float*) {
         return __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
     }
     __device__ static __forceinline__ float at(const T& r, int e) {
@@ -223,7 +261,7 @@ template <> struct GradRaw<kF16> {
 
 template <> struct GradRaw<kF32> {
     struct T { float4 a, b; };
-    __device__ static __forceinline__ T ld(const void* base, int64_t i) {
+    __device__ static __forceinline__ T ld(const void* base, int64_t i, const float*) {
         const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
         return T{__ldg(p), __ldg(p + 1)};
     }
@@ -231,6 +269,19 @@ template <> struct GradRaw<kF32> {
         const float4& h = e < 4 ? r.a : r.b;
         const int k = e & 3;
         return k == 0 ? h.x : k == 1 ? h.y : k == 2 ? h.z : h.w;
+    }
+};
+
+template <> struct GradRaw<kE4M3> {
+    struct T { uint2 c; float s; };
+    __device__ static __forceinline__ T ld(const void* base, int64_t i, const float* sc) {
+        return T{__ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(base) + i)), __ldg(sc + (i >> 4))};
+    }
+    __device__ static __forceinline__ float at(const T& r, int e) {
+        const uint32_t w = e < 4 ? r.c.x : r.c.y;
+        float lo, hi;
+        unpack_e4m3x2((e & 2) ? (w >> 16) : w, lo, hi);
+        return __fmul_rn((e & 1) ? hi : lo, r.s);
     }
 };
 
@@ -305,11 +356,14 @@ __device__ __forceinline__ int ephase(const void* p) {
 template <int NT, int GDT, bool FIRST>
 __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const void* const* gp, float w) {
     float* __restrict__ acc0 = ch.acc;
-    const char* g0 = static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes;
+    const void* gb = gp[ch.tensor];
+    const char* g0 = static_cast<const char*>(gb) + ch.start * Grad<GDT>::kBytes;
+    const float* sc = grad_scales<GDT>(gb, ch);
     const int len = ch.len;
     VecPlan pl{0, false, false};
     if (aligned16(acc0) && aligned16(g0)) pl = VecPlan{0, true, aligned32(acc0)};
     else if (ephase<4>(acc0) == ephase<Grad<GDT>::kBytes>(g0)) pl = VecPlan{(8 - ephase<4>(acc0)) & 7, true, true};
+    if (GDT == kE4M3 && pl.head != 0) pl.vec = false;  // an 8-bit vector must not straddle two blocks
     int head = 0, done = 0;
     if (pl.vec) {
         head = min(pl.head, len);
@@ -321,7 +375,7 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
         for (; i + (kUnroll - 1) * NT < nv; i += kUnroll * NT) {
             float gx[kUnroll][8], ax[kUnroll][8];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * NT) * kVec, gx[u]);
+            for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * NT) * kVec, gx[u], sc);
             if (!FIRST) {
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) ld8_f32(acc + (i + u * NT) * kVec, ax[u], wide);
@@ -336,7 +390,7 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
         }
         for (; i < nv; i += NT) {
             float gx[8], ax[8];
-            Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
+            Grad<GDT>::ld8(g, int64_t(i) * kVec, gx, sc);
             if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ax[e] = FIRST ? __fmul_rn(w, gx[e]) : __fmaf_rn(w, gx[e], ax[e]);
@@ -345,7 +399,7 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
         done = head + nv * kVec;
     }
     auto one = [&](int j) {
-        const float gj = Grad<GDT>::ld1(g0, j);
+        const float gj = Grad<GDT>::ld1(g0, j, sc);
         acc0[j] = FIRST ? __fmul_rn(w, gj) : __fmaf_rn(w, gj, acc0[j]);
     };
     for (int j = t; j < head; j += NT) one(j);          // head
@@ -356,7 +410,7 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
         float gx[kScalar], ax[kScalar];
 #pragma unroll
         for (int q = 0; q < kScalar; ++q) {
-            gx[q] = Grad<GDT>::ld1(g0, j + q * NT);
+            gx[q] = Grad<GDT>::ld1(g0, j + q * NT, sc);
             if (!FIRST) ax[q] = acc0[j + q * NT];
         }
 #pragma unroll
@@ -494,11 +548,14 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
     constexpr bool kReadG = MODE != kAccOnly;
     constexpr bool kReadAcc = MODE != kFirstOnly;
     float* __restrict__ acc0 = ch.acc;
-    const char* g0 = kReadG ? static_cast<const char*>(gp[ch.tensor]) + ch.start * Grad<GDT>::kBytes : nullptr;
+    const void* gb = kReadG ? gp[ch.tensor] : nullptr;
+    const char* g0 = kReadG ? static_cast<const char*>(gb) + ch.start * Grad<GDT>::kBytes : nullptr;
+    const float* sc = kReadG ? grad_scales<GDT>(gb, ch) : nullptr;
     const int len = ch.len;
     VecPlan pl{0, false, false};
     if (aligned16(acc0) && (!kReadG || aligned16(g0))) pl = VecPlan{0, true, aligned32(acc0)};
     else if (!kReadG || ephase<4>(acc0) == ephase<Grad<GDT>::kBytes>(g0)) pl = VecPlan{(8 - ephase<4>(acc0)) & 7, true, true};
+    if (kReadG && GDT == kE4M3 && pl.head != 0) pl.vec = false;  // an 8-bit vector must not straddle two blocks
     int head = 0, done = 0;
     if (pl.vec) {
         head = min(pl.head, len);
@@ -511,7 +568,7 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
             float gx[kUnroll][8], ax[kUnroll][8];
             if (kReadG) {
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * NT) * kVec, gx[u]);
+                for (int u = 0; u < kUnroll; ++u) Grad<GDT>::ld8(g, int64_t(i + u * NT) * kVec, gx[u], sc);
             }
             if (kReadAcc) {
 #pragma unroll
@@ -531,7 +588,7 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
         }
         for (; i < nv; i += NT) {
             float gx[8], ax[8];
-            if (kReadG) Grad<GDT>::ld8(g, int64_t(i) * kVec, gx);
+            if (kReadG) Grad<GDT>::ld8(g, int64_t(i) * kVec, gx, sc);
             if (kReadAcc) ld8_f32(acc + i * kVec, ax, wide);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -544,7 +601,7 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
         done = head + nv * kVec;
     }
     auto one = [&](int j) {
-        const float u = unscale1<MODE>(kReadAcc ? acc0[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g0, j) : 0.0f, w, inv_s);
+        const float u = unscale1<MODE>(kReadAcc ? acc0[j] : 0.0f, kReadG ? Grad<GDT>::ld1(g0, j, sc) : 0.0f, w, inv_s);
         acc0[j] = u;
         bad |= !isfinite(u);
         sq.one(u);
@@ -558,7 +615,7 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
 #pragma unroll
         for (int q = 0; q < kScalar; ++q) {
             ax[q] = kReadAcc ? acc0[j + q * NT] : 0.0f;
-            gx[q] = kReadG ? Grad<GDT>::ld1(g0, j + q * NT) : 0.0f;
+            gx[q] = kReadG ? Grad<GDT>::ld1(g0, j + q * NT, sc) : 0.0f;
         }
 #pragma unroll
         for (int q = 0; q < kScalar; ++q) {
@@ -607,6 +664,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     const int kk = a.k;
     float* __restrict__ acc0 = ch.acc;
     const char* g[KM];
+    const float* gs[KM];  // block scales (8-bit gradients)
     // without the store of u the accumulation buffer is not touched: the lists
     // alone decide the vector plan
     bool al = !STORE || aligned16(acc0);
@@ -617,17 +675,20 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         if (q < kk) {
             const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
             g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
+            gs[q] = grad_scales<GDT>(base, ch);
             if (!STORE && q == 0) r = ephase<Grad<GDT>::kBytes>(g[0]);
             al = al && aligned16(g[q]);
             same = same && ephase<Grad<GDT>::kBytes>(g[q]) == r;
         } else {
             g[q] = nullptr;
+            gs[q] = nullptr;
         }
     }
     const int len = ch.len;
     VecPlan pl{0, false, false};
     if (al) pl = VecPlan{0, true, !STORE || aligned32(acc0)};
     else if (same) pl = VecPlan{(8 - r) & 7, true, true};
+    if (GDT == kE4M3 && pl.head != 0) pl.vec = false;  // an 8-bit vector must not straddle two blocks
     int head = 0, done = 0;
     if (pl.vec) {
         head = min(pl.head, len);
@@ -664,7 +725,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
             typename GradRaw<GDT>::T raw[KM];
 #pragma unroll
             for (int q = 0; q < KM; ++q)
-                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q] + gofs, int64_t(i) * kVec);
+                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q] + gofs, int64_t(i) * kVec, gs[q]);
             float ax[8];
             if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
             mix(raw, ax);
@@ -673,10 +734,11 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         done = head + nv * kVec;
     }
     auto one = [&](int j) {
-        float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j)) : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j), acc0[j]);
+        float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j, gs[0]))
+                        : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j, gs[0]), acc0[j]);
 #pragma unroll
         for (int q = 1; q < KM; ++q)
-            if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j), v);
+            if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j, gs[q]), v);
         if (LAST) {
             v = __fmul_rn(v, inv_s);
             bad |= !isfinite(v);
@@ -696,7 +758,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         for (int e = 0; e < S; ++e) {
 #pragma unroll
             for (int q = 0; q < KM; ++q)
-                if (q < kk) gx[e][q] = Grad<GDT>::ld1(g[q], j + e * NT);
+                if (q < kk) gx[e][q] = Grad<GDT>::ld1(g[q], j + e * NT, gs[q]);
             if (!FIRST) ax[e] = acc0[j + e * NT];
         }
 #pragma unroll
@@ -719,7 +781,8 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
 template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
 __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
                                             : GDT == kF32 ? 2
-                                            : KM <= kFewLists ? TL_MINB_FEW : TL_MINB_MANY)
+                                            : KM <= kFewLists ? (GDT == kE4M3 ? TL_MINB_FEW - 1 : TL_MINB_FEW)
+                                            : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
              const __grid_constant__ GradTableMany inl,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
@@ -837,6 +900,7 @@ __device__ __forceinline__ void adamw1(float u, float& w, float& m, float& v, co
 // the same value bit for bit; nothing is read from the accumulation buffer.
 struct UFromAcc {
     static constexpr int kUnroll = TL_ADAM_UNROLL;
+    static constexpr bool kBlocked = false;
     struct Raw {
         float x[8];
     };
@@ -859,7 +923,9 @@ struct UFromLists {
     struct Raw {
         typename GradRaw<GDT>::T r[KM];
     };
+    static constexpr bool kBlocked = GDT == kE4M3;  // vectors must start on multiples of 8 elements
     const char* g[KM];
+    const float* gs[KM];  // block scales (8-bit gradients)
     const float* w;  // micro-batch weights n_q / N
     int kk;
     float inv_s;
@@ -870,8 +936,10 @@ struct UFromLists {
             if (q < kk) {
                 const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
                 g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
+                gs[q] = grad_scales<GDT>(base, ch);
             } else {
                 g[q] = nullptr;
+                gs[q] = nullptr;
             }
         }
     }
@@ -893,7 +961,7 @@ struct UFromLists {
     __device__ __forceinline__ void load(Raw& r, int o, bool) const {
 #pragma unroll
         for (int q = 0; q < KM; ++q)
-            if (q < kk) r.r[q] = GradRaw<GDT>::ld(g[q], o);
+            if (q < kk) r.r[q] = GradRaw<GDT>::ld(g[q], o, gs[q]);
     }
     __device__ __forceinline__ void value(const Raw& r, float (&u)[8]) const {
 #pragma unroll
@@ -908,10 +976,10 @@ struct UFromLists {
         for (int e = 0; e < 8; ++e) u[e] = __fmul_rn(u[e], inv_s);
     }
     __device__ __forceinline__ float at(int j) const {
-        float v = __fmul_rn(w[0], Grad<GDT>::ld1(g[0], j));
+        float v = __fmul_rn(w[0], Grad<GDT>::ld1(g[0], j, gs[0]));
 #pragma unroll
         for (int q = 1; q < KM; ++q)
-            if (q < kk) v = __fmaf_rn(w[q], Grad<GDT>::ld1(g[q], j), v);
+            if (q < kk) v = __fmaf_rn(w[q], Grad<GDT>::ld1(g[q], j, gs[q]), v);
         return __fmul_rn(v, inv_s);
     }
 };
@@ -931,6 +999,7 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Adam
         if (src.phase_is(r) && ephase<4>(m0) == r && ephase<4>(v0) == r && ephase<2>(p0) == r)
             pl = VecPlan{(8 - r) & 7, true, true};
     }
+    if (Src::kBlocked && pl.head != 0) pl.vec = false;  // an 8-bit vector must not straddle two blocks
     int head = 0, done = 0;
     if (pl.vec) {
         head = min(pl.head, len);
@@ -1154,6 +1223,7 @@ AccFn acc_fn_nt(int gdt, bool first) {
         case kBF16: return first ? k_accumulate<NT, kBF16, true> : k_accumulate<NT, kBF16, false>;
         case kF16: return first ? k_accumulate<NT, kF16, true> : k_accumulate<NT, kF16, false>;
         case kF32: return first ? k_accumulate<NT, kF32, true> : k_accumulate<NT, kF32, false>;
+        case kE4M3: return first ? k_accumulate<NT, kE4M3, true> : k_accumulate<NT, kE4M3, false>;
         default: return nullptr;
     }
 }
@@ -1176,6 +1246,7 @@ UnsFn uns_fn_nt(int gdt, int mode) {
         case kBF16: return uns_fn_dt<NT, kBF16>(mode);
         case kF16: return uns_fn_dt<NT, kF16>(mode);
         case kF32: return uns_fn_dt<NT, kF32>(mode);
+        case kE4M3: return uns_fn_dt<NT, kE4M3>(mode);
         default: return nullptr;
     }
 }
@@ -1198,6 +1269,7 @@ ManyFn many_fn_nt(int gdt, bool first, bool last, bool few) {
         case kBF16: return many_fn_dt<NT, kBF16>(first, last, few);
         case kF16: return many_fn_dt<NT, kF16>(first, last, few);
         case kF32: return many_fn_dt<NT, kF32>(first, last, few);
+        case kE4M3: return many_fn_dt<NT, kE4M3>(first, last, few);
         default: return nullptr;
     }
 }
@@ -1216,6 +1288,8 @@ ManyFn check_fn_nt(int gdt, bool few) {
                               : k_accum_many<NT, kF16, true, true, kMaxMany, false>;
         case kF32: return few ? k_accum_many<NT, kF32, true, true, kFewLists, false>
                               : k_accum_many<NT, kF32, true, true, kMaxMany, false>;
+        case kE4M3: return few ? k_accum_many<NT, kE4M3, true, true, kFewLists, false>
+                               : k_accum_many<NT, kE4M3, true, true, kMaxMany, false>;
         default: return nullptr;
     }
 }
@@ -1234,6 +1308,7 @@ RematFn remat_fn_pdt(int gdt, bool few) {
         case kBF16: return remat_fn_gdt<NT, PDT, kBF16>(few);
         case kF16: return remat_fn_gdt<NT, PDT, kF16>(few);
         case kF32: return remat_fn_gdt<NT, PDT, kF32>(few);
+        case kE4M3: return remat_fn_gdt<NT, PDT, kE4M3>(few);
         default: return nullptr;
     }
 }

@@ -23,6 +23,10 @@ Workloads (all seeded with 39):
                   one element of micro-batch 1 at step 2; 3 steps.
   stream_64m      16 x 4M = 64M parameters, bf16, k=3: a small case of the same kernels for
                   hardware-counter captures (each list larger than L2).
+  fp8_small       8-bit gradients ("Training at Scale" section 41.5: E4M3 codes with one fp32
+                  scale per block of 16): 10 tensors (4,096 x 6 and 1, 17, 1,000, 33,333), bf16
+                  params, k=3, grads N(0, 1e-2), a NaN code in micro-batch 2 of step 3; 4 steps.
+  llama_1b_fp8    the llama_1b tensor list and counts with 8-bit block-scaled gradients.
 Every workload uses AdamW lr 1e-3, betas (0.9, 0.95), eps 1e-8, weight decay 0.1 and
 master weights N(0, 0.02).
 """
@@ -43,7 +47,7 @@ class Workload:
     name: str
     numel: List[int]
     param_dtype: str          # "bf16" | "f16"
-    grad_dtype: str           # "bf16" | "f16" | "f32"
+    grad_dtype: str           # "bf16" | "f16" | "f32" | "e4m3b16"
     steps: int
     k: int
     grad_std: float
@@ -117,6 +121,12 @@ def make(name: str) -> Workload:
         return Workload(name, nm, "f16", "f16", steps=3, k=2, grad_std=1e-2, scaler_enabled=True,
                         init_scale=2.0 ** 14, interval=2000, grads_prescaled=True,
                         injections={(2, 0): [(int(sum(nm) * 0.61803), 0x7C00)]})
+    if name == "fp8_small":
+        return Workload(name, [4096] * 6 + [1, 17, 1000, 33333], "bf16", "e4m3b16", steps=4, k=3, grad_std=1e-2,
+                        injections={(3, 1): [(4096 * 6 + 500, 0x7F)]})
+    if name == "llama_1b_fp8":
+        return Workload(name, llama_numel(2048, 16, 8192, 128256, 512), "bf16", "e4m3b16", steps=5, k=8,
+                        grad_std=1e-3)
     if name == "stream_64m":
         # a small case of the 1.24B workload's kernels for counter captures: every list
         # is larger than the 129 MB L2 while the whole case holds ~1.5 GB of HBM
@@ -124,7 +134,7 @@ def make(name: str) -> Workload:
     raise KeyError(name)
 
 
-NAMES = ("bf16_small", "fp16_scaled", "llama_10m", "llama_1b", "ragged_100k")
+NAMES = ("bf16_small", "fp16_scaled", "llama_10m", "llama_1b", "ragged_100k", "fp8_small", "llama_1b_fp8")
 
 
 # ---------------------------------------------------------------------------
@@ -161,11 +171,17 @@ def grad_fp32(wl: Workload, step: int, mb: int, device="cpu", lo: int = 0, hi: O
 def grad_input(wl: Workload, step: int, mb: int, scale: float = 1.0, device="cpu"):
     """The gradient handed to the optimizer for micro-batch mb of step (1-based step):
     the gradient of the micro-batch mean loss times S, in grad_dtype, with the workload's
-    inf/NaN injections applied."""
+    inf/NaN injections applied.  For e4m3b16 a pair (uint8 codes of the whole list in
+    tensor order, fp32 block scales of every tensor in tensor order)."""
     import torch
     g = grad_fp32(wl, step, mb, device)
     if wl.grads_prescaled:
         g = g * float(scale)      # S is a power of two: exact in fp32
+    if wl.grad_dtype == "e4m3b16":
+        codes, scales = quantize_e4m3b16(g, wl.numel)
+        for idx, bits in wl.injections.get((step, mb), []):
+            codes[idx] = bits
+        return codes, scales
     if wl.grad_dtype == "f32":
         out = g
     else:
@@ -176,6 +192,47 @@ def grad_input(wl: Workload, step: int, mb: int, scale: float = 1.0, device="cpu
         else:
             out.view(torch.int16)[idx] = np.int16(np.uint16(bits).view(np.int16)).item()
     return out
+
+
+def quantize_e4m3b16(x, numel: List[int]):
+    """What a producer of 8-bit gradients hands over ("Training at Scale" section 41.5
+    recipe): per tensor, blocks of 16 consecutive elements (the last one may be short),
+    scale = max |x| over the block / 448 (1 for an all-zero block), codes = E4M3 of
+    x / scale rounded to nearest even (torch's float8_e4m3fn cast).  Returns (uint8 codes,
+    P elements; fp32 scales, every tensor's blocks in tensor order)."""
+    import torch
+    dev = x.device
+    n = torch.tensor(numel, dtype=torch.int64, device=dev)
+    nb = (n + 15) // 16
+    start = torch.cumsum(n, 0) - n
+    pstart = (torch.cumsum(nb, 0) - nb) * 16
+    P = int(n.sum())
+    # position of every element in a layout where each tensor is padded to whole blocks
+    pos = torch.arange(P, dtype=torch.int64, device=dev) + torch.repeat_interleave(pstart - start, n)
+    padded = torch.zeros(int(nb.sum()) * 16, dtype=torch.float32, device=dev)
+    padded[pos] = x.float()
+    blocks = padded.view(-1, 16)
+    scale = blocks.abs().amax(dim=1) / 448.0
+    scale = torch.where(scale == 0, torch.ones_like(scale), scale)
+    codes = (blocks / scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(-1)[pos]
+    return codes.contiguous(), scale.contiguous()
+
+
+def e4m3_layout(numel: List[int], gaps: bool, seed_key: int) -> Tuple[List[int], List[int], int]:
+    """Byte offsets of each 8-bit gradient tensor in one flat buffer: every tensor starts on
+    a 16-byte boundary (with gaps, after a seeded 0-3 x 16 byte gap) and holds its codes
+    padded to 16 bytes, then its block scales.  Returns (tensor offsets, scale offsets,
+    total bytes)."""
+    rng = np.random.default_rng([SEED, 6, seed_key])
+    gap = rng.integers(0, 4, len(numel)) if gaps else np.zeros(len(numel), np.int64)
+    offs, soffs, pos = [], [], 0
+    for n, g in zip(numel, gap):
+        pos += 16 * int(g)
+        nb = (int(n) + 15) // 16
+        offs.append(pos)
+        soffs.append(pos + 16 * nb)
+        pos = (pos + 20 * nb + 15) // 16 * 16
+    return offs, soffs, pos
 
 
 def layout_offsets(numel: List[int], gaps: bool, align_elems: int, seed_key: int) -> Tuple[List[int], int]:

@@ -13,7 +13,7 @@ import numpy as np
 import loss_scaled_adamw_gb300 as tl
 from loss_scaled_adamw_gb300 import workloads as W
 
-DT = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32}
+DT = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32, "e4m3b16": tl.TL_E4M3B16}
 
 
 def ordered32(a: np.ndarray) -> np.ndarray:
@@ -100,6 +100,35 @@ class DeviceList:
         return self.buf[self.index]
 
 
+class E4M3DeviceList:
+    """One list of 8-bit gradient tensors in a flat device buffer: each tensor starts on a
+    16-byte boundary and holds its E4M3 codes (padded to 16 bytes) and then its fp32 block
+    scales; gaps=True puts a seeded 0-3 x 16 byte gap before every tensor."""
+
+    def __init__(self, numel, gaps, key: int, device="cuda"):
+        import torch
+        self.numel = list(numel)
+        offs, soffs, total = W.e4m3_layout(self.numel, bool(gaps), key)
+        self.buf = torch.full((total + 16,), 0xEE, dtype=torch.uint8, device=device)
+        n = torch.tensor(self.numel, dtype=torch.int64)
+        nb = (n + 15) // 16
+        P, NB = int(n.sum()), int(nb.sum())
+        self.code_index = (torch.arange(P, dtype=torch.int64) + torch.repeat_interleave(
+            torch.tensor(offs, dtype=torch.int64) - (torch.cumsum(n, 0) - n), n)).to(device)
+        # scale b of tensor t sits at byte soffs[t] + 4 b, i.e. float index soffs[t] / 4 + b
+        self.scale_index = (torch.arange(NB, dtype=torch.int64) + torch.repeat_interleave(
+            torch.tensor(soffs, dtype=torch.int64) // 4 - (torch.cumsum(nb, 0) - nb), nb)).to(device)
+        base = self.buf.data_ptr()
+        self.ptrs = tl.PtrList([base + o for o in offs])
+        self.ptrs.keep = self.buf
+
+    def load(self, pair):
+        import torch
+        codes, scales = pair
+        self.buf[self.code_index] = codes.to(self.buf.device)
+        self.buf.view(torch.float32)[self.scale_index] = scales.to(self.buf.device)
+
+
 class GpuOptimizer:
     """The GPU library over one workload's tensor list."""
 
@@ -129,8 +158,11 @@ class GpuOptimizer:
     def grad_list(self, slot: int, flat):
         """Place a flat gradient tensor into the device grad list `slot`."""
         if slot not in self.grad_lists:
-            self.grad_lists[slot] = DeviceList(self.wl.numel, self.wl.grad_dtype, self.gaps, 100 + slot + self.key,
-                                               self.device)
+            if self.wl.grad_dtype == "e4m3b16":
+                self.grad_lists[slot] = E4M3DeviceList(self.wl.numel, self.gaps, 100 + slot + self.key, self.device)
+            else:
+                self.grad_lists[slot] = DeviceList(self.wl.numel, self.wl.grad_dtype, self.gaps,
+                                                   100 + slot + self.key, self.device)
         self.grad_lists[slot].load(flat)
         return self.grad_lists[slot].ptrs
 
@@ -160,12 +192,15 @@ def oracle_for(wl: W.Workload, master0):
     p0 = W.to_16bit(master0.cpu(), wl.param_dtype).view(torch.int16).numpy().view(np.uint16)
     return oracle.Oracle(master0.cpu().numpy().astype(np.float32), p0, param_dtype=wl.param_dtype,
                          grad_dtype=wl.grad_dtype, scaler_enabled=wl.scaler_enabled,
-                         init_scale=wl.init_scale, interval=wl.interval)
+                         init_scale=wl.init_scale, interval=wl.interval, numel=wl.numel)
 
 
 def grad_bits(g):
-    """numpy view of a gradient tensor for the oracle (uint16 bits or float32)."""
+    """numpy view of a gradient tensor for the oracle (uint16 bits or float32; for 8-bit
+    gradients the pair of codes and block scales)."""
     import torch
+    if isinstance(g, tuple):
+        return g[0].cpu().numpy(), g[1].cpu().numpy()
     g = g.cpu()
     if g.dtype == torch.float32:
         return g.numpy()
