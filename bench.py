@@ -560,8 +560,16 @@ def oracle_sample(wl, n_params: int):
     n = min(n_params, wl.P)
     g = torch.Generator().manual_seed(W.SEED)
     master = (torch.randn(n, generator=g) * wl.master_std).numpy().astype(np.float32)
-    grads = [W.to_16bit(torch.randn(n, generator=g) * wl.grad_std, wl.grad_dtype).view(torch.int16).numpy()
-             .view(np.uint16) for _ in range(wl.k)]
+    grads = []
+    for _ in range(wl.k):
+        x = torch.randn(n, generator=g) * wl.grad_std
+        if wl.grad_dtype == "e4m3b16":      # the slice taken as one tensor of n elements
+            codes, scales = W.quantize_e4m3b16(x, [n])
+            grads.append((codes.numpy(), scales.numpy()))
+        elif wl.grad_dtype == "f32":
+            grads.append(x.numpy().astype(np.float32))
+        else:
+            grads.append(W.to_16bit(x, wl.grad_dtype).view(torch.int16).numpy().view(np.uint16))
     p0 = W.to_16bit(torch.from_numpy(master), wl.param_dtype).view(torch.int16).numpy().view(np.uint16)
     return master, p0, grads
 
@@ -573,7 +581,7 @@ def time_oracle(wl, seconds: float, steps=None):
     import oracle
     n = 1 << 20
     master, p0, grads = oracle_sample(wl, n)
-    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype)
+    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype, numel=[master.size])
     t = time.perf_counter()
     o.step(grads, wl.counts(1), wl.max_norm)
     per_param = (time.perf_counter() - t) / n
@@ -581,7 +589,7 @@ def time_oracle(wl, seconds: float, steps=None):
     if steps is None:
         steps = max(1, int(round(seconds / (per_param * n))))
     master, p0, grads = oracle_sample(wl, n)
-    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype)
+    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype, numel=[master.size])
     t = time.perf_counter()
     for s in range(steps):
         o.step(grads, wl.counts(s + 1), wl.max_norm)
