@@ -27,6 +27,7 @@ Workloads (all seeded with 39):
                   scale per block of 16): 10 tensors (4,096 x 6 and 1, 17, 1,000, 33,333), bf16
                   params, k=3, grads N(0, 1e-2), a NaN code in micro-batch 2 of step 3; 4 steps.
   llama_1b_fp8    the llama_1b tensor list and counts with 8-bit block-scaled gradients.
+  stream_64m_fp8  stream_64m's list with 8-bit gradients and k=8 (counter captures).
 Every workload uses AdamW lr 1e-3, betas (0.9, 0.95), eps 1e-8, weight decay 0.1 and
 master weights N(0, 0.02).
 """
@@ -127,6 +128,9 @@ def make(name: str) -> Workload:
     if name == "llama_1b_fp8":
         return Workload(name, llama_numel(2048, 16, 8192, 128256, 512), "bf16", "e4m3b16", steps=5, k=8,
                         grad_std=1e-3)
+    if name == "stream_64m_fp8":
+        # the same small case with 8-bit gradients, k = 8 (lists of 80 MB each)
+        return Workload(name, [1 << 22] * 16, "bf16", "e4m3b16", steps=2, k=8, grad_std=1e-3)
     if name == "stream_64m":
         # a small case of the 1.24B workload's kernels for counter captures: every list
         # is larger than the 129 MB L2 while the whole case holds ~1.5 GB of HBM
