@@ -781,7 +781,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
 template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
 __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
                                             : GDT == kF32 ? 2
-                                            : KM <= kFewLists ? (GDT == kE4M3 && STORE ? TL_MINB_FEW - 1 : TL_MINB_FEW)
+                                            : KM <= kFewLists ? (GDT == kE4M3 ? TL_MINB_FEW - 1 : TL_MINB_FEW)
                                             : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
              const __grid_constant__ GradTableMany inl,
