@@ -106,11 +106,19 @@ def hbm_peak():
 
 
 def kernel_source_digest() -> str:
+    """Digest of the kernel sources' code: comments, indentation and blank lines do not
+    count, so recorded counters stay valid across edits that cannot change a kernel."""
     import hashlib
     h = hashlib.sha256()
     for f in ("tl_kernels.cu", "tl_internal.cuh"):
-        with open(os.path.join(ROOT, "loss_scaled_adamw_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "loss_scaled_adamw_gb300", "csrc", f)) as fh:
+            for line in fh:
+                cut = line.find("//")
+                if cut >= 0 and '"' not in line[:cut]:
+                    line = line[:cut]
+                line = line.strip()
+                if line:
+                    h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

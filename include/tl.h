@@ -176,7 +176,8 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
  * scaling": S a power of two makes unscaling exact.
  * u = (fma(w_k, g_k, acc), or w_k * g_k if no micro-batch was accumulated
  * before) * (1/S), stored into acc; the device overflow flag is raised if any
- * u is not finite; one fp64 partial sum of fl32(u*u) is written per chunk.
+ * u is not finite; fp64 partial sums of fl32(u*u) are written (one per warp
+ * of every chunk of the context's chunk table).
  * grads = NULL: all micro-batches were accumulated already (n_k ignored),
  * u = acc * (1/S).  The n_i of the update must total N by this call.
  * Errors: TL_EINVAL (counts do not add up to N), TL_ESTATE (out of order). */

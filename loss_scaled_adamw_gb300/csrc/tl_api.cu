@@ -2,7 +2,7 @@
 //
 // Holds the opaque context: argument validation (all of it before any work is
 // enqueued), the chunk table of the multi-tensor-apply launcher (built once per
-// tensor list and kept on the device), the per-chunk norm partials, the device
+// tensor list and kept on the device), the per-warp norm partials, the device
 // scalars, a cache of device-resident gradient pointer tables for lists too
 // long to pass by value, and the order of the calls of one logical update.
 #include "tl_internal.cuh"

@@ -468,10 +468,9 @@ k_accumulate(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegi
 // a3: last micro-batch + unscale + overflow check + squared-norm partial.
 // [MEG] section 8 (cast, divide by the loss scale, place in the fp32 buffer),
 // section 6 (overflow flag), section 9 (sum of squares); [MP] section 2 "Loss
-// scaling" (S a power of two: exact).  Squares are fp32 products summed in
-// fp32 over 8 elements, then in fp64 per thread; a group whose fp32 sum
-// overflowed is re-summed in fp64, so the squared norm is infinite exactly
-// when some fp32 square is.  One fp64 partial per chunk, no atomics.
+// scaling" (S a power of two: exact).  The fp32 squares are summed per thread
+// (SumSq below), then per warp in a fixed butterfly; each warp writes one fp64
+// partial per chunk, so there are no atomics and no block barrier.
 // ---------------------------------------------------------------------------
 template <int MODE>
 __device__ __forceinline__ float unscale1(float a, float gj, float w, float inv_s) {

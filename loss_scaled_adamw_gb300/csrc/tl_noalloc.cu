@@ -54,8 +54,9 @@ __device__ __forceinline__ int tensor_of_chunk(const NoAllocList& L, int64_t c) 
 }
 
 // u = acc * (1/S) in place; one partial sum of fp32 squares per chunk (fp32 over
-// 8 elements, fp64 per thread, fixed-order block reduction), the same
-// arithmetic as the unscale kernel of the allocating path.
+// 8 elements, fp64 per thread, fixed-order block reduction).  A simpler
+// summation than the allocating path's float-float one (this entry point has no
+// scratch for per-warp partials); its norm meets the same 1e-6 relative bound.
 __global__ void __launch_bounds__(kThreads)
 k_noalloc_unscale(const __grid_constant__ NoAllocList L, float inv_s, int64_t nchunks) {
     __shared__ double red[kThreads / 32];
