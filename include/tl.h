@@ -30,8 +30,11 @@
  * uses the same ntensors and numel[].  Distinct tensors must not overlap,
  * in any list (a tensor passed twice would be counted twice in the global
  * norm; the tied input/output table appears once).  A pointer must be
- * aligned to its element size; 16-byte alignment takes the vector path,
- * anything else a scalar path.
+ * aligned to its element size (8-bit gradient tensors: to 16 bytes).  A
+ * segment whose streams are all 16-byte aligned, or all share their element
+ * offset modulo 8 (tensors packed back to back in flat buffers), takes the
+ * vector path after at most 7 scalar elements; streams of unequal offsets take
+ * a scalar path (correct, slower).
  *
  * Errors.  Every function returns a status code; nothing is thrown across
  * this boundary.  A call that returns an error has launched no kernel and
