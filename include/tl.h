@@ -37,9 +37,13 @@
  * a scalar path (correct, slower).
  *
  * Errors.  Every function returns a status code; nothing is thrown across
- * this boundary.  A call that returns an error has launched no kernel and
- * touched no caller memory (at most it has refreshed the context's own cache
- * of gradient pointer tables).
+ * this boundary.  A call that returns TL_EINVAL or TL_ESTATE has launched no
+ * kernel and touched no caller memory (at most it has refreshed the context's
+ * own cache of gradient pointer tables).  TL_ECUDA reports a failed CUDA call;
+ * if a kernel launch of an update failed, part of that update may have run (the
+ * overflow flag or the accumulation buffer half-written), so the context
+ * abandons it and refuses every update call with TL_ESTATE until tl_set_state
+ * has rewritten its scalars (from a tl_get_state snapshot, say).
  * Non-finite gradients are NOT an error: they set the device overflow flag
  * and the update is skipped on the device.
  *

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -94,6 +95,14 @@ struct tl_ctx {
     int64_t n_sum = 0;
     int64_t N_update = 0;
     bool accumulated = false;
+    // a failed launch interrupted an update: its kernels may have run in part (the
+    // overflow flag or acc half-written), so no update runs until tl_set_state
+    bool interrupted = false;
+    // host-side fault injection for tests (environment TL_TEST_FAIL_LAUNCH=n at
+    // tl_create): the context's n-th kernel launch reports a failure instead of
+    // launching
+    int64_t fail_at = 0;
+    int64_t attempts = 0;
     // a re-materialising update: u was never stored; the step recomputes it from
     // these lists (list-major, ntensors pointers each) and counts
     bool remat = false;
@@ -114,6 +123,18 @@ int fail(tl_ctx* ctx, int code, const std::string& msg) {
 int cuda_fail(tl_ctx* ctx, cudaError_t e, const char* what) {
     std::string msg = std::string(what) + ": " + cudaGetErrorString(e);
     return fail(ctx, TL_ECUDA, msg);
+}
+
+// A launch of an update's kernels failed: the update is abandoned.
+int launch_fail(tl_ctx* ctx, cudaError_t e, const char* what) {
+    ctx->interrupted = true;
+    ctx->phase = kIdle;  // tl_set_state may run
+    return cuda_fail(ctx, e, what);
+}
+
+int refuse_if_interrupted(tl_ctx* ctx) {
+    if (!ctx->interrupted) return TL_OK;
+    return fail(ctx, TL_ESTATE, "a failed launch interrupted an update; restore the scalars with tl_set_state");
 }
 
 bool overlaps_any(const std::vector<Interval>& sorted, uintptr_t lo, uintptr_t hi) {
@@ -250,17 +271,25 @@ int grid_for(tl_ctx* ctx, int per_sm, int64_t nchunks) {
     return int(g);
 }
 
+// Every kernel launch of an update passes here first (the test fault injection).
+cudaError_t gate(tl_ctx* ctx) {
+    ctx->attempts += 1;
+    return ctx->fail_at > 0 && ctx->attempts == ctx->fail_at ? cudaErrorLaunchFailure : cudaSuccess;
+}
+
 // Launch one streaming operation over the chunk table: the whole-CTA part and
 // the small-tensor groups are separate launches (launch(small, c0, c1)).
 template <typename Launch>
 cudaError_t over_parts(tl_ctx* ctx, Launch launch) {
     if (ctx->nbig > 0) {
-        cudaError_t e = launch(false, int64_t(0), ctx->nbig);
+        cudaError_t e = gate(ctx);
+        if (e == cudaSuccess) e = launch(false, int64_t(0), ctx->nbig);
         if (e != cudaSuccess) return e;
         ctx->launches += 1;
     }
     if (ctx->nchunks > ctx->nbig) {
-        cudaError_t e = launch(true, ctx->nbig, ctx->nchunks);
+        cudaError_t e = gate(ctx);
+        if (e == cudaSuccess) e = launch(true, ctx->nbig, ctx->nchunks);
         if (e != cudaSuccess) return e;
         ctx->launches += 1;
     }
@@ -380,6 +409,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
 
     cudaError_t e = cudaGetDevice(&ctx->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
+    if (const char* f = std::getenv("TL_TEST_FAIL_LAUNCH")) ctx->fail_at = std::atoll(f);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
     // Segments and chunks.  A large tensor becomes one chunk
@@ -513,6 +543,7 @@ int tl_destroy(tl_ctx* ctx) {
 
 int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N, int first, tl_stream stream) {
     if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     if (grads == nullptr && ctx->ntensors > 0) return fail(ctx, TL_EINVAL, "grads must not be NULL");
     if (first != 0 && first != 1) return fail(ctx, TL_EINVAL, "first must be 0 or 1");
     int rc = check_counts(ctx, n_i, N);
@@ -538,7 +569,7 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
             return launch_accumulate(gdt, first != 0, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl,
                                      dtab, w, ctx->grid_acc[gdt][first][small ? 1 : 0], s);
         });
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "accumulate launch");
+        if (e != cudaSuccess) return launch_fail(ctx, e, "accumulate launch");
         mark_used(used, s);
     }
     if (first) {
@@ -553,6 +584,7 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
 
 int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t N, tl_stream stream) {
     if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     int mode;
     int rc;
     if (grads == nullptr) {
@@ -586,7 +618,7 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
             return launch_unscale(gdt, mode, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, dtab, w,
                                   ctx->d_state, ctx->d_partials, ctx->grid_uns[gdt][mode][small ? 1 : 0], s);
         });
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "unscale launch");
+        if (e != cudaSuccess) return launch_fail(ctx, e, "unscale launch");
         mark_used(used, s);
     }
     if (grads != nullptr) {
@@ -600,6 +632,7 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
 int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64_t* n, int64_t N, int last,
                        tl_stream stream) {
     if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     if (k < 1 || n == nullptr) return fail(ctx, TL_EINVAL, "need k >= 1 micro-batches and their counts");
     if (grads == nullptr && ctx->ntensors > 0) return fail(ctx, TL_EINVAL, "grads must not be NULL");
     if (last != 0 && last != 1) return fail(ctx, TL_EINVAL, "last must be 0 or 1");
@@ -644,7 +677,7 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
                 return launch_accum_many(gdt, f, l, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, a,
                                          ctx->d_state, ctx->d_partials, ctx->grid_many[gdt][vr][small ? 1 : 0], s);
             });
-            if (e != cudaSuccess) return cuda_fail(ctx, e, "many-list accumulate launch");
+            if (e != cudaSuccess) return launch_fail(ctx, e, "many-list accumulate launch");
             for (int i = 0; i < kk; ++i) mark_used(slots[j + i], s);
         }
     }
@@ -658,6 +691,7 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
 int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const int64_t* n, int64_t N,
                           tl_stream stream) {
     if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     if (k < 1 || k > kRematLists || n == nullptr)
         return fail(ctx, TL_EINVAL, "need 1 <= k <= " + std::to_string(kRematLists) + " micro-batches and their counts");
     if (grads == nullptr && ctx->ntensors > 0) return fail(ctx, TL_EINVAL, "grads must not be NULL");
@@ -687,7 +721,7 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
             return launch_check_many(gdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, a, ctx->d_state,
                                      ctx->d_partials, ctx->grid_check[gdt][few][small ? 1 : 0], s);
         });
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "many-list check launch");
+        if (e != cudaSuccess) return launch_fail(ctx, e, "many-list check launch");
         for (int i = 0; i < k; ++i) mark_used(slots[size_t(i)], s);
     }
     ctx->remat = true;
@@ -703,13 +737,16 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
 
 int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream) {
     if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     if (ctx->phase != kUnscaled) return fail(ctx, TL_ESTATE, "tl_grad_norm must follow tl_unscale_check");
     if (std::isnan(max_norm)) return fail(ctx, TL_EINVAL, "max_norm is NaN");
     int rc;
     if ((rc = check_device(ctx)) != TL_OK) return rc;
-    cudaError_t e = launch_norm(ctx->d_partials, ctx->nchunks * kGroup, ctx->d_norm_slots, ctx->d_state, max_norm,
-                                static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "norm launch");
+    cudaError_t e = gate(ctx);
+    if (e == cudaSuccess)
+        e = launch_norm(ctx->d_partials, ctx->nchunks * kGroup, ctx->d_norm_slots, ctx->d_state, max_norm,
+                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return launch_fail(ctx, e, "norm launch");
     ctx->launches += 1;
     ctx->phase = kNormed;
     return TL_OK;
@@ -717,6 +754,7 @@ int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream) {
 
 int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
     if (ctx == nullptr || hp == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     if (ctx->phase != kNormed) return fail(ctx, TL_ESTATE, "tl_clip_adamw_step must follow tl_grad_norm");
     if (!(hp->lr >= 0.0f) || !std::isfinite(hp->lr) || !(hp->beta1 >= 0.5f && hp->beta1 < 1.0f) ||
         !(hp->beta2 >= 0.5f && hp->beta2 < 1.0f) || !(hp->eps > 0.0f) || !std::isfinite(hp->eps) ||
@@ -731,7 +769,8 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
     if (ctx->nchunks == 0) {
         // no elements: still one launch, whose first CTA computes the beta powers
         // the scaler kernel commits
-        e = launch_adamw(pdt, false, ctx->d_chunks, ctx->d_cbegin, 0, 0, ctx->d_state, h, 1, s);
+        e = gate(ctx);
+        if (e == cudaSuccess) e = launch_adamw(pdt, false, ctx->d_chunks, ctx->d_cbegin, 0, 0, ctx->d_state, h, 1, s);
         if (e == cudaSuccess) ctx->launches += 1;
     } else if (ctx->remat) {
         // u recomputed from the lists the update was checked on (the same device
@@ -757,20 +796,22 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
                                 ctx->grid_adam[pdt][small ? 1 : 0], s);
         });
     }
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "adamw launch");
+    if (e != cudaSuccess) return launch_fail(ctx, e, "adamw launch");
     ctx->phase = kStepped;
     return TL_OK;
 }
 
 int tl_scaler_update(tl_ctx* ctx, tl_stream stream) {
     if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     if (ctx->phase != kStepped) return fail(ctx, TL_ESTATE, "tl_scaler_update must follow tl_clip_adamw_step");
     int rc;
     if ((rc = check_device(ctx)) != TL_OK) return rc;
     ScalerParams sp{ctx->cfg.scaler_enabled, ctx->cfg.growth, ctx->cfg.backoff, ctx->cfg.interval,
                     ctx->cfg.min_scale, ctx->cfg.max_scale};
-    cudaError_t e = launch_scaler(ctx->d_state, sp, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "scaler launch");
+    cudaError_t e = gate(ctx);
+    if (e == cudaSuccess) e = launch_scaler(ctx->d_state, sp, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return launch_fail(ctx, e, "scaler launch");
     ctx->launches += 1;
     ctx->phase = kIdle;
     ctx->n_sum = 0;
@@ -849,6 +890,11 @@ int tl_set_state(tl_ctx* ctx, const tl_state* in, tl_stream stream) {
     cudaError_t e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(DevState), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "writing the device scalars");
+    ctx->interrupted = false;
+    ctx->remat = false;
+    ctx->n_sum = 0;
+    ctx->N_update = 0;
+    ctx->accumulated = false;
     return TL_OK;
 }
 

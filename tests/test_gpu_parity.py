@@ -490,3 +490,36 @@ def test_llama_1b_full_size_sampled():
     gp = L["param"].flat()[idx_t].cpu().view(torch.int16).numpy().view(np.uint16)
     assert_ulps16(gp, p, 1, "llama_1b param")
     assert st.t == 1
+
+
+def test_failed_launch_abandons_the_update(monkeypatch):
+    """Host-side fault injection (no kernel is harmed): the context's 6th launch reports a
+    failure.  The update in flight is abandoned, every update call is refused until
+    tl_set_state restores the scalars, and the redone update matches the oracle."""
+    wl = custom([5000, 300, 17000], k=2, steps=1, counts=[3, 4])   # 3 whole-CTA chunks + 1 group
+    master0 = W.master_init(wl)
+    monkeypatch.setenv("TL_TEST_FAIL_LAUNCH", "6")
+    gpu = GpuOptimizer(wl, master0)
+    monkeypatch.delenv("TL_TEST_FAIL_LAUNCH")
+    orc = oracle_for(wl, master0)
+    grads = [W.grad_input(wl, 1, i) for i in range(2)]
+    pl = [gpu.grad_list(i, g) for i, g in enumerate(grads)]
+    hp = tl.tl_adamw_hp(**W.HP)
+    snap = tl.tl_get_state(gpu.ctx)
+    # launches: accumulate 1-2, unscale 3-4, norm 5, the first AdamW part 6 (fails, not launched)
+    tl.tl_accumulate(gpu.ctx, pl[0], 3, 7, 1)
+    tl.tl_unscale_check(gpu.ctx, pl[1], 4, 7)
+    tl.tl_grad_norm(gpu.ctx, 1.0)
+    with pytest.raises(tl.TLError) as ei:
+        tl.tl_clip_adamw_step(gpu.ctx, hp)
+    assert ei.value.status == tl.TL_ECUDA
+    for call in (lambda: tl.tl_scaler_update(gpu.ctx), lambda: tl.tl_accumulate(gpu.ctx, pl[0], 3, 7, 1),
+                 lambda: tl.tl_unscale_check_many(gpu.ctx, pl, [3, 4], 7)):
+        with pytest.raises(tl.TLError) as ei:
+            call()
+        assert ei.value.status == tl.TL_ESTATE
+    tl.tl_set_state(gpu.ctx, snap)
+    tl.logical_update(gpu.ctx, pl, [3, 4], 1.0, hp)
+    res = orc.step([grad_bits(g) for g in grads], [3, 4], 1.0, **W.HP)
+    compare_scalars(gpu.status(), orc, res, "redone update")
+    compare_state(gpu.pull(), orc, wl, "redone update")
