@@ -47,6 +47,12 @@
  * Non-finite gradients are NOT an error: they set the device overflow flag
  * and the update is skipped on the device.
  *
+ * Concurrency.  A context is not thread-safe: calls on one context must not
+ * overlap in time (distinct contexts are independent).  The calls of one
+ * update run in the order of the streams they are given; with more than one
+ * stream the caller orders them (events), since each call reads what the
+ * previous one wrote on the device.
+ *
  * Pages cited (by title):
  *   [MP]  "Mixed precision, loss scaling, gradient accumulation, and
  *         activation checkpointing" (tinyllm module L11.1)
