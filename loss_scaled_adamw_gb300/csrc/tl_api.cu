@@ -76,7 +76,6 @@ struct tl_ctx {
     std::vector<int64_t> numel;
     std::vector<Interval> state_iv;  // sorted intervals of every state tensor
     Chunk* d_chunks = nullptr;     // segments
-    int32_t* d_cbegin = nullptr;   // chunk -> first segment (nchunks + 1 entries)
     double* d_partials = nullptr;
     double* d_norm_slots = nullptr;  // one per CTA of the second-stage reduce
     DevState* d_state = nullptr;
@@ -332,7 +331,6 @@ void fill_many_args(const tl_ctx* ctx, const void* const* grads, const int64_t* 
 void free_ctx(tl_ctx* ctx) {
     if (ctx == nullptr) return;
     cudaFree(ctx->d_chunks);
-    cudaFree(ctx->d_cbegin);
     cudaFree(ctx->d_partials);
     cudaFree(ctx->d_norm_slots);
     cudaFree(ctx->d_state);
@@ -457,20 +455,25 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     int64_t nbig = 0;
     for (const ChunkBuild& cb : built)
         if (!(cb.segs.size() > 1 || cb.segs[0].len <= kSmall)) ++nbig;
+    // whole-CTA chunk c is segment c; every group holds kGroup segments, a short
+    // group padded with empty segments (its first tensor, length 0) so that a warp
+    // finds its tensor without an index table
     std::vector<Chunk> chunks;
-    std::vector<int32_t> cbegin;
-    cbegin.reserve(built.size() + 1);
-    for (const ChunkBuild& cb : built) {
-        cbegin.push_back(int32_t(chunks.size()));
+    chunks.reserve(size_t(nbig) + (built.size() - size_t(nbig)) * kGroup);
+    for (size_t b = 0; b < built.size(); ++b) {
+        const ChunkBuild& cb = built[b];
         chunks.insert(chunks.end(), cb.segs.begin(), cb.segs.end());
+        if (int64_t(b) >= nbig) {
+            Chunk pad = cb.segs[0];
+            pad.len = 0;
+            for (size_t i = cb.segs.size(); i < size_t(kGroup); ++i) chunks.push_back(pad);
+        }
     }
-    cbegin.push_back(int32_t(chunks.size()));
     nchunks = int64_t(built.size());
     ctx->nchunks = nchunks;
     ctx->nbig = nbig;
     const size_t nc_alloc = size_t(std::max<int64_t>(nchunks, 1));
     if (cudaMalloc(&ctx->d_chunks, sizeof(Chunk) * std::max<size_t>(chunks.size(), 1)) != cudaSuccess ||
-        cudaMalloc(&ctx->d_cbegin, sizeof(int32_t) * cbegin.size()) != cudaSuccess ||
         cudaMalloc(&ctx->d_partials, sizeof(double) * nc_alloc * kGroup) != cudaSuccess ||
         cudaMalloc(&ctx->d_norm_slots, sizeof(double) * kNormBlocks) != cudaSuccess ||
         cudaMalloc(&ctx->d_state, sizeof(DevState)) != cudaSuccess) {
@@ -507,8 +510,6 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && nchunks > 0)
         e = cudaMemcpyAsync(ctx->d_chunks, chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(ctx->d_cbegin, cbegin.data(), sizeof(int32_t) * cbegin.size(), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
@@ -566,7 +567,7 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
     if (ctx->nchunks > 0) {
         const int gdt = ctx->cfg.grad_dtype;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_accumulate(gdt, first != 0, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl,
+            return launch_accumulate(gdt, first != 0, small, ctx->d_chunks, c0, c1, inl,
                                      dtab, w, ctx->grid_acc[gdt][first][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "accumulate launch");
@@ -615,7 +616,7 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
     if (ctx->nchunks > 0) {
         const int gdt = ctx->cfg.grad_dtype;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_unscale(gdt, mode, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, dtab, w,
+            return launch_unscale(gdt, mode, small, ctx->d_chunks, c0, c1, inl, dtab, w,
                                   ctx->d_state, ctx->d_partials, ctx->grid_uns[gdt][mode][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "unscale launch");
@@ -674,7 +675,7 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
             const int vr = (f ? 1 : 0) | (l ? 2 : 0) | (kk <= kFewLists ? 4 : 0);
             const int gdt = ctx->cfg.grad_dtype;
             cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, a,
+                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, c0, c1, inl, a,
                                          ctx->d_state, ctx->d_partials, ctx->grid_many[gdt][vr][small ? 1 : 0], s);
             });
             if (e != cudaSuccess) return launch_fail(ctx, e, "many-list accumulate launch");
@@ -718,7 +719,7 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
         const int gdt = ctx->cfg.grad_dtype;
         const int few = k <= kFewLists ? 1 : 0;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_check_many(gdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, inl, a, ctx->d_state,
+            return launch_check_many(gdt, small, ctx->d_chunks, c0, c1, inl, a, ctx->d_state,
                                      ctx->d_partials, ctx->grid_check[gdt][few][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "many-list check launch");
@@ -770,7 +771,7 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         // no elements: still one launch, whose first CTA computes the beta powers
         // the scaler kernel commits
         e = gate(ctx);
-        if (e == cudaSuccess) e = launch_adamw(pdt, false, ctx->d_chunks, ctx->d_cbegin, 0, 0, ctx->d_state, h, 1, s);
+        if (e == cudaSuccess) e = launch_adamw(pdt, false, ctx->d_chunks, 0, 0, ctx->d_state, h, 1, s);
         if (e == cudaSuccess) ctx->launches += 1;
     } else if (ctx->remat) {
         // u recomputed from the lists the update was checked on (the same device
@@ -785,14 +786,14 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         fill_many_args(ctx, ctx->remat_grads.data(), ctx->remat_n, ctx->N_update, 0, k, by_value, tabs, a, inl);
         const int gdt = ctx->cfg.grad_dtype;
         e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_adamw_remat(pdt, gdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_state, h, inl, a,
+            return launch_adamw_remat(pdt, gdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h, inl, a,
                                       ctx->grid_remat[pdt][gdt][k <= kFewLists ? 1 : 0][small ? 1 : 0], s);
         });
         if (e == cudaSuccess)
             for (int i = 0; i < k; ++i) mark_used(slots[size_t(i)], s);
     } else {
         e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_adamw(pdt, small, ctx->d_chunks, ctx->d_cbegin, c0, c1, ctx->d_state, h,
+            return launch_adamw(pdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h,
                                 ctx->grid_adam[pdt][small ? 1 : 0], s);
         });
     }

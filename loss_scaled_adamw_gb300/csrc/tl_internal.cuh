@@ -41,8 +41,8 @@ constexpr int kGradTypes = 4;
 // which change from call to call, are indexed by tensor and offset by start.
 // gscale is the byte offset from a tensor's gradient pointer to its block
 // scales (8-bit gradients: the codes rounded up to 16 bytes).
-// Chunk c covers segments [cbegin[c], cbegin[c + 1]); in the whole-CTA part of
-// the table chunk c is segment c.
+// In the whole-CTA part of the table chunk c is segment c; the groups that follow
+// hold kGroup segments each (short groups padded with empty segments).
 struct Chunk {
     float* acc;
     float* master;
@@ -118,26 +118,26 @@ enum UnscaleMode : int {
 // small = false for whole-CTA chunks (one segment of a large tensor each),
 // small = true for groups of small tensors (one warp per tensor).  `grid` is
 // the persistent grid size; a gtab of nullptr means the pointers are in `inl`.
-cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, int64_t c0,
                               int64_t c1, const GradTable& inl, const void* const* gtab, float w,
                               int grid, cudaStream_t s);
-cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
                            int64_t c1, const GradTable& inl, const void* const* gtab, float w,
                            DevState* st, double* partials, int grid, cudaStream_t s);
-cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
+cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
                               int64_t c0, int64_t c1, const GradTableMany& inl,
                               const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s);
 // The many-list pass without the store of u (all lists of the update at once),
 // and the AdamW pass that recomputes u from the same lists.
-cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
                               cudaStream_t s);
-cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, int64_t c0,
                                int64_t c1, DevState* st, AdamHP hp, const GradTableMany& inl, const ManyArgs& a,
                                int grid, cudaStream_t s);
 cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevState* st, float max_norm,
                         cudaStream_t s);
-cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
                          DevState* st, AdamHP hp, int grid, cudaStream_t s);
 cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);
 cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s);

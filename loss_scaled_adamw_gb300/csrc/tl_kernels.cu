@@ -30,12 +30,19 @@ namespace tl {
 namespace {
 
 // Minimum resident CTAs per SM requested from the compiler (register budget) for
-// the many-list kernels (TL_MINB_FEW: launches of one or two lists, whose chunks
+// the accumulation kernel (the first micro-batch, which reads no partial sum,
+// needs fewer registers), the many-list kernels (TL_MINB_FEW: launches of one or two lists, whose chunks
 // are worked faster when more of them are in flight), the AdamW kernel and its
 // re-materialising form; *_UNROLL: 8-element vectors per thread per trip of the
 // AdamW loops.  The defaults are the fastest measured (one vector per thread at
 // 2 CTAs/SM equals two at 1 CTA/SM on the 1.24B list, 2-4 % faster on the
 // ragged 100k list, whose segments are mostly partial).
+#ifndef TL_MINB_ACC
+#define TL_MINB_ACC 4
+#endif
+#ifndef TL_MINB_ACC_FIRST
+#define TL_MINB_ACC_FIRST 6
+#endif
 #ifndef TL_MINB_MANY
 #define TL_MINB_MANY 3
 #endif
@@ -419,6 +426,14 @@ __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const
     for (; j < len; j += NT) one(j);
 }
 
+// Warp w's tensor of group chunk c.  The groups follow the whole-CTA chunks in the
+// table, kGroup segments each (a short group is padded with empty segments), and
+// the launch over the groups starts at c0 = the first group, whose first segment
+// is segment c0 (the whole-CTA chunks before it hold one segment each).
+__device__ __forceinline__ const Chunk& group_segment(const Chunk* __restrict__ chunks, int64_t c0, int64_t c) {
+    return chunks[c0 + (c - c0) * kGroup + (threadIdx.x >> 5)];
+}
+
 // The whole-CTA chunks of a persistent CTA (c0 + blockIdx.x, then every gridDim.x),
 // each descriptor handed to work(c, ch).  With PF the next descriptor is loaded
 // into registers before the current chunk is worked, so that its load overlaps the
@@ -446,8 +461,8 @@ __device__ __forceinline__ void for_chunks(const Chunk* __restrict__ chunks, int
 }
 
 template <int NT, int GDT, bool FIRST>
-__global__ void __launch_bounds__(kThreads)
-k_accumulate(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+__global__ void __launch_bounds__(kThreads, FIRST ? TL_MINB_ACC_FIRST : TL_MINB_ACC)
+k_accumulate(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
              const __grid_constant__ GradTable inl,
              const void* const* __restrict__ gtab, float w) {
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
@@ -458,9 +473,7 @@ k_accumulate(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegi
         return;
     }
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
-        if (wi < cbegin[c + 1] - b0) accumulate_segment<32, GDT, FIRST>(chunks[b0 + wi], threadIdx.x & 31, gp, w);
+        accumulate_segment<32, GDT, FIRST>(group_segment(chunks, c0, c), threadIdx.x & 31, gp, w);
     }
 }
 
@@ -657,7 +670,7 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
 
 template <int NT, int GDT, int MODE>
 __global__ void __launch_bounds__(kThreads, NT == kThreads && GDT != kF32 ? 3 : 2)
-k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
           const __grid_constant__ GradTable inl,
           const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials) {
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
@@ -674,10 +687,7 @@ k_unscale(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, 
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         SumSq sq;
         bool bad = false;
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
-        if (wi < cbegin[c + 1] - b0)
-            unscale_segment<32, GDT, MODE>(chunks[b0 + wi], threadIdx.x & 31, gp, w, inv_s, sq, bad);
+        unscale_segment<32, GDT, MODE>(group_segment(chunks, c0, c), threadIdx.x & 31, gp, w, inv_s, sq, bad);
         finish_warp(sq, bad, c, st, partials);
     }
 }
@@ -815,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
                                             : GDT == kF32 ? 2
                                             : KM <= kFewLists ? (GDT == kE4M3 ? TL_MINB_FEW - 1 : TL_MINB_FEW)
                                             : TL_MINB_MANY)
-k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
              const __grid_constant__ GradTableMany inl,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
@@ -831,10 +841,8 @@ k_accum_many(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegi
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
         SumSq sq;
         bool bad = false;
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
-        if (wi < cbegin[c + 1] - b0)
-            many_segment<32, GDT, FIRST, LAST, KM, STORE>(chunks[b0 + wi], threadIdx.x & 31, inl, a, inv_s, sq, bad);
+        many_segment<32, GDT, FIRST, LAST, KM, STORE>(group_segment(chunks, c0, c), threadIdx.x & 31, inl, a, inv_s,
+                                                      sq, bad);
         if (LAST) finish_warp(sq, bad, c, st, partials);
     }
 }
@@ -1157,7 +1165,7 @@ __device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const Ada
 
 template <int NT, int PDT>
 __global__ void __launch_bounds__(kThreads, TL_MINB_ADAM)
-k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
         DevState* __restrict__ st, AdamHP hp) {
     AdamConsts k;
     if (adam_consts(st, hp, k)) return;
@@ -1168,12 +1176,8 @@ k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, in
         return;
     }
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
-        if (wi < cbegin[c + 1] - b0) {
-            const Chunk& ch = chunks[b0 + wi];
-            adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromAcc(ch));
-        }
+        const Chunk& ch = group_segment(chunks, c0, c);
+        adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromAcc(ch));
     }
 }
 
@@ -1181,7 +1185,7 @@ k_adamw(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, in
 // resident gradient lists (at most KM <= kRematLists of them) instead of read.
 template <int NT, int PDT, int GDT, int KM>
 __global__ void __launch_bounds__(kThreads, KM <= kFewLists && GDT != kF32 ? TL_MINB_REMAT_FEW : TL_MINB_REMAT)
-k_adamw_remat(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbegin, int64_t c0, int64_t c1,
+k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
               DevState* __restrict__ st, AdamHP hp, const __grid_constant__ GradTableMany inl,
               const __grid_constant__ ManyArgs a) {
     AdamConsts k;
@@ -1194,12 +1198,8 @@ k_adamw_remat(const Chunk* __restrict__ chunks, const int32_t* __restrict__ cbeg
         return;
     }
     for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const int b0 = cbegin[c];
-        const int wi = threadIdx.x >> 5;
-        if (wi < cbegin[c + 1] - b0) {
-            const Chunk& ch = chunks[b0 + wi];
-            adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
-        }
+        const Chunk& ch = group_segment(chunks, c0, c);
+        adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
     }
 }
 
@@ -1249,12 +1249,12 @@ __global__ void k_seed(const DevState* __restrict__ st, float w, float* __restri
 // (one warp per tensor) over whole-CTA segments; each has its own register
 // budget.
 // ---------------------------------------------------------------------------
-using AccFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const GradTable, const void* const*, float);
-using UnsFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const GradTable, const void* const*, float,
+using AccFn = void (*)(const Chunk*, int64_t, int64_t, const GradTable, const void* const*, float);
+using UnsFn = void (*)(const Chunk*, int64_t, int64_t, const GradTable, const void* const*, float,
                        DevState*, double*);
-using ManyFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, const GradTableMany, const ManyArgs,
+using ManyFn = void (*)(const Chunk*, int64_t, int64_t, const GradTableMany, const ManyArgs,
                         DevState*, double*);
-using AdamFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, DevState*, AdamHP);
+using AdamFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP);
 
 template <int NT>
 AccFn acc_fn_nt(int gdt, bool first) {
@@ -1334,7 +1334,7 @@ ManyFn check_fn_nt(int gdt, bool few) {
 }
 ManyFn check_fn(int gdt, bool small, bool few) { return small ? check_fn_nt<32>(gdt, few) : check_fn_nt<kThreads>(gdt, few); }
 
-using RematFn = void (*)(const Chunk*, const int32_t*, int64_t, int64_t, DevState*, AdamHP, const GradTableMany,
+using RematFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP, const GradTableMany,
                          const ManyArgs);
 
 template <int NT, int PDT, int GDT>
@@ -1373,30 +1373,30 @@ AdamFn adam_fn(int pdt, bool small) {
 
 }  // namespace
 
-cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, int64_t c0,
                               int64_t c1, const GradTable& inl, const void* const* gtab, float w, int grid,
                               cudaStream_t s) {
     AccFn f = acc_fn(gdt, first, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, gtab, w);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, inl, gtab, w);
     return cudaGetLastError();
 }
 
-cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
                            int64_t c1, const GradTable& inl, const void* const* gtab, float w, DevState* st,
                            double* partials, int grid, cudaStream_t s) {
     UnsFn f = uns_fn(gdt, mode, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, gtab, w, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, inl, gtab, w, st, partials);
     return cudaGetLastError();
 }
 
-cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks, const int32_t* cbegin,
+cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
                               int64_t c0, int64_t c1, const GradTableMany& inl, const ManyArgs& a, DevState* st,
                               double* partials, int grid, cudaStream_t s) {
     ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, a, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, inl, a, st, partials);
     return cudaGetLastError();
 }
 
@@ -1408,29 +1408,29 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
     return cudaGetLastError();
 }
 
-cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
                               cudaStream_t s) {
     ManyFn f = check_fn(gdt, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, inl, a, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, inl, a, st, partials);
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0,
+cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, int64_t c0,
                                int64_t c1, DevState* st, AdamHP hp, const GradTableMany& inl, const ManyArgs& a,
                                int grid, cudaStream_t s) {
     RematFn f = remat_fn(pdt, gdt, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kRematLists) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, st, hp, inl, a);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, inl, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, const int32_t* cbegin, int64_t c0, int64_t c1,
+cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
                          DevState* st, AdamHP hp, int grid, cudaStream_t s) {
     AdamFn f = adam_fn(pdt, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, cbegin, c0, c1, st, hp);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp);
     return cudaGetLastError();
 }
 
