@@ -88,6 +88,10 @@ struct tl_ctx {
     int grid_adam[3][2] = {};
     int grid_many[kGradTypes][8][2] = {};
     int grid_check[kGradTypes][2][2] = {};        // [grad dtype][few lists][part]
+    // chunks per run of the kernels that write norm partials, per part: 1 where the
+    // chunks are mostly full segments, kRun where they are short (one warp
+    // reduction per run instead of per chunk)
+    int run[2] = {1, 1};
     int grid_remat[3][kGradTypes][2][2] = {};     // [param dtype][grad dtype][few lists][part]
     // the update in flight
     int phase = kIdle;
@@ -508,6 +512,8 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     ds.norm_ticket = 0;
     ds.pad = 0;
     e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
+    // partial slots not at the start of a run stay zero for good
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d_partials, 0, sizeof(double) * nc_alloc * kGroup, s);
     if (e == cudaSuccess && nchunks > 0)
         e = cudaMemcpyAsync(ctx->d_chunks, chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -516,17 +522,22 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     // Persistent grid sizes from the occupancy of each kernel variant the
     // context's dtypes can launch.
     const int gdt = cfg->grad_dtype, pdt = cfg->param_dtype;
+    int64_t big_elems = 0;
+    for (int64_t c = 0; c < nbig; ++c) big_elems += chunks[size_t(c)].len;
+    ctx->run[0] = nbig > 0 && big_elems < nbig * (kChunk / 2) ? kRun : 1;
+    ctx->run[1] = kRun;
     for (int part = 0; part < 2; ++part) {
         const bool small = part == 1;
         const int64_t n = small ? nchunks - nbig : nbig;
+        const int64_t nruns = (n + ctx->run[part] - 1) / ctx->run[part];
         for (int f = 0; f < 2; ++f) ctx->grid_acc[gdt][f][part] = grid_for(ctx, blocks_per_sm(0, gdt, f, small), n);
         for (int md = 0; md < 3; ++md)
-            ctx->grid_uns[gdt][md][part] = grid_for(ctx, blocks_per_sm(1, gdt, md, small), n);
+            ctx->grid_uns[gdt][md][part] = grid_for(ctx, blocks_per_sm(1, gdt, md, small), nruns);
         ctx->grid_adam[pdt][part] = grid_for(ctx, blocks_per_sm(2, pdt, 0, small), n);
         for (int vr = 0; vr < 8; ++vr)
-            ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr, small), n);
+            ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr, small), nruns);
         for (int few = 0; few < 2; ++few) {
-            ctx->grid_check[gdt][few][part] = grid_for(ctx, blocks_per_sm(4, gdt, few ? 4 : 0, small), n);
+            ctx->grid_check[gdt][few][part] = grid_for(ctx, blocks_per_sm(4, gdt, few ? 4 : 0, small), nruns);
             ctx->grid_remat[pdt][gdt][few][part] =
                 grid_for(ctx, blocks_per_sm(5, pdt, gdt | (few ? 4 : 0), small), n);
         }
@@ -616,7 +627,7 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
     if (ctx->nchunks > 0) {
         const int gdt = ctx->cfg.grad_dtype;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_unscale(gdt, mode, small, ctx->d_chunks, c0, c1, inl, dtab, w,
+            return launch_unscale(gdt, mode, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, dtab, w,
                                   ctx->d_state, ctx->d_partials, ctx->grid_uns[gdt][mode][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "unscale launch");
@@ -675,7 +686,7 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
             const int vr = (f ? 1 : 0) | (l ? 2 : 0) | (kk <= kFewLists ? 4 : 0);
             const int gdt = ctx->cfg.grad_dtype;
             cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, c0, c1, inl, a,
+                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a,
                                          ctx->d_state, ctx->d_partials, ctx->grid_many[gdt][vr][small ? 1 : 0], s);
             });
             if (e != cudaSuccess) return launch_fail(ctx, e, "many-list accumulate launch");
@@ -719,7 +730,7 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
         const int gdt = ctx->cfg.grad_dtype;
         const int few = k <= kFewLists ? 1 : 0;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_check_many(gdt, small, ctx->d_chunks, c0, c1, inl, a, ctx->d_state,
+            return launch_check_many(gdt, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a, ctx->d_state,
                                      ctx->d_partials, ctx->grid_check[gdt][few][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "many-list check launch");

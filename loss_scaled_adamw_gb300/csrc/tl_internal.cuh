@@ -23,6 +23,10 @@ constexpr int kChunk = 16384;
 #endif
 constexpr int kSmall = TL_SMALL;
 constexpr int kGroup = 8;            // = warps per CTA
+#ifndef TL_RUN
+#define TL_RUN 4
+#endif
+constexpr int kRun = TL_RUN;         // chunks per run where chunks are short (see launch_unscale)
 constexpr int kThreads = 256;        // streaming kernels: 8 warps per CTA
 constexpr int kNormThreads = 256;    // threads per CTA of the second-stage reduce
 constexpr int kNormBlocks = 128;     // CTAs of the second-stage reduce: fixed, so its order is device-independent
@@ -114,7 +118,9 @@ enum UnscaleMode : int {
     kAccAndGrad = 2 // u = fma(w, g, acc) / S: the last of several micro-batches
 };
 
-// Launchers (tl_kernels.cu).  Each streaming launcher covers chunks [c0, c1):
+// Launchers (tl_kernels.cu).  Each streaming launcher covers chunks [c0, c1); the
+// ones that write squared-norm partials take the chunks in runs of `run` (one
+// partial per warp per run, in the slots of the run's first chunk):
 // small = false for whole-CTA chunks (one segment of a large tensor each),
 // small = true for groups of small tensors (one warp per tensor).  `grid` is
 // the persistent grid size; a gtab of nullptr means the pointers are in `inl`.
@@ -122,14 +128,14 @@ cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chun
                               int64_t c1, const GradTable& inl, const void* const* gtab, float w,
                               int grid, cudaStream_t s);
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
-                           int64_t c1, const GradTable& inl, const void* const* gtab, float w,
+                           int64_t c1, int run, const GradTable& inl, const void* const* gtab, float w,
                            DevState* st, double* partials, int grid, cudaStream_t s);
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
-                              int64_t c0, int64_t c1, const GradTableMany& inl,
+                              int64_t c0, int64_t c1, int run, const GradTableMany& inl,
                               const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s);
 // The many-list pass without the store of u (all lists of the update at once),
 // and the AdamW pass that recomputes u from the same lists.
-cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
+cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
                               cudaStream_t s);
 cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, int64_t c0,

@@ -434,6 +434,19 @@ __device__ __forceinline__ const Chunk& group_segment(const Chunk* __restrict__ 
     return chunks[c0 + (c - c0) * kGroup + (threadIdx.x >> 5)];
 }
 
+// Chunks [c0, c1) in runs of `run` consecutive chunks of the table, CTA b taking
+// runs b, b + gridDim.x, ...: work(c) for every chunk of a run in table order, then
+// done(first chunk of the run).  Runs are fixed by the table, not by the grid, so a
+// sum kept over a run has the same order on any device.
+template <class Work, class Done>
+__device__ __forceinline__ void for_runs(int64_t c0, int64_t c1, int run, Work work, Done done) {
+    for (int64_t r0 = c0 + int64_t(blockIdx.x) * run; r0 < c1; r0 += int64_t(gridDim.x) * run) {
+        const int64_t r1 = r0 + run < c1 ? r0 + run : c1;
+        for (int64_t c = r0; c < r1; ++c) work(c);
+        done(r0);
+    }
+}
+
 // The whole-CTA chunks of a persistent CTA (c0 + blockIdx.x, then every gridDim.x),
 // each descriptor handed to work(c, ch).  With PF the next descriptor is loaded
 // into registers before the current chunk is worked, so that its load overlaps the
@@ -670,26 +683,21 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
 
 template <int NT, int GDT, int MODE>
 __global__ void __launch_bounds__(kThreads, NT == kThreads && GDT != kF32 ? 3 : 2)
-k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
+k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
           const __grid_constant__ GradTable inl,
           const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials) {
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
     const float inv_s = __fdiv_rn(1.0f, st->S);
-    if (NT == kThreads) {
-        for_chunks<false>(chunks, c0, c1, [&](int64_t c, const Chunk& ch) {
-            SumSq sq;
-            bool bad = false;
-            unscale_segment<kThreads, GDT, MODE>(ch, threadIdx.x, gp, w, inv_s, sq, bad);
-            finish_warp(sq, bad, c, st, partials);
-        });
-        return;
-    }
-    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        SumSq sq;
-        bool bad = false;
-        unscale_segment<32, GDT, MODE>(group_segment(chunks, c0, c), threadIdx.x & 31, gp, w, inv_s, sq, bad);
-        finish_warp(sq, bad, c, st, partials);
-    }
+    SumSq sq;
+    bool bad = false;
+    for_runs(c0, c1, run, [&](int64_t c) {
+        if (NT == kThreads) unscale_segment<kThreads, GDT, MODE>(chunks[c], threadIdx.x, gp, w, inv_s, sq, bad);
+        else unscale_segment<32, GDT, MODE>(group_segment(chunks, c0, c), threadIdx.x & 31, gp, w, inv_s, sq, bad);
+    }, [&](int64_t r0) {
+        finish_warp(sq, bad, r0, st, partials);
+        sq = SumSq();
+        bad = false;
+    });
 }
 
 // ---------------------------------------------------------------------------
@@ -823,28 +831,27 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
 template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
 __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
                                             : GDT == kF32 ? 2
-                                            : KM <= kFewLists ? (GDT == kE4M3 ? TL_MINB_FEW - 1 : TL_MINB_FEW)
+                                            : KM <= kFewLists ? (GDT == kE4M3 || (LAST && !FIRST) ? TL_MINB_FEW - 1 : TL_MINB_FEW)
                                             : TL_MINB_MANY)
-k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
+k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
              const __grid_constant__ GradTableMany inl,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
-    if (NT == kThreads) {
-        for_chunks<false>(chunks, c0, c1, [&](int64_t c, const Chunk& ch) {
-            SumSq sq;
-            bool bad = false;
-            many_segment<kThreads, GDT, FIRST, LAST, KM, STORE>(ch, threadIdx.x, inl, a, inv_s, sq, bad);
-            if (LAST) finish_warp(sq, bad, c, st, partials);
-        });
-        return;
-    }
-    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        SumSq sq;
-        bool bad = false;
-        many_segment<32, GDT, FIRST, LAST, KM, STORE>(group_segment(chunks, c0, c), threadIdx.x & 31, inl, a, inv_s,
-                                                      sq, bad);
-        if (LAST) finish_warp(sq, bad, c, st, partials);
-    }
+    SumSq sq;
+    bool bad = false;
+    for_runs(c0, c1, run, [&](int64_t c) {
+        if (NT == kThreads)
+            many_segment<kThreads, GDT, FIRST, LAST, KM, STORE>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
+        else
+            many_segment<32, GDT, FIRST, LAST, KM, STORE>(group_segment(chunks, c0, c), threadIdx.x & 31, inl, a,
+                                                          inv_s, sq, bad);
+    }, [&](int64_t r0) {
+        if (LAST) {
+            finish_warp(sq, bad, r0, st, partials);
+            sq = SumSq();
+            bad = false;
+        }
+    });
 }
 
 // ---------------------------------------------------------------------------
@@ -1184,7 +1191,8 @@ k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
 // The re-materialising AdamW pass: u of every element recomputed from the
 // resident gradient lists (at most KM <= kRematLists of them) instead of read.
 template <int NT, int PDT, int GDT, int KM>
-__global__ void __launch_bounds__(kThreads, KM <= kFewLists && GDT != kF32 ? TL_MINB_REMAT_FEW : TL_MINB_REMAT)
+__global__ void __launch_bounds__(kThreads, NT != kThreads && GDT == kF32 ? 1
+                                            : KM <= kFewLists && GDT != kF32 ? TL_MINB_REMAT_FEW : TL_MINB_REMAT)
 k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
               DevState* __restrict__ st, AdamHP hp, const __grid_constant__ GradTableMany inl,
               const __grid_constant__ ManyArgs a) {
@@ -1250,9 +1258,9 @@ __global__ void k_seed(const DevState* __restrict__ st, float w, float* __restri
 // budget.
 // ---------------------------------------------------------------------------
 using AccFn = void (*)(const Chunk*, int64_t, int64_t, const GradTable, const void* const*, float);
-using UnsFn = void (*)(const Chunk*, int64_t, int64_t, const GradTable, const void* const*, float,
+using UnsFn = void (*)(const Chunk*, int64_t, int64_t, int, const GradTable, const void* const*, float,
                        DevState*, double*);
-using ManyFn = void (*)(const Chunk*, int64_t, int64_t, const GradTableMany, const ManyArgs,
+using ManyFn = void (*)(const Chunk*, int64_t, int64_t, int, const GradTableMany, const ManyArgs,
                         DevState*, double*);
 using AdamFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP);
 
@@ -1383,20 +1391,20 @@ cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chun
 }
 
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
-                           int64_t c1, const GradTable& inl, const void* const* gtab, float w, DevState* st,
+                           int64_t c1, int run, const GradTable& inl, const void* const* gtab, float w, DevState* st,
                            double* partials, int grid, cudaStream_t s) {
     UnsFn f = uns_fn(gdt, mode, small);
-    if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, inl, gtab, w, st, partials);
+    if (f == nullptr || run < 1) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, gtab, w, st, partials);
     return cudaGetLastError();
 }
 
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
-                              int64_t c0, int64_t c1, const GradTableMany& inl, const ManyArgs& a, DevState* st,
-                              double* partials, int grid, cudaStream_t s) {
+                              int64_t c0, int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a,
+                              DevState* st, double* partials, int grid, cudaStream_t s) {
     ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists);
-    if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, inl, a, st, partials);
+    if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials);
     return cudaGetLastError();
 }
 
@@ -1408,12 +1416,12 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
     return cudaGetLastError();
 }
 
-cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
+cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
                               cudaStream_t s) {
     ManyFn f = check_fn(gdt, small, a.k <= kFewLists);
-    if (f == nullptr || a.k < 1 || a.k > kMaxMany) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, inl, a, st, partials);
+    if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials);
     return cudaGetLastError();
 }
 
