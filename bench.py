@@ -284,6 +284,9 @@ class GpuWorkload:
         self.plist = plist
         self.plists = {n: plist(getattr(self, n), keys[n]) for n in keys}
         self.gplists = [plist(g, 10 + i) for i, g in enumerate(self.grads)]
+        # element offset of the first gradient element of tensor 0 in grads[0]
+        first = int(self.gplists[0].array[0]) - self.grads[0].data_ptr()
+        self.plists_first_offset = first // self.grads[0].element_size()
         self.many = tl.ManyLists(self.gplists)
         dt = {"bf16": tl.TL_BF16, "f16": tl.TL_F16, "f32": tl.TL_F32, "e4m3b16": tl.TL_E4M3B16}
         cfg = tl.make_config(dt[wl.param_dtype], dt[wl.grad_dtype], wl.scaler_enabled,
@@ -441,7 +444,8 @@ def run_gpu(args, rank, world, local_rank):
         head = timed[args.path]
         graphs = {p: time_graph(args, gw, p, world) for p in names} if args.graph else None
         e2e = None if args.no_e2e else run_e2e(args, gw, world)
-    st = tl.tl_read_status(gw.ctx)
+        st = tl.tl_read_status(gw.ctx)
+        skipped = time_skipped(args, gw, args.path, world)
     kernels = head["kernels"]
     dom = max((n for n in kernels if "achieved_gbs" in kernels[n]), key=lambda n: kernels[n]["share"])
     peak, peak_kind = hbm_peak()
@@ -472,9 +476,43 @@ def run_gpu(args, rank, world, local_rank):
         **({"cuda_graph": graphs} if graphs else {}),
         "status": {"S": st.S, "t": st.t, "skipped": st.skipped, "norm": st.norm},
     }
+    out["skipped_step"] = skipped
     if e2e is not None:
         out["e2e"] = e2e
     return out
+
+
+def time_skipped(args, gw, path, world):
+    """The same path timed while every step overflows (a non-finite value planted in
+    the first element of the first micro-batch's gradients): the overflow check still
+    reads every gradient, the AdamW kernel exits on the device flag.  The element is
+    restored afterwards."""
+    import torch
+    import loss_scaled_adamw_gb300 as tl
+    g = gw.grads[0]
+    pos = int(gw.plists_first_offset)
+    saved = g[pos].clone()
+    if g.dtype == torch.uint8:
+        g[pos] = 0x7F                       # an E4M3 NaN code
+    else:
+        g[pos] = float("inf")
+    for _ in range(max(args.warmup, 1)):
+        gw.step(path)
+    torch.cuda.synchronize()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        gw.step(path)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    st = tl.tl_read_status(gw.ctx)
+    g[pos] = saved
+    torch.cuda.synchronize()
+    el = max_over_ranks(t0.elapsed_time(t1) / 1e3, gw.device)
+    return {"path": path, "ms_per_step": el / args.steps * 1e3, "value": whole_job_rate(gw.P, args.steps, world, el),
+            "unit": UNIT, "skipped": int(st.skipped)}
 
 
 def run_e2e(args, gw, world):
