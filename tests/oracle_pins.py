@@ -550,6 +550,61 @@ def pin_state_bytes_per_param(lib):
     assert sum(parts.values()) + o.acc.itemsize == 20
 
 
+def pin_nonfinite_without_scaler_still_skips(lib):
+    """[MP] "Dynamic scaling": bf16 needs no scaler, but a finite check still gates the
+    step (pitfall s17: stepping on a NaN when the scaler is off).  With the scaler
+    disabled a NaN or inf gradient skips the update: weights, moments, model copy, t and
+    S = 1 unchanged; the next clean update commits as usual."""
+    rng = np.random.default_rng(17)
+    master = rng.standard_normal(64).astype(np.float32) * 0.02
+    o = make_oracle(lib, master, pdtype="bf16", gdtype="f32")
+    g = [rng.standard_normal(64).astype(np.float32) * 1e-2 for _ in range(2)]
+    o.step(g, [2, 3], 1.0)
+    before = [x.copy() for x in (o.w, o.m, o.v, o.p)]
+    t0 = o.state.t
+    for bad in (np.nan, np.inf):
+        gb = [x.copy() for x in g]
+        gb[1][7] = bad
+        r = o.step(gb, [2, 3], 1.0)
+        assert r.skipped == 1 and o.state.t == t0 and o.state.S == 1.0 and o.state.count == 0
+        for a, b in zip(before, (o.w, o.m, o.v, o.p)):
+            assert np.array_equal(a, b)
+    r = o.step(g, [2, 3], 1.0)
+    assert r.skipped == 0 and o.state.t == t0 + 1
+
+
+def pin_resume_keeps_the_good_step_count(lib):
+    """[MP] section 4: the scaler's state_dict keeps S and the good-step count (pitfall
+    s16: losing the count on resume).  An update sequence interrupted after 3 steps and
+    resumed from (S, count, t, beta powers, w, m, v, param) ends exactly where the
+    uninterrupted one does, S growing at the same step (interval 4)."""
+    rng = np.random.default_rng(16)
+    master = rng.standard_normal(32).astype(np.float32) * 0.02
+    grads = [[fp16_scaled(rng.standard_normal(32).astype(np.float32) * 1e-3, 2.0 ** 8)] for _ in range(7)]
+    kw = dict(pdtype="f16", gdtype="f16", scaler_enabled=True, init_scale=2.0 ** 8, interval=4)
+    a = make_oracle(lib, master, **kw)
+    seq_a = []
+    for g in grads:
+        a.step(g, [5], 1.0)
+        seq_a.append(a.state.S)
+    b = make_oracle(lib, master, **kw)
+    for g in grads[:3]:
+        b.step(g, [5], 1.0)
+    c = make_oracle(lib, master, **kw)
+    for f in ("w", "m", "v", "p"):
+        setattr(c, f, getattr(b, f).copy())
+    c.state = oracle.State(b.state.S, b.state.count, b.state.t, b.state.b1p, b.state.b2p)
+    assert c.state.count == 3
+    seq_c = []
+    for g in grads[3:]:
+        c.step(g, [5], 1.0)
+        seq_c.append(c.state.S)
+    assert seq_c == seq_a[3:] and seq_a[3] == 2.0 ** 9 and seq_a[2] == 2.0 ** 8
+    for f in ("w", "m", "v", "p"):
+        assert np.array_equal(getattr(a, f), getattr(c, f)), f
+    assert (a.state.S, a.state.count, a.state.t) == (c.state.S, c.state.count, c.state.t)
+
+
 # ---- 8-bit gradients with fine-grained scaling ([T41] section 41.5) --------
 
 def _torch_e4m3(codes):

@@ -66,6 +66,10 @@ MUTANTS = [
     ("f16_bias_off", "mag = ldexpf((float)(1024 + man), exp - 25);", "mag = ldexpf((float)(1024 + man), exp - 24);"),
     ("f16_subnormal_scale", "mag = ldexpf((float)man, -24);", "mag = ldexpf((float)man, -25);"),
     ("param_not_recast", "p[j] = (pdtype == TLO_DT_F16) ? tlo_f32_to_f16(wj) : tlo_f32_to_bf16(wj);", "(void)p;"),
+    # [MP] pitfall 16: losing the good-step count; pitfall 17: stepping on a NaN without a scaler
+    ("s16_count_lost", "        st->count += 1;\n", "        st->count = 1;\n"),
+    ("s17_nan_without_scaler", "    if (!found_inf) {\n        tlo_adamw_scalars s",
+     "    if (!found_inf || !cfg->enabled) {\n        tlo_adamw_scalars s"),
     # 8-bit gradients: E4M3 layout and block scales
     ("e4m3_bias_off", "((e + 120u) << 23)", "((e + 121u) << 23)"),
     ("e4m3_mantissa_shift", "| (m << 20));", "| (m << 21));"),
