@@ -174,6 +174,18 @@ def test_skip_leaves_state_bitwise_unchanged():
     assert gpu.status().t == 2
 
 
+@pytest.mark.parametrize("resident", [False, True, "remat"], ids=["per_microbatch", "resident", "remat"])
+def test_nonfinite_without_scaler_skips(resident):
+    """bf16 without a loss scaler (the finite check still gates every update): a NaN and
+    then an inf gradient skip their updates with S = 1 kept, and the state stays within
+    the parity tolerances of the oracle throughout."""
+    wl = custom([5000, 300, 20000], k=2, steps=4, counts=[3, 4],
+                injections={(2, 0): [(123, 0x7FC0)], (3, 1): [(20100, 0x7F80)]})
+    _, _, log = run_parity(wl, resident=resident)
+    assert [e["skipped"] for e in log] == [0, 1, 1, 0]
+    assert all(e["S"] == 1.0 for e in log)
+
+
 def _small_ctx(scaler=False):
     wl = custom([100, 28], k=2, steps=1, counts=[1, 1], scaler=scaler, init_scale=8.0, interval=3,
                 pdtype="f16" if scaler else "bf16", gdtype="f16" if scaler else "bf16")
