@@ -535,3 +535,39 @@ def test_failed_launch_abandons_the_update(monkeypatch):
     res = orc.step([grad_bits(g) for g in grads], [3, 4], 1.0, **W.HP)
     compare_scalars(gpu.status(), orc, res, "redone update")
     compare_state(gpu.pull(), orc, wl, "redone update")
+
+
+def _outside_mask(dl):
+    """Positions of a DeviceList buffer that belong to no tensor (gaps, padding, tail)."""
+    inside = np.zeros(dl.buf.numel(), dtype=bool)
+    for o, n in zip(dl.offs, dl.numel):
+        inside[o:o + n] = True
+    return torch.from_numpy(~inside).to(dl.buf.device)
+
+
+@pytest.mark.parametrize("gaps", [False, True, "packed"], ids=["aligned", "gaps", "packed"])
+@pytest.mark.parametrize("resident", [False, True, "remat"], ids=["per_microbatch", "resident", "remat"])
+def test_no_write_outside_tensors(gaps, resident):
+    """Canary words: every buffer position outside the tensors (gaps between tensors,
+    alignment padding, the tail) holds a sentinel before the updates and still holds it
+    after them; the gradient buffers are not written at all."""
+    wl = custom([1, 7, 9, 127, 1025, 16385, 33, 40000, 8], k=3, steps=3, counts=[2, 3, 4])
+    master0 = W.master_init(wl)
+    gpu = GpuOptimizer(wl, master0, gaps=gaps)
+    masks = {}
+    for name, dl in gpu.lists.items():
+        masks[name] = _outside_mask(dl)
+        sentinel = 12345.678 if dl.buf.dtype == torch.float32 else -7.5
+        dl.buf[masks[name]] = sentinel
+    canary = {name: dl.buf[masks[name]].clone() for name, dl in gpu.lists.items()}
+    hp = tl.tl_adamw_hp(**W.HP)
+    for step in (1, 2, 3):
+        grads = [W.grad_input(wl, step, i) for i in range(wl.k)]
+        pl = [gpu.grad_list(i, g) for i, g in enumerate(grads)]
+        before = [gpu.grad_lists[i].buf.clone() for i in range(wl.k)]
+        tl.logical_update(gpu.ctx, pl, wl.counts(step), 1.0, hp, resident=resident)
+        torch.cuda.synchronize()
+        for i in range(wl.k):
+            assert torch.equal(gpu.grad_lists[i].buf, before[i]), f"gradient list {i} was written"
+    for name, dl in gpu.lists.items():
+        assert torch.equal(dl.buf[masks[name]], canary[name]), f"{name}: a write outside the tensors"
