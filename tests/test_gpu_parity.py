@@ -545,13 +545,14 @@ def _outside_mask(dl):
     return torch.from_numpy(~inside).to(dl.buf.device)
 
 
+@pytest.mark.parametrize("gdtype", ["bf16", "e4m3b16"])
 @pytest.mark.parametrize("gaps", [False, True, "packed"], ids=["aligned", "gaps", "packed"])
 @pytest.mark.parametrize("resident", [False, True, "remat"], ids=["per_microbatch", "resident", "remat"])
-def test_no_write_outside_tensors(gaps, resident):
+def test_no_write_outside_tensors(gaps, resident, gdtype):
     """Canary words: every buffer position outside the tensors (gaps between tensors,
     alignment padding, the tail) holds a sentinel before the updates and still holds it
     after them; the gradient buffers are not written at all."""
-    wl = custom([1, 7, 9, 127, 1025, 16385, 33, 40000, 8], k=3, steps=3, counts=[2, 3, 4])
+    wl = custom([1, 7, 9, 127, 1025, 16385, 33, 40000, 8], gdtype=gdtype, k=3, steps=3, counts=[2, 3, 4])
     master0 = W.master_init(wl)
     gpu = GpuOptimizer(wl, master0, gaps=gaps)
     masks = {}
