@@ -524,10 +524,15 @@ def run_e2e(args, gw, world):
     import torch
     import loss_scaled_adamw_gb300 as tl
     k = gw.wl.k
-    host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gw.grads]
-    for h, g in zip(host, gw.grads):
-        h.copy_(g)
-    sets = [gw.grads, [torch.empty_like(g) for g in gw.grads]]
+    try:
+        host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gw.grads]
+        for h, g in zip(host, gw.grads):
+            h.copy_(g)
+        sets = [gw.grads, [torch.empty_like(g) for g in gw.grads]]
+    except RuntimeError as ex:      # pinned host memory or a second device set unavailable
+        host = sets = None
+        torch.cuda.empty_cache()
+        return {"unavailable": f"buffers of the end-to-end leg could not be allocated: {str(ex).splitlines()[0]}"}
     many = [gw.many, tl.ManyLists([gw.plist(g, 10 + i) for i, g in enumerate(sets[1])])]
     torch.cuda.synchronize()
     copy_stream = torch.cuda.Stream()
