@@ -524,6 +524,7 @@ def run_e2e(args, gw, world):
     import torch
     import loss_scaled_adamw_gb300 as tl
     k = gw.wl.k
+    why = ""
     try:
         host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gw.grads]
         for h, g in zip(host, gw.grads):
@@ -532,7 +533,11 @@ def run_e2e(args, gw, world):
     except RuntimeError as ex:      # pinned host memory or a second device set unavailable
         host = sets = None
         torch.cuda.empty_cache()
-        return {"unavailable": f"buffers of the end-to-end leg could not be allocated: {str(ex).splitlines()[0]}"}
+        why = str(ex).splitlines()[0]
+    # every rank runs the leg or none does (its barriers and reductions are collective)
+    if max_over_ranks(1.0 if why else 0.0, gw.device) > 0.0:
+        return {"unavailable": "buffers of the end-to-end leg could not be allocated"
+                               + (f": {why}" if why else " on another rank")}
     many = [gw.many, tl.ManyLists([gw.plist(g, 10 + i) for i, g in enumerate(sets[1])])]
     torch.cuda.synchronize()
     copy_stream = torch.cuda.Stream()
