@@ -690,15 +690,15 @@ def main(argv=None):
         if backend == "nccl":
             torch.cuda.set_device(local_rank)
         dist.init_process_group(backend)
-    if True:
-        out = run_gpu(args, rank, world, local_rank)
-        if rank == 0:
-            if not args.no_cpu_baseline:
-                from loss_scaled_adamw_gb300 import workloads as W
-                import oracle
-                oracle.build()
-                out["cpu_baseline"] = time_oracle(W.make(args.workload), args.cpu_seconds)
-            print(json.dumps(out), flush=True)
+    out = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        # the oracle's CPU baseline: rank 0 of a single-GPU run only
+        if not args.no_cpu_baseline and world == 1:
+            from loss_scaled_adamw_gb300 import workloads as W
+            import oracle
+            oracle.build()
+            out["cpu_baseline"] = time_oracle(W.make(args.workload), args.cpu_seconds)
+        print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
