@@ -360,6 +360,16 @@ __device__ __forceinline__ int ephase(const void* p) {
     return static_cast<int>((reinterpret_cast<uintptr_t>(p) / ES) & 7);
 }
 
+// In the vector plan the head (< 8 elements) and the tail (< 8) of a segment are
+// single elements.  A segment that takes them early gives each to one thread:
+// head element t to thread t, tail element done + (t - 8) to thread t >= 8 (a
+// warp has 32 threads).  Returns the element of thread t, or -1.
+__device__ __forceinline__ int edge_element(int t, int head, int done, int len) {
+    if (t < head) return t;
+    if (t >= 8 && t - 8 < len - done) return done + (t - 8);
+    return -1;
+}
+
 template <int NT, int GDT, bool FIRST>
 __device__ __forceinline__ void accumulate_segment(const Chunk& ch, int t, const void* const* gp, float w) {
     float* __restrict__ acc0 = ch.acc;
@@ -953,6 +963,7 @@ __device__ __forceinline__ void adamw1(float u, float& w, float& m, float& v, co
 struct UFromAcc {
     static constexpr int kUnroll = TL_ADAM_UNROLL;
     static constexpr bool kBlocked = false;
+    static constexpr bool kEarly = true;   // edge elements loaded ahead of the vector loop
     struct Raw {
         float x[8];
     };
@@ -976,6 +987,7 @@ struct UFromLists {
         typename GradRaw<GDT>::T r[KM];
     };
     static constexpr bool kBlocked = GDT == kE4M3;  // vectors must start on multiples of 8 elements
+    static constexpr bool kEarly = false;  // KM gradients per edge element would stay live across the loop
     const char* g[KM];
     const float* gs[KM];  // block scales (8-bit gradients)
     const float* w;  // micro-batch weights n_q / N
@@ -1055,6 +1067,19 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Adam
     int head = 0, done = 0;
     if (pl.vec) {
         head = min(pl.head, len);
+        done = head + (len - head) / kVec * kVec;
+    }
+    // with Src::kEarly the edge elements' inputs are loaded before the vector
+    // loop, so that their latency overlaps it, and finished after it
+    const int ej = Src::kEarly && pl.vec ? edge_element(t, head, done, len) : -1;
+    float eu = 0.0f, ew = 0.0f, em = 0.0f, ev = 0.0f;
+    if (ej >= 0) {
+        eu = src.at(ej);
+        ew = w0[ej];
+        em = m0[ej];
+        ev = v0[ej];
+    }
+    if (pl.vec) {
         const bool wide = pl.wide;
         void* p = p0 + head;
         const int nv = (len - head) / kVec;
@@ -1100,8 +1125,15 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Adam
             st8_f32(v0 + o, vx, wide);
             st8_param<PDT>(p, i * kVec, wx);
         }
-        done = head + nv * kVec;
     }
+    if (ej >= 0) {
+        adamw1(eu, ew, em, ev, k);
+        w0[ej] = ew;
+        m0[ej] = em;
+        v0[ej] = ev;
+        Param<PDT>::st1(p0, ej, ew);
+    }
+    if (Src::kEarly && pl.vec) return;
     auto one = [&](int j) {
         float wj = w0[j], mj = m0[j], vj = v0[j];
         adamw1(src.at(j), wj, mj, vj, k);
