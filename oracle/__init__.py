@@ -98,6 +98,7 @@ def _bind(lib):
         "tlo_sumsq": (f64, [vp, i64]),
         "tlo_norm_from_sumsq": (f32, [f64]),
         "tlo_clip_coef": (f32, [f32, f32]),
+        "tlo_scheduled_lr": (f32, [vp, i64, i64]),
         "tlo_adamw_prepare": (AdamWScalars, [ctypes.POINTER(AdamWHP), f64, f64]),
         "tlo_adamw_recast": (None, [vp, vp, vp, vp, i32, vp, i64, f32, ctypes.POINTER(AdamWScalars)]),
         "tlo_scaler_update": (None, [ctypes.POINTER(State), ctypes.POINTER(ScalerCfg), i32, f64, f64]),
@@ -161,10 +162,16 @@ class Oracle:
         return int(self.w.size)
 
     def step(self, grads, counts, max_norm: float, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8,
-             weight_decay=0.1) -> Result:
+             weight_decay=0.1, lr_schedule=None) -> Result:
         """One attempted logical update over k micro-batches (grads[i] is a flat
         array of P gradient values: uint16 bits for bf16/f16, float32 for f32; for
-        e4m3b16 a pair (uint8 codes of P elements, float32 block scales))."""
+        e4m3b16 a pair (uint8 codes of P elements, float32 block scales)).  With
+        lr_schedule (float32 rates of optimizer steps 1, 2, ...) the rate is the
+        schedule's entry for the step this update would commit, in place of lr."""
+        if lr_schedule is not None:
+            table = np.ascontiguousarray(lr_schedule, dtype=np.float32)
+            assert table.size > 0
+            lr = self.lib.tlo_scheduled_lr(_ptr(table), table.size, self.state.t)
         k = len(grads)
         if self.gdtype == DT_E4M3B16:
             assert self.numel is not None and int(self.numel.sum()) == self.P

@@ -270,6 +270,17 @@ typedef struct {
     float lr, beta1, beta2, eps, weight_decay;
 } tlo_adamw_hp;
 
+/* The learning rate a schedule gives the update that would commit optimizer
+ * step t+1, where t counts the committed steps only: [RST] "Discard a failed
+ * partial logical update" (a skipped attempt leaves the optimizer step where it
+ * was and the next scheduled step still available) and "Carry one logical update
+ * into schedule reasoning" (warm-up and decay are stated per logical update).
+ * table[i] is the rate of optimizer step i+1; past the end of the table the last
+ * entry holds. */
+float tlo_scheduled_lr(const float* table, int64_t len, int64_t t) {
+    return table[t < len ? t : len - 1];
+}
+
 /* The per-step scalars of AdamW for the step about to be committed (t+1),
  * computed in fp64 from the beta powers kept as state ([RST] "Discard a
  * failed partial logical update": the optimizer state includes the beta

@@ -303,6 +303,31 @@ def pin_skip_changes_nothing_and_drops_bad_grads(lib):
     assert np.all(np.isfinite(a.w)) and a.state.t == b.state.t == 2
 
 
+def pin_schedule_follows_committed_steps(lib):
+    """[RST] ch. 13 "Discard a failed partial logical update": after one commit and one
+    skipped attempt the optimizer step is still 1, and scheduled step 2 is the one still
+    available.  With zero gradients only the decoupled decay acts, so the rate each update
+    used can be read off exactly.  Start from w0 = 1 with weight decay 1 and rates 1/2, 1/4,
+    1/8 for steps 1-3:
+    - step 1 gives w = 1/2, and the skipped attempt leaves it there;
+    - scheduled step 2 then gives 1/2 - 1/4 * 1/2 = 3/8 (7/16 would mean the attempt had
+      consumed a step);
+    - step 3 gives 21/64;
+    - past the end of the table the last rate holds: 147/512."""
+    table = np.array([0.5, 0.25, 0.125], np.float32)
+    o = make_oracle(lib, np.ones(4, np.float32), pdtype="f16", gdtype="f32")
+    zero = np.zeros(4, np.float32)
+    bad = zero.copy()
+    bad[1] = np.inf
+    hp = dict(max_norm=0.0, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=1.0, lr_schedule=table)
+    want = []
+    for g in (zero, bad, zero, zero, zero):
+        o.step([g], [1], **hp)
+        want.append((float(o.w[0]), int(o.state.t), int(o.last.skipped)))
+    assert want == [(0.5, 1, 0), (0.5, 1, 1), (0.375, 2, 0), (21 / 64, 3, 0), (147 / 512, 4, 0)], want
+    assert np.all(o.w == o.w[0])
+
+
 # --------------------------------------------------------------------------
 # Global norm and clipping
 # --------------------------------------------------------------------------

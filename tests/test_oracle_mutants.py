@@ -58,6 +58,9 @@ MUTANTS = [
     ("m_uses_g_squared", "float mj = s->beta1 * m[j] + s->one_minus_beta1 * g;", "float mj = s->beta1 * m[j] + s->one_minus_beta1 * (g * g);"),
     ("v_uses_g", "s->one_minus_beta2 * (g * g);", "s->one_minus_beta2 * g;"),
     ("update_sign", "wj = wj - s->step_size * (mj / denom);", "wj = wj + s->step_size * (mj / denom);"),
+    # schedule slips: a rate one step ahead, or the first rate for every step
+    ("schedule_off_by_one", "return table[t < len ? t : len - 1];", "return table[t + 1 < len ? t + 1 : len - 1];"),
+    ("schedule_first_only", "return table[t < len ? t : len - 1];", "return table[0];"),
     ("clip_coef_unused", "float g = u[j] * coef;", "float g = u[j];"),
     # recast / formats
     ("bf16_truncates", "if (rem > 0x8000u || (rem == 0x8000u && (kept & 1u))) kept += 1u;\n    return (uint16_t)(sign | kept);",
