@@ -256,6 +256,29 @@ int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream);
  * Errors: TL_EINVAL (hp), TL_ESTATE. */
 int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream);
 
+/* Learning-rate schedule read on the device.  With a schedule set, the update
+ * that would commit optimizer step t+1 (t = committed steps, the device count)
+ * takes lr = lr_table[min(t, len-1)] in place of hp->lr; the other
+ * hyper-parameters still come from tl_clip_adamw_step.  The index counts
+ * committed steps only, so an update skipped on overflow leaves the next
+ * scheduled rate for the next attempt ([RST] ch. 13 "Discard a failed partial
+ * logical update": the optimizer step stays and the scheduled step remains
+ * available; "Carry one logical update into schedule reasoning": warm-up and
+ * decay are per logical update).  Because the rate is chosen on the device, a
+ * skipped step needs no host read, and a captured CUDA graph follows the
+ * schedule on every replay.
+ *   lr_table: len fp32 rates (entry i for optimizer step i+1) in memory the
+ *     device can read (device, managed or pinned host), 4-byte aligned; owned
+ *     by the caller, who keeps it alive and its values finite and >= 0 while
+ *     it is set.  It is read when each AdamW kernel runs, so entries may be
+ *     rewritten between updates in stream order.
+ *   len = 0 (lr_table ignored) removes the schedule: hp->lr applies again.
+ * Takes effect for the tl_clip_adamw_step calls made after it (a CUDA graph
+ * keeps the table address it was captured with).  Host-only; launches nothing.
+ * Errors: TL_EINVAL (len < 0; lr_table NULL, misaligned or not readable by
+ * the device when len > 0). */
+int tl_set_lr_schedule(tl_ctx* ctx, const float* lr_table, int64_t len);
+
 /* Scaler state machine and optimizer scalars (a6).  [MEG] section 5; [MP]
  * "Dynamic scaling" and the five-step trace of section 3; [RST] ch. 13
  * "Discard a failed partial logical update".

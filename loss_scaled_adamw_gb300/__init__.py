@@ -33,7 +33,7 @@ EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "t
             "tl_unscale_check", "tl_grad_norm",
             "tl_clip_adamw_step", "tl_scaler_update", "tl_read_status", "tl_get_state", "tl_set_state",
             "tl_scale_ptr", "tl_num_params", "tl_num_chunks", "tl_launch_count", "tl_status_string",
-            "tl_last_error", "tl_unscale_norm_noalloc", "tl_loss_seed")
+            "tl_last_error", "tl_unscale_norm_noalloc", "tl_loss_seed", "tl_set_lr_schedule")
 
 
 class TLError(RuntimeError):
@@ -126,6 +126,7 @@ def load_library():
         "tl_last_error": (ctypes.c_char_p, [vp]),
         "tl_unscale_norm_noalloc": (i32, [i64, ctypes.POINTER(i64), pp, f32, f32, vp, vp]),
         "tl_loss_seed": (i32, [vp, i64, i64, vp, vp]),
+        "tl_set_lr_schedule": (i32, [vp, vp, i64]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -173,6 +174,7 @@ class Context:
     def __init__(self, handle: ctypes.c_void_p, keep):
         self.handle = handle
         self._keep = keep
+        self.lr_table = None  # the learning-rate schedule tensor while one is set
 
     def __del__(self):
         if getattr(self, "handle", None) and _lib is not None:
@@ -293,6 +295,22 @@ def tl_loss_seed(ctx: Context, n_i: int, N: int, out_addr: int, stream=None) -> 
     """Write S * n_i / N (fp32) to the device address out_addr on the stream."""
     _check(ctx, "tl_loss_seed", load_library().tl_loss_seed(ctx.handle, int(n_i), int(N),
                                                             ctypes.c_void_p(int(out_addr)), _stream(stream)))
+
+
+def tl_set_lr_schedule(ctx: Context, table) -> None:
+    """Learning rates of optimizer steps 1, 2, ... read on the device (a float32 CUDA
+    tensor), or None to go back to hp.lr.  The context keeps a reference to the tensor
+    while it is set."""
+    if table is None:
+        _check(ctx, "tl_set_lr_schedule", load_library().tl_set_lr_schedule(ctx.handle, None, 0))
+        ctx.lr_table = None
+        return
+    import torch
+    if table.dtype != torch.float32 or not table.is_contiguous() or table.dim() != 1:
+        raise ValueError("the schedule is a contiguous 1-D float32 tensor")
+    _check(ctx, "tl_set_lr_schedule", load_library().tl_set_lr_schedule(
+        ctx.handle, ctypes.c_void_p(table.data_ptr()), int(table.numel())))
+    ctx.lr_table = table
 
 
 def tl_num_params(ctx: Context) -> int:

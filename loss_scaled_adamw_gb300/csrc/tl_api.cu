@@ -112,6 +112,9 @@ struct tl_ctx {
     int remat_k = 0;
     std::vector<const void*> remat_grads;
     int64_t remat_n[kRematLists] = {};
+    // learning-rate schedule read by the AdamW kernels (caller-owned; null: hp.lr)
+    const float* lr_sched = nullptr;
+    int64_t lr_len = 0;
     int64_t launches = 0;
     std::string last_error;
 };
@@ -774,7 +777,7 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         return fail(ctx, TL_EINVAL, "AdamW hyper-parameters out of range");
     int rc;
     if ((rc = check_device(ctx)) != TL_OK) return rc;
-    AdamHP h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+    AdamHP h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, ctx->lr_sched, ctx->lr_len};
     const int pdt = ctx->cfg.param_dtype;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
@@ -920,6 +923,37 @@ int tl_loss_seed(tl_ctx* ctx, int64_t n_i, int64_t N, float* out, tl_stream stre
     cudaError_t e = launch_seed(ctx->d_state, w, out, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(ctx, e, "seed launch");
     ctx->launches += 1;
+    return TL_OK;
+}
+
+int tl_set_lr_schedule(tl_ctx* ctx, const float* lr_table, int64_t len) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (len < 0) return fail(ctx, TL_EINVAL, "schedule length must be >= 0");
+    if (len == 0) {
+        ctx->lr_sched = nullptr;
+        ctx->lr_len = 0;
+        return TL_OK;
+    }
+    if (lr_table == nullptr || (reinterpret_cast<uintptr_t>(lr_table) & 3u) != 0)
+        return fail(ctx, TL_EINVAL, "schedule must be a 4-byte aligned address");
+    int rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    // the kernels read the table: it must be memory the device can address
+    cudaPointerAttributes at{};
+    cudaError_t e = cudaPointerGetAttributes(&at, lr_table);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "schedule address");
+    bool readable = at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged ||
+                    (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr);
+    if (at.type == cudaMemoryTypeDevice && at.device != ctx->device) readable = false;
+    if (!readable) {
+        int pageable = 0;
+        if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, ctx->device) !=
+            cudaSuccess)
+            pageable = 0;
+        if (!pageable) return fail(ctx, TL_EINVAL, "schedule must be in memory the device can read");
+    }
+    ctx->lr_sched = lr_table;
+    ctx->lr_len = len;
     return TL_OK;
 }
 

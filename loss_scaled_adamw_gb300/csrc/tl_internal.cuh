@@ -109,6 +109,8 @@ struct ScalerParams {
 
 struct AdamHP {
     float lr, beta1, beta2, eps, wd;
+    const float* lr_sched;  // device schedule: lr = lr_sched[min(t, lr_len - 1)] when set
+    int64_t lr_len;
 };
 
 // What the a3 kernel reads besides the accumulation buffer.

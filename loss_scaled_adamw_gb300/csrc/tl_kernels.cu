@@ -1181,10 +1181,14 @@ __device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const Ada
         skip = f;
         const double b1n = __dmul_rn(st->b1p, static_cast<double>(hp.beta1));
         const double b2n = __dmul_rn(st->b2p, static_cast<double>(hp.beta2));
+        // a schedule is indexed by the committed steps: a skipped attempt leaves
+        // the next scheduled rate for the next one
+        const int64_t t = st->t;
+        const float lr = hp.lr_sched != nullptr ? hp.lr_sched[t < hp.lr_len ? t : hp.lr_len - 1] : hp.lr;
         AdamConsts k;
-        k.step = __double2float_rn(__ddiv_rn(static_cast<double>(hp.lr), __dadd_rn(1.0, -b1n)));
+        k.step = __double2float_rn(__ddiv_rn(static_cast<double>(lr), __dadd_rn(1.0, -b1n)));
         k.bc2s = __double2float_rn(__dsqrt_rn(__dadd_rn(1.0, -b2n)));
-        k.lrwd = __double2float_rn(__dmul_rn(static_cast<double>(hp.lr), static_cast<double>(hp.wd)));
+        k.lrwd = __double2float_rn(__dmul_rn(static_cast<double>(lr), static_cast<double>(hp.wd)));
         k.b1 = hp.beta1;
         k.omb1 = __fsub_rn(1.0f, hp.beta1);
         k.b2 = hp.beta2;

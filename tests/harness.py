@@ -228,10 +228,12 @@ def compare_scalars(st, orc, res, what: str, check_norm=True):
 
 
 def run_parity(wl: W.Workload, gaps=False, device="cuda", steps=None, compare_every=1, hp=None, max_norm=None,
-               resident=False):
+               resident=False, lr_schedule=None):
     """Run `steps` logical updates of a workload on the GPU and in the oracle from the same
     inputs, comparing scalars after every step and the state every `compare_every` steps.
-    resident=True drives the many-list pass (all k micro-batches read in one pass)."""
+    resident=True drives the many-list pass (all k micro-batches read in one pass).
+    lr_schedule (float32 rates of optimizer steps 1, 2, ...) is set on the device and
+    given to the oracle."""
     import torch
     master0 = W.master_init(wl, "cpu")
     gpu = GpuOptimizer(wl, master0, gaps=gaps, device=device)
@@ -239,13 +241,18 @@ def run_parity(wl: W.Workload, gaps=False, device="cuda", steps=None, compare_ev
     hp = hp or W.HP
     mn = wl.max_norm if max_norm is None else max_norm
     steps = wl.steps if steps is None else steps
+    okw = {}
+    if lr_schedule is not None:
+        table = np.ascontiguousarray(lr_schedule, dtype=np.float32)
+        tl.tl_set_lr_schedule(gpu.ctx, torch.from_numpy(table).to(device))
+        okw["lr_schedule"] = table
     log = []
     for step in range(1, steps + 1):
         counts = wl.counts(step)
         S = orc.state.S  # the oracle's loss scale decides how the next gradients are scaled
         grads = [W.grad_input(wl, step, i, scale=S, device="cpu") for i in range(wl.k)]
         gpu.step(grads, counts, hp=hp, max_norm=mn, resident=resident)
-        res = orc.step([grad_bits(g) for g in grads], counts, mn, **hp)
+        res = orc.step([grad_bits(g) for g in grads], counts, mn, **hp, **okw)
         st = gpu.status()
         compare_scalars(st, orc, res, f"{wl.name} step {step}")
         entry = {"step": step, "skipped": res.skipped, "S": st.S, "norm_gpu": st.norm, "norm_oracle": res.norm}

@@ -108,6 +108,7 @@ def test_calls_on_null_context_are_rejected(lib):
     assert lib.tl_read_status(None, None, None) == tl.TL_EINVAL
     assert lib.tl_get_state(None, None, None) == tl.TL_EINVAL
     assert lib.tl_set_state(None, None, None) == tl.TL_EINVAL
+    assert lib.tl_set_lr_schedule(None, None, 0) == tl.TL_EINVAL
     assert lib.tl_destroy(None) == tl.TL_OK
     assert lib.tl_scale_ptr(None) is None
     assert lib.tl_num_params(None) == 0 and lib.tl_launch_count(None) == 0
