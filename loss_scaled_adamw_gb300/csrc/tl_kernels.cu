@@ -46,6 +46,11 @@ namespace {
 #ifndef TL_MINB_MANY
 #define TL_MINB_MANY 3
 #endif
+// 8-bit lists put fewer bytes in flight per thread (8 codes and a shared scale
+// per list and vector): more resident warps make up for it
+#ifndef TL_MINB_MANY_E4M3
+#define TL_MINB_MANY_E4M3 4
+#endif
 #ifndef TL_MINB_FEW
 #define TL_MINB_FEW 5
 #endif
@@ -842,7 +847,7 @@ template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
 __global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
                                             : GDT == kF32 ? 2
                                             : KM <= kFewLists ? (GDT == kE4M3 || (LAST && !FIRST) ? TL_MINB_FEW - 1 : TL_MINB_FEW)
-                                            : TL_MINB_MANY)
+                                            : GDT == kE4M3 ? TL_MINB_MANY_E4M3 : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
              const __grid_constant__ GradTableMany inl,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
