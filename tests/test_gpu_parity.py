@@ -442,12 +442,17 @@ def test_ragged_100k_full(layout):
     run_parity(wl, gaps=layout, compare_every=wl.steps)
 
 
-def test_llama_1b_full_size_sampled():
-    """The ~1.24B-parameter list at full size, k=8, in the benchmark's launch configuration:
-    the norm against the oracle's sum over every element (streamed through host memory in
-    slices), and 200,000 sampled elements of master, m, v and params computed one by one."""
+@pytest.mark.parametrize("name,resident", [("llama_1b", True), ("llama_1b", False), ("llama_1b_fp8", True)],
+                         ids=["bf16-resident", "bf16-per_microbatch", "e4m3b16-resident"])
+def test_llama_1b_full_size_sampled(name, resident):
+    """The ~1.24B-parameter list at full size, k=8, through the call sequence the
+    benchmark times (resident: the headline), the per-micro-batch sequence, and the
+    resident sequence over 8-bit block-scaled gradients.  The norm is checked against
+    the oracle's sum over every element; 200,000 sampled elements of master, m, v and
+    params are computed one by one through the oracle's functions."""
     import oracle
-    wl = W.make("llama_1b")
+    wl = W.make(name)
+    fp8 = wl.grad_dtype == "e4m3b16"
     master0 = W.master_init(wl, "cuda")
     gpu = GpuOptimizer(wl, master0)
     counts = wl.counts(1)
@@ -457,8 +462,7 @@ def test_llama_1b_full_size_sampled():
     idx = np.unique(rng.integers(0, wl.P, 200_000))
     idx_t = torch.from_numpy(idx).cuda()
     w0 = master0[idx_t].cpu().numpy()
-    g_s = [grad_bits(g[idx_t]) for g in grads]
-    gpu.step(grads, counts)
+    gpu.step(grads, counts, resident=resident)
     st = gpu.status()
     lib = oracle.load()
 
@@ -466,18 +470,23 @@ def test_llama_1b_full_size_sampled():
         return a.ctypes.data_as(ctypes.c_void_p)
 
     weights = [lib.tlo_microbatch_weight(n, N) for n in counts]
-    # oracle squared norm over all elements, streamed in slices of 2^26
-    sumsq = 0.0
-    found = 0
-    step = 1 << 26
-    for lo in range(0, wl.P, step):
-        hi = min(wl.P, lo + step)
-        acc = np.empty(hi - lo, np.float32)
-        for i, g in enumerate(grads):
-            gb = grad_bits(g[lo:hi])
-            lib.tlo_accumulate(P_(acc), P_(gb), oracle.DT_BF16, hi - lo, weights[i], 1 if i == 0 else 0)
-        found |= lib.tlo_unscale_check(P_(acc), hi - lo, 1.0)
-        sumsq += lib.tlo_sumsq(P_(acc), hi - lo)
+    # the oracle's u over every element, one list at a time (host memory), keeping
+    # each list's sampled inputs for the element-wise check below
+    acc = np.empty(wl.P, np.float32)
+    samples = []
+    for i, g in enumerate(grads):
+        if fp8:
+            vals = oracle.dequant_e4m3b16(g[0].cpu().numpy(), g[1].cpu().numpy(), wl.numel)
+            dt = oracle.DT_F32
+        else:
+            vals = np.ascontiguousarray(grad_bits(g))
+            dt = oracle.DT_BF16
+        lib.tlo_accumulate(P_(acc), P_(vals), dt, wl.P, weights[i], 1 if i == 0 else 0)
+        samples.append((np.ascontiguousarray(vals[idx]), dt))
+        del vals
+    found = lib.tlo_unscale_check(P_(acc), wl.P, 1.0)
+    sumsq = lib.tlo_sumsq(P_(acc), wl.P)
+    del acc
     assert found == 0 and st.found_inf == 0 and st.skipped == 0
     norm = lib.tlo_norm_from_sumsq(sumsq)
     assert abs(st.norm - norm) <= 1e-6 * norm, (st.norm, norm)
@@ -485,8 +494,8 @@ def test_llama_1b_full_size_sampled():
     # sampled elements, one by one, through the oracle's functions in the step's order
     n = idx.size
     acc = np.empty(n, np.float32)
-    for i in range(wl.k):
-        lib.tlo_accumulate(P_(acc), P_(np.ascontiguousarray(g_s[i])), oracle.DT_BF16, n, weights[i], 1 if i == 0 else 0)
+    for i, (vals, dt) in enumerate(samples):
+        lib.tlo_accumulate(P_(acc), P_(vals), dt, n, weights[i], 1 if i == 0 else 0)
     lib.tlo_unscale_check(P_(acc), n, 1.0)
     hp = oracle.AdamWHP(**{k: v for k, v in W.HP.items()})
     sc = lib.tlo_adamw_prepare(ctypes.byref(hp), float(np.float32(0.9)), float(np.float32(0.95)))
@@ -496,11 +505,11 @@ def test_llama_1b_full_size_sampled():
     p = np.empty(n, np.uint16)
     lib.tlo_adamw_recast(P_(w), P_(m), P_(v), P_(p), oracle.DT_BF16, P_(acc), n, coef, ctypes.byref(sc))
     L = gpu.lists
-    assert_ulps32(L["master"].flat()[idx_t].cpu().numpy(), w, 2, "llama_1b master")
-    assert_ulps32(L["m"].flat()[idx_t].cpu().numpy(), m, 2, "llama_1b m")
-    assert_ulps32(L["v"].flat()[idx_t].cpu().numpy(), v, 2, "llama_1b v")
+    assert_ulps32(L["master"].flat()[idx_t].cpu().numpy(), w, 2, f"{name} master")
+    assert_ulps32(L["m"].flat()[idx_t].cpu().numpy(), m, 2, f"{name} m")
+    assert_ulps32(L["v"].flat()[idx_t].cpu().numpy(), v, 2, f"{name} v")
     gp = L["param"].flat()[idx_t].cpu().view(torch.int16).numpy().view(np.uint16)
-    assert_ulps16(gp, p, 1, "llama_1b param")
+    assert_ulps16(gp, p, 1, f"{name} param")
     assert st.t == 1
 
 
