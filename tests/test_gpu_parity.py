@@ -432,14 +432,21 @@ def test_single_tensor_beyond_2_pow_31_full():
 # the full-size workloads
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("layout", [True, "packed"], ids=["misaligned", "packed"])
-def test_ragged_100k_full(layout):
-    """100,000 ragged tensors (~400M parameters) in flat buffers, either with independent
-    seeded gaps (most tensors off any 16-byte boundary, scalar paths) or packed back to
-    back (same element phase in every list: peeled vector paths); fp16 with loss
-    scaling, an inf in micro-batch 1 of step 2; every element compared."""
+@pytest.mark.parametrize("layout,resident", [(True, False), ("packed", False), (False, True), (False, "remat")],
+                         ids=["misaligned", "packed", "aligned-resident", "aligned-remat"])
+def test_ragged_100k_full(layout, resident):
+    """100,000 ragged tensors (~400M parameters) in flat buffers.  Three layouts:
+    - independent seeded gaps: most tensors off any 16-byte boundary, so the scalar
+      paths run;
+    - packed back to back: the same element phase in every list, so the peeled
+      vector paths run;
+    - every tensor 32-byte aligned, with the resident and the re-materialising
+      sequences the benchmark times.
+    fp16 with loss scaling and an inf in micro-batch 1 of step 2; every element is
+    compared."""
     wl = W.make("ragged_100k")
-    run_parity(wl, gaps=layout, compare_every=wl.steps)
+    _, _, log = run_parity(wl, gaps=layout, compare_every=wl.steps, resident=resident)
+    assert [e["skipped"] for e in log] == [0, 1, 0]
 
 
 @pytest.mark.parametrize("name,resident", [("llama_1b", True), ("llama_1b", False), ("llama_1b_fp8", True)],
