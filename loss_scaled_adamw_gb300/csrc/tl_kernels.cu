@@ -51,6 +51,15 @@ namespace {
 #ifndef TL_MINB_MANY_E4M3
 #define TL_MINB_MANY_E4M3 4
 #endif
+// Small-tensor groups (a warp per tensor, a few hundred elements each) are
+// latency-bound: more resident CTAs keep more tensors in flight.  The one- and
+// two-list forms of the many-list kernel, and AdamW.
+#ifndef TL_MINB_GROUP_FEW
+#define TL_MINB_GROUP_FEW 5
+#endif
+#ifndef TL_MINB_ADAM_GROUP
+#define TL_MINB_ADAM_GROUP 3
+#endif
 #ifndef TL_MINB_FEW
 #define TL_MINB_FEW 5
 #endif
@@ -844,7 +853,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
 }
 
 template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
-__global__ void __launch_bounds__(kThreads, NT != kThreads ? 1
+__global__ void __launch_bounds__(kThreads, NT != kThreads ? (GDT == kF32 || KM > kFewLists ? 1 : GDT == kE4M3 ? TL_MINB_GROUP_FEW - 1 : TL_MINB_GROUP_FEW)
                                             : GDT == kF32 ? 2
                                             : KM <= kFewLists ? (GDT == kE4M3 || (LAST && !FIRST) ? TL_MINB_FEW - 1 : TL_MINB_FEW)
                                             : GDT == kE4M3 ? TL_MINB_MANY_E4M3 : TL_MINB_MANY)
@@ -1212,7 +1221,7 @@ __device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const Ada
 }
 
 template <int NT, int PDT>
-__global__ void __launch_bounds__(kThreads, TL_MINB_ADAM)
+__global__ void __launch_bounds__(kThreads, NT != kThreads ? TL_MINB_ADAM_GROUP : TL_MINB_ADAM)
 k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
         DevState* __restrict__ st, AdamHP hp) {
     AdamConsts k;
