@@ -540,6 +540,14 @@ __device__ __forceinline__ float unscale1(float a, float gj, float w, float inv_
 // by many ulps.)  A vector holding a larger or infinite value is summed in fp64
 // instead, so the total is infinite exactly when some fp32 square is; NaN
 // propagates through the float-float path.
+// d + q in fp64 for the rare large-value case of the squared-norm sum, kept out
+// of line: inlined into a per-element loop it may be if-converted, and then every
+// element issues the fp64 instructions, which this GPU runs at a small fraction
+// of the fp32 rate.
+__device__ __noinline__ double dadd_out_of_line(double d, float q) {
+    return __dadd_rn(d, static_cast<double>(q));
+}
+
 struct SumSq {
     float hi = 0.0f;
     float lo = 0.0f;
@@ -574,7 +582,7 @@ struct SumSq {
         const float q = __fmul_rn(u, u);
         if (fabsf(u) >= 72057594037927936.0f) {
             big = true;
-            d = __dadd_rn(d, static_cast<double>(q));
+            d = dadd_out_of_line(d, q);
             return;
         }
         add(q);
