@@ -103,7 +103,8 @@ typedef void* tl_stream;
  * [MP] section 4 "The interface": DynamicLossScaler(init=2^16, growth=2,
  * backoff=0.5, interval=2000); [MEG] section 5: the controller and its
  * min_loss_scale floor.  All five scale values must be powers of two so that
- * unscaling only changes exponents ([MP] section 2 "Loss scaling").  With
+ * unscaling only changes exponents ([MP] section 2 "Loss scaling"), and the
+ * loss scales at least 2^-126 (normal numbers, so that 1/S is finite).  With
  * scaler_enabled = 0 (bf16 training, [MP] "Dynamic scaling": bf16 needs no
  * scaler) S stays 1, the good-step count stays 0, and the finite check still
  * gates every update. */
@@ -330,17 +331,23 @@ typedef struct {
  * another allocator, no allocation allowed after start-up, or an allocation
  * that would disturb a capture or a memory plan), who therefore cannot use
  * tl_create.  It needs no context.
- * acc: ntensors fp32 device tensors of numel[i] elements, holding the
- * accumulated scaled gradient; they are overwritten with u = acc * (1/S).
- * S: a positive power of two.  max_norm <= 0 disables clipping.  out: device
- * memory (8-byte aligned) that receives the result; same arithmetic as
- * tl_unscale_check + tl_grad_norm.
- * Scratch: a fixed array inside the library (512 KiB of fp64 partials,
- * allocated when the library is loaded and held by every GPU that loads it
- * until the process exits).  Limits: ntensors <= 256 and at most 2^16 chunks
- * of 16,384 elements (2^30 elements); larger lists give TL_EINVAL.  The first
- * call on a device looks up the scratch address for that device, so make that
- * first call before any stream capture.  Every call shares the scratch and
+ * acc: ntensors fp32 device tensors of numel[i] elements (4-byte aligned),
+ * holding the accumulated scaled gradient; they are overwritten with
+ * u = acc * (1/S).  S: a power of two, at least 2^-126 (so that 1/S is exact
+ * and finite).  max_norm <= 0 disables clipping.  out: device memory (8-byte
+ * aligned) that receives the result.  u and the overflow rule are those of
+ * tl_unscale_check (u bit for bit); the squared norm is summed in another
+ * order (fp32 over 8 squares, fp64 beyond), so norm and sumsq agree with
+ * tl_grad_norm to 1e-6 relative, not bit for bit.
+ * Scratch: a fixed array inside the library, 512 KiB of fp64 partials, held
+ * by every GPU that loads it until the process exits.  Under CUDA's lazy
+ * module loading (the default) the array is created on a device by the FIRST
+ * call of this function there, which therefore takes device memory once and
+ * can fail for want of it; later calls allocate nothing.  Make that first
+ * call on each device before any stream capture and before handing all
+ * device memory to another allocator (or set CUDA_MODULE_LOADING=EAGER).
+ * Limits: ntensors <= 256 and at most 2^16 chunks of 16,384 elements (2^30
+ * elements); larger lists give TL_EINVAL.  Every call shares the scratch and
  * writes every partial it reads; calls that overlap on the GPU race on it.
  * Errors: TL_EINVAL (sizes, pointers, S), TL_ECUDA. */
 int tl_unscale_norm_noalloc(int64_t ntensors, const int64_t* numel, float* const* acc, float S,

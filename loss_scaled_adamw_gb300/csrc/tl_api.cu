@@ -8,6 +8,7 @@
 #include "tl_internal.cuh"
 
 #include <algorithm>
+#include <cfloat>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -32,8 +33,10 @@ uintptr_t grad_bytes(int dt, int64_t n) {
     return uintptr_t(n) * uintptr_t(elem_size(dt));
 }
 
+// A normal power of two (>= 2^-126): unscaling by it only changes exponents and
+// its reciprocal is finite.
 bool is_pow2(float x) {
-    if (!(x > 0.0f) || !std::isfinite(x)) return false;
+    if (!(x >= FLT_MIN) || !std::isfinite(x)) return false;
     int e = 0;
     return std::frexp(x, &e) == 0.5f;
 }

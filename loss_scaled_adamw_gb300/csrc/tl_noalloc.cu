@@ -9,9 +9,19 @@
 // allocate after initialisation (latency-critical or certified loops), and code
 // running where a new allocation would break an ongoing capture or an external
 // memory plan.  For them this entry point does the unscale / overflow / norm /
-// clip part of the step with scratch memory that exists from the moment the
-// library is loaded: a file-scope __device__ array below, which every GPU that
-// loads the library holds until the process exits.
+// clip part of the step with scratch memory that the library brings with it: a
+// file-scope __device__ array below, which every GPU that loads this code holds
+// until the process exits.
+//
+// When the scratch comes into being.  Under CUDA's lazy module loading (the
+// default of recent toolkits) the module holding the array is loaded on a
+// device at its first use there: the first call of this entry point on that
+// device (its symbol lookup, occupancy query or launch).  That first call
+// therefore takes device memory once (the 512 KiB array and the module's code)
+// and can fail for want of it; it must come before any stream capture and
+// before all device memory has been handed to another allocator.  Every later
+// call on that device allocates nothing.  With CUDA_MODULE_LOADING=EAGER in the
+// environment the module is loaded with the CUDA context instead.
 //
 // Limits: at most kNoAllocMaxTensors tensors and kNoAllocMaxChunks chunks of
 // kChunk elements (2^16 * 2^14 = 2^30 elements); larger lists are rejected
@@ -21,6 +31,7 @@
 // at once) race on it and must be serialised by the caller.
 #include "tl_internal.cuh"
 
+#include <cfloat>
 #include <cmath>
 #include <mutex>
 
@@ -149,8 +160,10 @@ std::mutex g_setup_mu;
 double* g_scratch_addr[kMaxDevices] = {nullptr};
 int g_grid[kMaxDevices] = {0};
 
+// A normal power of two: its reciprocal is then exact and finite (a subnormal S
+// below 2^-127 would make 1/S overflow to infinity).
 bool pow2(float x) {
-    if (!(x > 0.0f) || !std::isfinite(x)) return false;
+    if (!(x >= FLT_MIN) || !std::isfinite(x)) return false;
     int e = 0;
     return std::frexp(x, &e) == 0.5f;
 }
@@ -212,7 +225,7 @@ extern "C" int tl_unscale_norm_noalloc(int64_t ntensors, const int64_t* numel, f
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (nchunks > 0) {
         const int g = static_cast<int>(nchunks < grid ? nchunks : grid);
-        k_noalloc_unscale<<<g, kThreads, 0, s>>>(L, 1.0f / S, nchunks);  // S a power of two: exact
+        k_noalloc_unscale<<<g, kThreads, 0, s>>>(L, 1.0f / S, nchunks);  // S a normal power of two: exact
         if (cudaGetLastError() != cudaSuccess) return TL_ECUDA;
     }
     k_noalloc_norm<<<1, kNoAllocNormThreads, 0, s>>>(partials, nchunks, max_norm, out);

@@ -92,7 +92,9 @@ def test_create_rejects_invalid_arguments(lib):
                      "backoff_ge_1": dict(scaler_enabled=True, backoff=1.0),
                      "interval_0": dict(scaler_enabled=True, interval=0),
                      "min_gt_max": dict(scaler_enabled=True, min_scale=8.0, max_scale=4.0),
-                     "init_below_min": dict(scaler_enabled=True, init_scale=1.0, min_scale=2.0)}.items():
+                     "init_below_min": dict(scaler_enabled=True, init_scale=1.0, min_scale=2.0),
+                     # a subnormal floor: 1/S would overflow to infinity
+                     "min_subnormal": dict(scaler_enabled=True, init_scale=1.0, min_scale=2.0 ** -127)}.items():
         cfg = tl.make_config(**{**dict(param_dtype=tl.TL_BF16, grad_dtype=tl.TL_BF16), **kw})
         cases[name] = (numel, lists, cfg)
     for name, (nm, ls, cfg) in cases.items():

@@ -3,11 +3,17 @@
 an allocation that would disturb a capture or memory plan).  It works from a scratch
 array compiled into the library instead of memory it allocates.
 
-Checked through the C ABI against the allocating entry points (tl_accumulate with
-one full-weight micro-batch, tl_unscale_check, tl_grad_norm) on the same inputs, on
-two calls in a row: the unscaled gradient bit for bit, the norm to 1e-6 relative,
-the clip coefficient and the overflow flag exactly.  This file is collected last
-on purpose."""
+Checked through the C ABI, on two calls in a row each time:
+  - against the allocating entry points (tl_accumulate with one full-weight
+    micro-batch, tl_unscale_check, tl_grad_norm) on the same inputs: the unscaled
+    gradient bit for bit, the norm to 1e-6 relative, the clip coefficient and the
+    overflow flag exactly;
+  - against the oracle (its unscale/check, squared-norm sum and clip coefficient)
+    with tensors 16-byte aligned, tensors at 4-byte but not 16-byte offsets (the
+    scalar loop), and elements near 2^63 whose fp32 squares are finite but whose
+    fp32 sums overflow (the fp64 fallback);
+  - that a call after the first on a device leaves the free device memory unchanged.
+This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -97,6 +103,73 @@ def test_no_alloc_matches_allocating_path_twice():
             assert np.isinf(got.norm) and np.isinf(ref.norm) and got.coef == ref.coef
 
 
+def _oracle_reference(vals, S, max_norm):
+    """u, overflow flag, squared norm, norm and clip coefficient of one flat fp32 list from
+    the oracle's functions (the allocation-free call computes exactly this)."""
+    import oracle
+    lib = oracle.load()
+    u = np.ascontiguousarray(vals, dtype=np.float32).copy()
+    P_ = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    found = lib.tlo_unscale_check(P_(u), u.size, S)
+    sumsq = lib.tlo_sumsq(P_(u), u.size)
+    norm = lib.tlo_norm_from_sumsq(sumsq)
+    return u, found, sumsq, norm, lib.tlo_clip_coef(norm, max_norm)
+
+
+def _place(numel, misalign):
+    """Tensor offsets (in fp32 elements) in one flat buffer: 16-byte aligned, or shifted by
+    1-3 elements so that most tensors start on a 4-byte but not a 16-byte boundary."""
+    offs, pos = [], 0
+    for i, n in enumerate(numel):
+        pos = (pos + 7) // 8 * 8 + ((1 + i % 3) if misalign else 0)
+        offs.append(pos)
+        pos += n
+    return offs, pos
+
+
+@pytest.mark.parametrize("case", ["aligned", "misaligned", "large_values"])
+def test_no_alloc_matches_oracle_twice(case):
+    import oracle  # noqa: F401  (built by the fixture's build step)
+    misalign = case == "misaligned"
+    offs, total = _place(NUMEL, misalign)
+    buf = torch.zeros(total + 16, dtype=torch.float32, device="cuda")
+    addrs = [buf.data_ptr() + 4 * o for o in offs]
+    if misalign:
+        assert sum(a % 16 != 0 for a, n in zip(addrs, NUMEL) if n) >= 6
+    out = torch.zeros(4, dtype=torch.float64, device="cuda")
+    rng = np.random.default_rng(7 + len(case))
+    free_before_second = None
+    for call in range(2):
+        vals = (rng.standard_normal(total) * 0.01 * S).astype(np.float32)
+        if case == "large_values":
+            # u near 1.5 * 2^63: each fp32 square (about 1.9e38) is finite, the sum of two is not
+            for o, n in zip(offs, NUMEL):
+                if n >= 64:
+                    vals[o + 8:o + 24] = np.float32(1.5 * 2.0 ** 63 * S) * (1 + 0.01 * np.arange(16, dtype=np.float32))
+        if call == 1 and case != "large_values":
+            vals[offs[5] + 77] = np.nan                  # the second call overflows
+        buf.copy_(torch.from_numpy(vals))
+        torch.cuda.synchronize()
+        if call == 1:
+            free_before_second = torch.cuda.mem_get_info()[0]
+        tl.tl_unscale_norm_noalloc(NUMEL, tl.PtrList(addrs), S, MAX_NORM, out.data_ptr())
+        got = _result(out)
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] == free_before_second, "the second call allocated device memory"
+        flat = np.concatenate([vals[o:o + n] for o, n in zip(offs, NUMEL)])
+        u_ref, found, sumsq, norm, coef = _oracle_reference(flat, S, MAX_NORM)
+        res = buf.cpu().numpy()
+        u_gpu = np.concatenate([res[o:o + n] for o, n in zip(offs, NUMEL)])
+        assert np.array_equal(u_gpu.view(np.uint32), u_ref.view(np.uint32)), f"{case} call {call}: u differs"
+        assert got.found_inf == found, (case, call, got.found_inf, found)
+        if not found:
+            assert abs(got.sumsq - sumsq) <= 2e-6 * sumsq, (got.sumsq, sumsq)
+            assert abs(got.norm - norm) <= 1e-6 * norm, (got.norm, norm)
+            assert abs(got.coef - coef) <= 2e-6 * coef, (got.coef, coef)
+        if case == "large_values":
+            assert found == 0 and got.norm > 1e19 and got.coef < 1e-18
+
+
 def test_no_alloc_rejects_lists_beyond_its_scratch():
     out = torch.zeros(4, dtype=torch.float64, device="cuda")
     big = [1 << 30, 1]  # 2^16 + 1 chunks of 2^14: more than the scratch holds
@@ -107,6 +180,8 @@ def test_no_alloc_rejects_lists_beyond_its_scratch():
         tl.tl_unscale_norm_noalloc([1] * 257, tl.PtrList([(1 << 40) + 64 * i for i in range(257)]), S, MAX_NORM,
                                    out.data_ptr())
     assert ei.value.status == tl.TL_EINVAL
-    with pytest.raises(tl.TLError) as ei:
-        tl.tl_unscale_norm_noalloc([4], tl.PtrList([1 << 40]), 3.0, MAX_NORM, out.data_ptr())
-    assert ei.value.status == tl.TL_EINVAL
+    # S must be a normal power of two: 3 is none, and below 2^-126 the reciprocal is not finite
+    for bad_s in (3.0, 2.0 ** -127, 2.0 ** -149, 0.0, float("inf")):
+        with pytest.raises(tl.TLError) as ei:
+            tl.tl_unscale_norm_noalloc([4], tl.PtrList([1 << 40]), bad_s, MAX_NORM, out.data_ptr())
+        assert ei.value.status == tl.TL_EINVAL, bad_s
