@@ -55,6 +55,8 @@ class Workload:
     scaler_enabled: bool = False
     init_scale: float = 1.0
     interval: int = 2000
+    min_scale: float = 1.0            # the loss scale's floor and cap (powers of two)
+    max_scale: float = 2.0 ** 127
     max_norm: float = 1.0
     master_std: float = 0.02
     # (step, micro-batch) -> list of (flat element index, 16-bit pattern)

@@ -149,7 +149,8 @@ class GpuOptimizer:
         self.lists["master"].load(master0)
         self.lists["param"].load(W.to_16bit(master0.to(device), wl.param_dtype))
         cfg = tl.make_config(DT[wl.param_dtype], DT[wl.grad_dtype], wl.scaler_enabled, wl.init_scale
-                             if wl.scaler_enabled else 1.0, interval=wl.interval)
+                             if wl.scaler_enabled else 1.0, interval=wl.interval, min_scale=wl.min_scale,
+                             max_scale=wl.max_scale)
         L = self.lists
         self.ctx = tl.tl_create(wl.numel, L["param"].ptrs, L["master"].ptrs, L["m"].ptrs, L["v"].ptrs,
                                 L["acc"].ptrs, cfg)
@@ -192,7 +193,8 @@ def oracle_for(wl: W.Workload, master0):
     p0 = W.to_16bit(master0.cpu(), wl.param_dtype).view(torch.int16).numpy().view(np.uint16)
     return oracle.Oracle(master0.cpu().numpy().astype(np.float32), p0, param_dtype=wl.param_dtype,
                          grad_dtype=wl.grad_dtype, scaler_enabled=wl.scaler_enabled,
-                         init_scale=wl.init_scale, interval=wl.interval, numel=wl.numel)
+                         init_scale=wl.init_scale, interval=wl.interval, min_scale=wl.min_scale,
+                         max_scale=wl.max_scale, numel=wl.numel)
 
 
 def grad_bits(g):
@@ -260,3 +262,83 @@ def run_parity(wl: W.Workload, gaps=False, device="cuda", steps=None, compare_ev
             entry["state"] = compare_state(gpu.pull(), orc, wl, f"{wl.name} step {step}")
         log.append(entry)
     return gpu, orc, log
+
+
+# ---------------------------------------------------------------------------
+# the oracle over very long lists: element-wise oracle functions called on disjoint
+# contiguous slices from several threads (ctypes releases the GIL during a foreign
+# call).  Each element still goes through the oracle's own arithmetic; nothing here
+# adds, reorders or fuses an operation.  Sums keep the oracle's sequential order.
+# ---------------------------------------------------------------------------
+
+def host_threads() -> int:
+    import os
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _slices(P: int, parts: int):
+    step = (P + parts - 1) // parts
+    return [(lo, min(P, lo + step)) for lo in range(0, P, max(step, 1))]
+
+
+def parallel_slices(fn, P: int, threads: int = 0):
+    """Run fn(lo, hi) over disjoint contiguous slices of [0, P) on host threads; returns
+    the per-slice results in slice order."""
+    from concurrent.futures import ThreadPoolExecutor
+    threads = threads or host_threads()
+    sl = _slices(P, threads)
+    if len(sl) <= 1:
+        return [fn(lo, hi) for lo, hi in sl]
+    with ThreadPoolExecutor(threads) as ex:
+        return list(ex.map(lambda s: fn(*s), sl))
+
+
+def oracle_accumulate_par(lib, acc, vals, dt: int, w: float, first: bool):
+    """The oracle's accumulate (acc = w*g, or fma(w, g, acc)) over a long flat list."""
+    import ctypes
+    es = vals.dtype.itemsize
+    a0, g0 = acc.ctypes.data, vals.ctypes.data
+    parallel_slices(lambda lo, hi: lib.tlo_accumulate(ctypes.c_void_p(a0 + 4 * lo), ctypes.c_void_p(g0 + es * lo),
+                                                      dt, hi - lo, w, 1 if first else 0), acc.size)
+
+
+def oracle_unscale_par(lib, acc, S: float) -> int:
+    """The oracle's unscale and finite check over a long flat list (the flag is the OR of
+    the slices' flags)."""
+    import ctypes
+    a0 = acc.ctypes.data
+    return int(any(parallel_slices(lambda lo, hi: lib.tlo_unscale_check(ctypes.c_void_p(a0 + 4 * lo), hi - lo, S),
+                                   acc.size)))
+
+
+def oracle_dequant_par(codes, scales, numel):
+    """The oracle's 8-bit dequantization of a whole tensor list, tensor ranges on threads
+    (each range's codes and block scales are contiguous in tensor order)."""
+    import ctypes
+    import oracle
+    lib = oracle.load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    n = np.ascontiguousarray(numel, dtype=np.int64)
+    out = np.empty(codes.size, dtype=np.float32)
+    ce = np.concatenate([[0], np.cumsum(n)])
+    se = np.concatenate([[0], np.cumsum((n + 15) // 16)])
+    # tensor ranges of about equal element counts
+    parts = host_threads()
+    bounds = sorted(set([0, n.size] + [int(np.searchsorted(ce, ce[-1] * i / parts)) for i in range(1, parts)]))
+
+    def one(i):
+        t0, t1 = bounds[i], bounds[i + 1]
+        if t1 <= t0:
+            return
+        lst = oracle.E4M3List(codes.ctypes.data + int(ce[t0]), scales.ctypes.data + 4 * int(se[t0]),
+                              n.ctypes.data + 8 * t0, t1 - t0)
+        lib.tlo_dequant_e4m3b16(ctypes.byref(lst), ctypes.c_void_p(out.ctypes.data + 4 * int(ce[t0])))
+
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(parts) as ex:
+        list(ex.map(one, range(len(bounds) - 1)))
+    return out

@@ -68,6 +68,55 @@ def test_llama_10m():
 
 
 # ---------------------------------------------------------------------------
+# hyper-parameters, clipping off, and the loss scale's floor and cap
+# ---------------------------------------------------------------------------
+
+# A second common setting (betas 0.9 / 0.999, eps 1e-6, no weight decay) and an
+# exaggerated one (small betas, a large eps and decay), so that a slip in the bias
+# corrections, the eps placement or the decay shows at the parity tolerances.
+HP_SETS = {
+    "adam_0999": dict(lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-6, weight_decay=0.0),
+    "exaggerated": dict(lr=1e-3, beta1=0.7, beta2=0.8, eps=3e-3, weight_decay=0.9),
+}
+
+
+@pytest.mark.parametrize("hp", list(HP_SETS), ids=list(HP_SETS))
+@pytest.mark.parametrize("resident", [False, True, "remat"], ids=["per_microbatch", "resident", "remat"])
+def test_hyper_parameter_sets(hp, resident):
+    """The kernels' AdamW constants and element update under two more hyper-parameter sets,
+    6 updates from zero moments, ragged misaligned tensors, clip active."""
+    wl = custom([5000, 300, 20000, 17, 2 * 16384 + 5, 1], k=3, steps=6, counts=[3, 4, 2], grad_std=3e-2)
+    _, _, log = run_parity(wl, gaps=True, hp=HP_SETS[hp], resident=resident)
+    assert all(e["norm_oracle"] > 1.0 for e in log)
+
+
+@pytest.mark.parametrize("resident", [False, True, "remat"], ids=["per_microbatch", "resident", "remat"])
+def test_clip_disabled(resident):
+    """max_norm = 0 disables clipping ([MEG] section 9 clip, read as off for max_norm <= 0):
+    coefficient 1 although the norm (about 1.65) is above 1."""
+    gpu, orc, log = run_parity(W.make("bf16_small"), max_norm=0.0, resident=resident)
+    st = gpu.status()
+    assert st.coef == 1.0 and all(e["norm_oracle"] > 1.0 for e in log)
+
+
+def test_scaler_floor_and_cap():
+    """[MEG] section 5: the scale never backs off below min_loss_scale, and (reading R2) never
+    grows past max_scale.  fp16, S0 = 2^16, growth every 2 clean updates, cap 2^17, floor
+    2^14; updates 5-9 overflow.  S after each update, derived by hand from the rules:
+    2^16, 2^17 (grown), 2^17, 2^17 (capped), 2^16, 2^15, 2^14, 2^14 (floored), 2^14,
+    2^14, 2^15, 2^15; the GPU and the oracle agree on every one."""
+    inj = {(s, 0): [(1234 + s, 0x7C00)] for s in range(5, 10)}
+    wl = W.Workload("floor_cap", [5000, 300, 20000], "f16", "f16", steps=12, k=1, grad_std=1e-4,
+                    scaler_enabled=True, init_scale=2.0 ** 16, interval=2, min_scale=2.0 ** 14,
+                    max_scale=2.0 ** 17, fixed_counts=[64], grads_prescaled=True, injections=inj)
+    gpu, orc, log = run_parity(wl, gaps=True, compare_every=3)
+    expect = [16, 17, 17, 17, 16, 15, 14, 14, 14, 14, 15, 15]
+    assert [e["S"] for e in log] == [2.0 ** x for x in expect]
+    assert [e["skipped"] for e in log] == [0] * 4 + [1] * 5 + [0] * 3
+    assert gpu.status().t == 7
+
+
+# ---------------------------------------------------------------------------
 # ragged, misaligned, empty and degenerate lists
 # ---------------------------------------------------------------------------
 
@@ -452,72 +501,85 @@ def test_ragged_100k_full(layout, resident):
 @pytest.mark.parametrize("name,resident", [("llama_1b", True), ("llama_1b", False), ("llama_1b_fp8", True)],
                          ids=["bf16-resident", "bf16-per_microbatch", "e4m3b16-resident"])
 def test_llama_1b_full_size_sampled(name, resident):
-    """The ~1.24B-parameter list at full size, k=8, through the call sequence the
-    benchmark times (resident: the headline), the per-micro-batch sequence, and the
-    resident sequence over 8-bit block-scaled gradients.  The norm is checked against
-    the oracle's sum over every element; 200,000 sampled elements of master, m, v and
-    params are computed one by one through the oracle's functions."""
+    """The ~1.24B-parameter list at full size, k=8, over the workload's 5 updates, through
+    the call sequence the benchmark times (resident: the headline), the per-micro-batch
+    sequence, and the resident sequence over 8-bit block-scaled gradients.  Every update:
+    the norm against the oracle's sum over every element (the oracle's accumulate and
+    unscale run on slices of the list on the host threads, its sum in order), and
+    200,000 sampled elements of master, m, v and params advanced one by one through the
+    oracle's functions with that update's global clip coefficient, so updates 2-5 read
+    non-zero moments back."""
     import oracle
+    from harness import oracle_accumulate_par, oracle_dequant_par, oracle_unscale_par
     wl = W.make(name)
     fp8 = wl.grad_dtype == "e4m3b16"
     master0 = W.master_init(wl, "cuda")
     gpu = GpuOptimizer(wl, master0)
-    counts = wl.counts(1)
-    N = sum(counts)
-    grads = [W.grad_input(wl, 1, i, device="cuda") for i in range(wl.k)]
     rng = np.random.default_rng(123)
     idx = np.unique(rng.integers(0, wl.P, 200_000))
     idx_t = torch.from_numpy(idx).cuda()
-    w0 = master0[idx_t].cpu().numpy()
-    gpu.step(grads, counts, resident=resident)
-    st = gpu.status()
+    n = idx.size
     lib = oracle.load()
 
     def P_(a):
         return a.ctypes.data_as(ctypes.c_void_p)
 
-    weights = [lib.tlo_microbatch_weight(n, N) for n in counts]
-    # the oracle's u over every element, one list at a time (host memory), keeping
-    # each list's sampled inputs for the element-wise check below
-    acc = np.empty(wl.P, np.float32)
-    samples = []
-    for i, g in enumerate(grads):
-        if fp8:
-            vals = oracle.dequant_e4m3b16(g[0].cpu().numpy(), g[1].cpu().numpy(), wl.numel)
-            dt = oracle.DT_F32
-        else:
-            vals = np.ascontiguousarray(grad_bits(g))
-            dt = oracle.DT_BF16
-        lib.tlo_accumulate(P_(acc), P_(vals), dt, wl.P, weights[i], 1 if i == 0 else 0)
-        samples.append((np.ascontiguousarray(vals[idx]), dt))
-        del vals
-    found = lib.tlo_unscale_check(P_(acc), wl.P, 1.0)
-    sumsq = lib.tlo_sumsq(P_(acc), wl.P)
-    del acc
-    assert found == 0 and st.found_inf == 0 and st.skipped == 0
-    norm = lib.tlo_norm_from_sumsq(sumsq)
-    assert abs(st.norm - norm) <= 1e-6 * norm, (st.norm, norm)
-    coef = lib.tlo_clip_coef(norm, wl.max_norm)
-    # sampled elements, one by one, through the oracle's functions in the step's order
-    n = idx.size
-    acc = np.empty(n, np.float32)
-    for i, (vals, dt) in enumerate(samples):
-        lib.tlo_accumulate(P_(acc), P_(vals), dt, n, weights[i], 1 if i == 0 else 0)
-    lib.tlo_unscale_check(P_(acc), n, 1.0)
-    hp = oracle.AdamWHP(**{k: v for k, v in W.HP.items()})
-    sc = lib.tlo_adamw_prepare(ctypes.byref(hp), float(np.float32(0.9)), float(np.float32(0.95)))
-    w = w0.astype(np.float32).copy()
+    # the sampled state, advanced by the oracle's functions
+    w = master0[idx_t].cpu().numpy().astype(np.float32).copy()
     m = np.zeros(n, np.float32)
     v = np.zeros(n, np.float32)
     p = np.empty(n, np.uint16)
-    lib.tlo_adamw_recast(P_(w), P_(m), P_(v), P_(p), oracle.DT_BF16, P_(acc), n, coef, ctypes.byref(sc))
-    L = gpu.lists
-    assert_ulps32(L["master"].flat()[idx_t].cpu().numpy(), w, 2, f"{name} master")
-    assert_ulps32(L["m"].flat()[idx_t].cpu().numpy(), m, 2, f"{name} m")
-    assert_ulps32(L["v"].flat()[idx_t].cpu().numpy(), v, 2, f"{name} v")
-    gp = L["param"].flat()[idx_t].cpu().view(torch.int16).numpy().view(np.uint16)
-    assert_ulps16(gp, p, 1, f"{name} param")
-    assert st.t == 1
+    state = oracle.State(1.0, 0, 0, 1.0, 1.0)
+    scfg = oracle.ScalerCfg(0, 2.0, 0.5, 2000, 1.0, 2.0 ** 127)
+    hp = oracle.AdamWHP(**{k: v_ for k, v_ in W.HP.items()})
+    acc = np.empty(wl.P, np.float32)
+    del master0
+    for step in range(1, wl.steps + 1):
+        counts = wl.counts(step)
+        N = sum(counts)
+        grads = [W.grad_input(wl, step, i, device="cuda") for i in range(wl.k)]
+        gpu.step(grads, counts, resident=resident)
+        st = gpu.status()
+        weights = [lib.tlo_microbatch_weight(c, N) for c in counts]
+        # the oracle's u over every element, one list at a time (host memory), keeping
+        # each list's sampled inputs for the element-wise check below
+        samples = []
+        for i, g in enumerate(grads):
+            if fp8:
+                vals = oracle_dequant_par(g[0].cpu().numpy(), g[1].cpu().numpy(), wl.numel)
+                dt = oracle.DT_F32
+            else:
+                vals = np.ascontiguousarray(grad_bits(g))
+                dt = oracle.DT_BF16
+            oracle_accumulate_par(lib, acc, vals, dt, weights[i], i == 0)
+            samples.append((np.ascontiguousarray(vals[idx]), dt))
+            del vals
+        del grads
+        found = oracle_unscale_par(lib, acc, 1.0)
+        sumsq = lib.tlo_sumsq(P_(acc), wl.P)
+        assert found == 0 and st.found_inf == 0 and st.skipped == 0
+        norm = lib.tlo_norm_from_sumsq(sumsq)
+        assert abs(st.norm - norm) <= 1e-6 * norm, (step, st.norm, norm)
+        coef = lib.tlo_clip_coef(norm, wl.max_norm)
+        # sampled elements, one by one, through the oracle's functions in the step's order
+        u = np.empty(n, np.float32)
+        for i, (vals, dt) in enumerate(samples):
+            lib.tlo_accumulate(P_(u), P_(vals), dt, n, weights[i], 1 if i == 0 else 0)
+        lib.tlo_unscale_check(P_(u), n, 1.0)
+        b1n = state.b1p * float(np.float32(hp.beta1))
+        b2n = state.b2p * float(np.float32(hp.beta2))
+        sc = lib.tlo_adamw_prepare(ctypes.byref(hp), b1n, b2n)
+        lib.tlo_adamw_recast(P_(w), P_(m), P_(v), P_(p), oracle.DT_BF16, P_(u), n, coef, ctypes.byref(sc))
+        lib.tlo_scaler_update(ctypes.byref(state), ctypes.byref(scfg), 0, b1n, b2n)
+        L = gpu.lists
+        what = f"{name} update {step}"
+        assert_ulps32(L["master"].flat()[idx_t].cpu().numpy(), w, 2, f"{what} master")
+        assert_ulps32(L["m"].flat()[idx_t].cpu().numpy(), m, 2, f"{what} m")
+        assert_ulps32(L["v"].flat()[idx_t].cpu().numpy(), v, 2, f"{what} v")
+        gp = L["param"].flat()[idx_t].cpu().view(torch.int16).numpy().view(np.uint16)
+        assert_ulps16(gp, p, 1, f"{what} param")
+        assert st.t == state.t == step and st.b1p == state.b1p and st.b2p == state.b2p
+    assert gpu.status().t == 5
 
 
 def test_failed_launch_abandons_the_update(monkeypatch):
