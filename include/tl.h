@@ -144,7 +144,7 @@ typedef struct {
     int32_t count;      /* good steps since the last overflow or growth */
     int64_t t;          /* committed optimizer steps */
     int32_t skipped;    /* 1 if the last finished update was skipped */
-    int32_t found_inf;  /* overflow flag of the update in flight (0 after tl_scaler_update) */
+    int32_t found_inf;  /* overflow flag of the update in flight (0 once its AdamW launch has run) */
     float norm;         /* global L2 norm of the last update's unscaled gradient */
     float coef;         /* clip coefficient applied by the last update (<= 1) */
     double sumsq;       /* squared norm in fp64 */
@@ -238,8 +238,56 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
  * coefficient is applied only when below 1 (eps = 1e-6); max_norm <= 0
  * disables clipping (coef = 1, the norm is still computed).  The partials
  * are reduced in a fixed order, so the norm is deterministic.  A non-finite
- * squared norm raises the overflow flag.  Errors: TL_ESTATE. */
+ * squared norm raises the overflow flag.  Where the device work happens: for
+ * a context of at most 4,096 chunks the pass of tl_unscale_check (or of the
+ * last tl_accumulate_many, or tl_unscale_check_many) reduces the norm in its
+ * last CTA and this call launches nothing; longer tables get a second-stage
+ * launch here.  Either way the AdamW launch derives the coefficient from the
+ * device norm and this max_norm.  Errors: TL_ESTATE. */
 int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream);
+
+/* The sharded form of a4, for an update whose tensor list is split over
+ * several contexts (one per rank of a sharded optimizer, each owning a slice of
+ * the parameters, see tl_partition).  "Megatron Internals III", section 6
+ * "Overflow must be global": all ranks of one logical update take the same
+ * step-or-skip decision (the flag is all-reduced with max); section 9 and
+ * [ZRO] "Operational sharp edges", "Gradient clipping": each rank sums the
+ * squares of its own slice, those scalars are all-reduced (sum) before the
+ * square root is taken, and every rank clips with the same coefficient.
+ * tl_local_sumsq (in place of tl_grad_norm, after the pass) writes this
+ * context's squared norm (fp64) and overflow flag (0 or 1) into caller device
+ * memory on the stream, without any host synchronisation.  The caller
+ * combines them across ranks (e.g. an all-reduce: sum of the squared norms,
+ * max of the flags) into device memory, and tl_grad_norm_from takes the
+ * combined values as the update's: sumsq, norm = sqrt(sumsq), the flag raised
+ * if the combined flag is set or the sum is not finite, and the clip
+ * coefficient from max_norm.  tl_clip_adamw_step and tl_scaler_update follow
+ * as usual, so every rank skips or steps together and moves S identically.
+ *   d_sumsq: one double, 8-byte aligned; d_flag: one int32, 4-byte aligned
+ *   (device memory, owned by the caller).
+ * Errors: TL_EINVAL (pointers, max_norm NaN), TL_ESTATE (out of order). */
+int tl_local_sumsq(tl_ctx* ctx, double* d_sumsq, int32_t* d_flag, tl_stream stream);
+int tl_grad_norm_from(tl_ctx* ctx, const double* d_sumsq, const int32_t* d_flag, float max_norm,
+                      tl_stream stream);
+
+/* The slice of a tensor list that rank `rank` of nranks owns in a sharded
+ * optimizer ([ZRO] "The scheme": partition the parameter vector into N
+ * disjoint slices, slice i on device i; "Partition granularity": slicing the
+ * flat vector splits tensors across owners).  The list is flattened in tensor
+ * order, then element order (P elements); the cuts are b_j = the largest
+ * multiple of align not above floor(j * P / nranks) for j = 0 .. nranks - 1,
+ * and b_nranks = P.  Rank r owns [b_r, b_(r+1)), returned as pieces in tensor
+ * order: piece q is elements [start[q], start[q] + len[q]) of tensor
+ * tensor[q]; empty pieces are left out, so *count <= ntensors.  A context over
+ * a rank's pieces takes each state tensor's address plus start (and the same
+ * for the gradients).  align (>= 1) keeps the cuts on multiples of align
+ * elements (16 keeps 8-bit gradient blocks whole inside a tensor that starts
+ * on a block).  Host only: no CUDA call.  *count is always written; the pieces
+ * are written only when cap >= *count.
+ * Errors: TL_EINVAL (sizes, nranks < 1, rank outside [0, nranks), align < 1,
+ * cap too small, NULL arrays). */
+int tl_partition(int64_t ntensors, const int64_t* numel, int32_t nranks, int32_t rank, int64_t align,
+                 int64_t* tensor, int64_t* start, int64_t* len, int64_t cap, int64_t* count);
 
 /* Clip + AdamW on the fp32 masters + recast to the model dtype (a5).
  * [MEG] sections 7 and 9 (clip with the global coefficient, step the fp32
@@ -286,11 +334,17 @@ int tl_set_lr_schedule(tl_ctx* ctx, const float* lr_table, int64_t len);
  * Overflow: S = max(S*backoff, min_scale), count = 0, t and the beta powers
  * unchanged, skipped = 1.  Clean: t += 1, beta powers advanced, count += 1,
  * and when count reaches interval S = min(S*growth, max_scale), count = 0.
- * Clears the overflow flag and closes the update.  Errors: TL_ESTATE. */
+ * The overflow flag is cleared.  The device work runs in the last CTA of the
+ * AdamW launch of tl_clip_adamw_step (after every CTA has read S and the
+ * flag), so a status read after tl_clip_adamw_step already shows it; this
+ * call closes the update on the host and launches nothing.
+ * Errors: TL_ESTATE. */
 int tl_scaler_update(tl_ctx* ctx, tl_stream stream);
 
 /* Synchronous reads and writes of the device scalars (these wait for the
- * stream).  tl_set_state is allowed only between updates and checks S
+ * stream).  tl_read_status between tl_grad_norm and tl_clip_adamw_step first
+ * computes the clip coefficient of the update in flight on the device.
+ * tl_set_state is allowed only between updates and checks S
  * (power of two within [min_scale, max_scale], or 1 when disabled), count
  * (0 <= count < interval) and t >= 0 ([MP] section 4 catalogue: a resume
  * keeps S and the count; bad arguments raise).  Errors: TL_EINVAL,

@@ -33,7 +33,8 @@ EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "t
             "tl_unscale_check", "tl_grad_norm",
             "tl_clip_adamw_step", "tl_scaler_update", "tl_read_status", "tl_get_state", "tl_set_state",
             "tl_scale_ptr", "tl_num_params", "tl_num_chunks", "tl_launch_count", "tl_status_string",
-            "tl_last_error", "tl_unscale_norm_noalloc", "tl_loss_seed", "tl_set_lr_schedule")
+            "tl_last_error", "tl_unscale_norm_noalloc", "tl_loss_seed", "tl_set_lr_schedule",
+            "tl_local_sumsq", "tl_grad_norm_from", "tl_partition")
 
 
 class TLError(RuntimeError):
@@ -127,6 +128,11 @@ def load_library():
         "tl_unscale_norm_noalloc": (i32, [i64, ctypes.POINTER(i64), pp, f32, f32, vp, vp]),
         "tl_loss_seed": (i32, [vp, i64, i64, vp, vp]),
         "tl_set_lr_schedule": (i32, [vp, vp, i64]),
+        "tl_local_sumsq": (i32, [vp, vp, vp, vp]),
+        "tl_grad_norm_from": (i32, [vp, vp, vp, f32, vp]),
+        "tl_partition": (i32, [i64, ctypes.POINTER(i64), ctypes.c_int32, ctypes.c_int32, i64,
+                               ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64), i64,
+                               ctypes.POINTER(i64)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -311,6 +317,36 @@ def tl_set_lr_schedule(ctx: Context, table) -> None:
     _check(ctx, "tl_set_lr_schedule", load_library().tl_set_lr_schedule(
         ctx.handle, ctypes.c_void_p(table.data_ptr()), int(table.numel())))
     ctx.lr_table = table
+
+
+def tl_local_sumsq(ctx: Context, sumsq_addr: int, flag_addr: int, stream=None) -> None:
+    """Write this context's squared norm (fp64) and overflow flag (int32) to the device
+    addresses on the stream (the sharded form of tl_grad_norm, first half)."""
+    _check(ctx, "tl_local_sumsq", load_library().tl_local_sumsq(ctx.handle, ctypes.c_void_p(int(sumsq_addr)),
+                                                                ctypes.c_void_p(int(flag_addr)), _stream(stream)))
+
+
+def tl_grad_norm_from(ctx: Context, sumsq_addr: int, flag_addr: int, max_norm: float, stream=None) -> None:
+    """Take the squared norm and flag combined across shards (device addresses) as the
+    update's norm and overflow decision."""
+    _check(ctx, "tl_grad_norm_from", load_library().tl_grad_norm_from(
+        ctx.handle, ctypes.c_void_p(int(sumsq_addr)), ctypes.c_void_p(int(flag_addr)), float(max_norm),
+        _stream(stream)))
+
+
+def tl_partition(numel: Sequence[int], nranks: int, rank: int, align: int = 1):
+    """The pieces (tensor index, first element, length) of the slice rank `rank` of
+    `nranks` owns (host only)."""
+    lib = load_library()
+    n = len(numel)
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numel])
+    cap = max(n, 1)
+    t, s, l = (ctypes.c_int64 * cap)(), (ctypes.c_int64 * cap)(), (ctypes.c_int64 * cap)()
+    cnt = ctypes.c_int64()
+    rc = lib.tl_partition(n, arr, int(nranks), int(rank), int(align), t, s, l, cap, ctypes.byref(cnt))
+    if rc != TL_OK:
+        raise TLError("tl_partition", rc, lib.tl_status_string(rc).decode())
+    return [(int(t[q]), int(s[q]), int(l[q])) for q in range(cnt.value)]
 
 
 def tl_num_params(ctx: Context) -> int:

@@ -22,7 +22,27 @@ using namespace tl;
 
 namespace {
 
-enum Phase { kIdle = 0, kAccum = 1, kUnscaled = 2, kNormed = 3, kStepped = 4 };
+enum Phase { kIdle = 0, kAccum = 1, kUnscaled = 2, kNormed = 3, kStepped = 4, kLocal = 5 };
+
+// Segment length: the longest power of two in [kMinSeg, kChunk] that still gives the
+// whole-CTA part at least kSegPerSm segments per SM, so that a persistent grid of a
+// few CTAs per SM gets several rounds of similar segments (a list of ~10M elements
+// in 16,384-element segments would give barely two rounds, and its last round would
+// run on a fraction of the grid).  Long lists keep kChunk.
+#ifndef TL_SEG_MIN
+#define TL_SEG_MIN 4096
+#endif
+#ifndef TL_SEG_PER_SM
+#define TL_SEG_PER_SM 24
+#endif
+constexpr int64_t kMinSeg = TL_SEG_MIN;
+constexpr int64_t kSegPerSm = TL_SEG_PER_SM;
+// Small tensors are grouped one per warp (a part of the table with its own launch)
+// only when the list holds at least this many of them; fewer small tensors become
+// whole-CTA segments of their own, so the pass is one launch.  The environment
+// variable TL_SMALL_GROUP_MIN, read by tl_create, overrides it (tests set 1 to run
+// the group kernels on short lists).
+constexpr int64_t kGroupMin = 128;
 
 int elem_size(int dt) { return dt == TL_F32 ? 4 : dt == TL_E4M3B16 ? 1 : 2; }
 
@@ -85,6 +105,11 @@ struct tl_ctx {
     GradSlot slots[kGradSlots];
     uint64_t clock = 0;
     int64_t nbig = 0;              // chunks [0, nbig) are whole-CTA segments, [nbig, nchunks) small-tensor groups
+    int64_t seg = kChunk;          // segment length of this list (a power of two <= kChunk)
+    // the partial-writing pass finishes the norm in its last CTA (few partial slots);
+    // else tl_grad_norm launches the 128-CTA second stage
+    bool fuse_norm = false;
+    float max_norm = 0.0f;         // clip threshold of the update in flight (set by tl_grad_norm / _from)
     // persistent grid sizes per kernel variant, [..][0] for the whole-CTA part, [..][1] for the groups
     int grid_acc[kGradTypes][2][2] = {};
     int grid_uns[kGradTypes][3][2] = {};
@@ -287,22 +312,30 @@ cudaError_t gate(tl_ctx* ctx) {
 }
 
 // Launch one streaming operation over the chunk table: the whole-CTA part and
-// the small-tensor groups are separate launches (launch(small, c0, c1)).
+// the small-tensor groups are separate launches (launch(small, c0, c1, last), last
+// true for the final launch of the operation).
 template <typename Launch>
 cudaError_t over_parts(tl_ctx* ctx, Launch launch) {
+    const bool groups = ctx->nchunks > ctx->nbig;
     if (ctx->nbig > 0) {
         cudaError_t e = gate(ctx);
-        if (e == cudaSuccess) e = launch(false, int64_t(0), ctx->nbig);
+        if (e == cudaSuccess) e = launch(false, int64_t(0), ctx->nbig, !groups);
         if (e != cudaSuccess) return e;
         ctx->launches += 1;
     }
-    if (ctx->nchunks > ctx->nbig) {
+    if (groups) {
         cudaError_t e = gate(ctx);
-        if (e == cudaSuccess) e = launch(true, ctx->nbig, ctx->nchunks);
+        if (e == cudaSuccess) e = launch(true, ctx->nbig, ctx->nchunks, true);
         if (e != cudaSuccess) return e;
         ctx->launches += 1;
     }
     return cudaSuccess;
+}
+
+// Partial slots the last launch of a partial-writing pass reduces itself (0: the
+// norm is left to the second-stage launch of tl_grad_norm).
+int64_t fin_slots(const tl_ctx* ctx, bool last) {
+    return ctx->fuse_norm && last ? ctx->nchunks * kGroup : 0;
 }
 
 // Resolve (and validate) k gradient lists (list-major, ntensors pointers each)
@@ -420,16 +453,31 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     if (const char* f = std::getenv("TL_TEST_FAIL_LAUNCH")) ctx->fail_at = std::atoll(f);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
-    // Segments and chunks.  A large tensor becomes one chunk
-    // per kChunk elements; small tensors (<= kSmall elements) are grouped kGroup
-    // to a chunk, one per warp.  Chunks are then ordered by work, largest first
+    // Segments and chunks.  A large tensor becomes one chunk per `seg` elements;
+    // small tensors (<= kSmall elements) are grouped kGroup to a chunk, one per warp,
+    // when there are many of them.  Chunks are then ordered by work, largest first
     // (stable), so every round of the persistent grid gets chunks of similar size.
+    int64_t group_min = kGroupMin;
+    if (const char* g = std::getenv("TL_SMALL_GROUP_MIN")) group_min = std::max<int64_t>(1, std::atoll(g));
+    int64_t n_small = 0, small_elems = 0;
+    for (int64_t i = 0; i < ntensors; ++i)
+        if (numel[i] > 0 && numel[i] <= kSmall) { ++n_small; small_elems += numel[i]; }
+    const bool grouping = n_small >= group_min;
+    {
+        const int64_t whole = P - (grouping ? small_elems : 0);
+        int64_t seg = kChunk;
+        while (seg > kMinSeg && whole / seg < kSegPerSm * ctx->sm_count) seg /= 2;
+        ctx->seg = seg;
+    }
+    const int64_t seg_len = ctx->seg;
     struct ChunkBuild {
         std::vector<Chunk> segs;
         int64_t work = 0;
+        bool group = false;
     };
     std::vector<ChunkBuild> built;
     ChunkBuild group;
+    group.group = true;
     // the descriptor of elements [st, st + len) of tensor i, with its state addresses
     auto seg = [&](int64_t i, int64_t st, int64_t len) {
         return Chunk{acc[i] + st, master[i] + st, m[i] + st, v[i] + st,
@@ -437,18 +485,19 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     };
     for (int64_t i = 0; i < ntensors; ++i) {
         if (numel[i] == 0) continue;
-        if (numel[i] <= kSmall) {
+        if (grouping && numel[i] <= kSmall) {
             group.segs.push_back(seg(i, 0, numel[i]));
             group.work += numel[i];
             if (int(group.segs.size()) == kGroup) {
                 built.push_back(std::move(group));
                 group = ChunkBuild();
+                group.group = true;
             }
             continue;
         }
-        for (int64_t st = 0; st < numel[i]; st += kChunk) {
+        for (int64_t st = 0; st < numel[i]; st += seg_len) {
             ChunkBuild one;
-            const int32_t len = int32_t(std::min<int64_t>(kChunk, numel[i] - st));
+            const int32_t len = int32_t(std::min<int64_t>(seg_len, numel[i] - st));
             one.segs.push_back(seg(i, st, len));
             one.work = len;
             built.push_back(std::move(one));
@@ -457,14 +506,12 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     if (!group.segs.empty()) built.push_back(std::move(group));
     // whole-CTA chunks first, then the groups; each part by work, largest first
     std::stable_sort(built.begin(), built.end(), [](const ChunkBuild& a, const ChunkBuild& b) {
-        const bool ga = a.segs.size() > 1 || a.segs[0].len <= kSmall;
-        const bool gb = b.segs.size() > 1 || b.segs[0].len <= kSmall;
-        if (ga != gb) return gb;
+        if (a.group != b.group) return b.group;
         return a.work > b.work;
     });
     int64_t nbig = 0;
     for (const ChunkBuild& cb : built)
-        if (!(cb.segs.size() > 1 || cb.segs[0].len <= kSmall)) ++nbig;
+        if (!cb.group) ++nbig;
     // whole-CTA chunk c is segment c; every group holds kGroup segments, a short
     // group padded with empty segments (its first tensor, length 0) so that a warp
     // finds its tensor without an index table
@@ -513,9 +560,9 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     ds.norm = 0.0f;
     ds.coef = 1.0f;
     ds.sumsq = 0.0;
-    ds.b1p_next = 1.0;
-    ds.b2p_next = 1.0;
     ds.norm_ticket = 0;
+    ds.pass_ticket = 0;
+    ds.adam_ticket = 0;
     ds.pad = 0;
     e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
     // partial slots not at the start of a run stay zero for good
@@ -530,8 +577,9 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     const int gdt = cfg->grad_dtype, pdt = cfg->param_dtype;
     int64_t big_elems = 0;
     for (int64_t c = 0; c < nbig; ++c) big_elems += chunks[size_t(c)].len;
-    ctx->run[0] = nbig > 0 && big_elems < nbig * (kChunk / 2) ? kRun : 1;
+    ctx->run[0] = nbig > 0 && big_elems < nbig * (seg_len / 2) ? kRun : 1;
     ctx->run[1] = kRun;
+    ctx->fuse_norm = nchunks > 0 && nchunks * kGroup <= kFuseNormSlots;
     for (int part = 0; part < 2; ++part) {
         const bool small = part == 1;
         const int64_t n = small ? nchunks - nbig : nbig;
@@ -583,7 +631,7 @@ int tl_accumulate(tl_ctx* ctx, const void* const* grads, int64_t n_i, int64_t N,
     const float w = static_cast<float>(static_cast<double>(n_i) / static_cast<double>(N));
     if (ctx->nchunks > 0) {
         const int gdt = ctx->cfg.grad_dtype;
-        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool) {
             return launch_accumulate(gdt, first != 0, small, ctx->d_chunks, c0, c1, inl,
                                      dtab, w, ctx->grid_acc[gdt][first][small ? 1 : 0], s);
         });
@@ -632,9 +680,10 @@ int tl_unscale_check(tl_ctx* ctx, const void* const* grads, int64_t n_k, int64_t
     const float w = grads == nullptr ? 1.0f : static_cast<float>(static_cast<double>(n_k) / static_cast<double>(N));
     if (ctx->nchunks > 0) {
         const int gdt = ctx->cfg.grad_dtype;
-        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
             return launch_unscale(gdt, mode, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, dtab, w,
-                                  ctx->d_state, ctx->d_partials, ctx->grid_uns[gdt][mode][small ? 1 : 0], s);
+                                  ctx->d_state, ctx->d_partials, fin_slots(ctx, lastl),
+                                  ctx->grid_uns[gdt][mode][small ? 1 : 0], s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "unscale launch");
         mark_used(used, s);
@@ -691,9 +740,10 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
         if (ctx->nchunks > 0) {
             const int vr = (f ? 1 : 0) | (l ? 2 : 0) | (kk <= kFewLists ? 4 : 0);
             const int gdt = ctx->cfg.grad_dtype;
-            cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+            cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
                 return launch_accum_many(gdt, f, l, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a,
-                                         ctx->d_state, ctx->d_partials, ctx->grid_many[gdt][vr][small ? 1 : 0], s);
+                                         ctx->d_state, ctx->d_partials, fin_slots(ctx, lastl),
+                                         ctx->grid_many[gdt][vr][small ? 1 : 0], s);
             });
             if (e != cudaSuccess) return launch_fail(ctx, e, "many-list accumulate launch");
             for (int i = 0; i < kk; ++i) mark_used(slots[j + i], s);
@@ -735,9 +785,10 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
         fill_many_args(ctx, grads, n, N, 0, k, by_value, tabs, a, inl);
         const int gdt = ctx->cfg.grad_dtype;
         const int few = k <= kFewLists ? 1 : 0;
-        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
+        cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
             return launch_check_many(gdt, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a, ctx->d_state,
-                                     ctx->d_partials, ctx->grid_check[gdt][few][small ? 1 : 0], s);
+                                     ctx->d_partials, fin_slots(ctx, lastl), ctx->grid_check[gdt][few][small ? 1 : 0],
+                                     s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "many-list check launch");
         for (int i = 0; i < k; ++i) mark_used(slots[size_t(i)], s);
@@ -760,12 +811,62 @@ int tl_grad_norm(tl_ctx* ctx, float max_norm, tl_stream stream) {
     if (std::isnan(max_norm)) return fail(ctx, TL_EINVAL, "max_norm is NaN");
     int rc;
     if ((rc = check_device(ctx)) != TL_OK) return rc;
-    cudaError_t e = gate(ctx);
-    if (e == cudaSuccess)
-        e = launch_norm(ctx->d_partials, ctx->nchunks * kGroup, ctx->d_norm_slots, ctx->d_state, max_norm,
-                        static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return launch_fail(ctx, e, "norm launch");
+    // With the norm finished by the pass itself there is nothing to launch: the AdamW
+    // launch derives the clip coefficient from the device norm and max_norm.
+    if (!ctx->fuse_norm) {
+        cudaError_t e = gate(ctx);
+        if (e == cudaSuccess)
+            e = launch_norm(ctx->d_partials, ctx->nchunks * kGroup, ctx->d_norm_slots, ctx->d_state, max_norm,
+                            static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return launch_fail(ctx, e, "norm launch");
+        ctx->launches += 1;
+    }
+    ctx->max_norm = max_norm;
+    ctx->phase = kNormed;
+    return TL_OK;
+}
+
+int tl_local_sumsq(tl_ctx* ctx, double* d_sumsq, int32_t* d_flag, tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
+    if (ctx->phase != kUnscaled) return fail(ctx, TL_ESTATE, "tl_local_sumsq must follow tl_unscale_check");
+    if (d_sumsq == nullptr || (reinterpret_cast<uintptr_t>(d_sumsq) & 7u) != 0 || d_flag == nullptr ||
+        (reinterpret_cast<uintptr_t>(d_flag) & 3u) != 0)
+        return fail(ctx, TL_EINVAL, "d_sumsq (8-byte aligned) and d_flag (4-byte aligned) must be device addresses");
+    int rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (!ctx->fuse_norm) {
+        e = gate(ctx);
+        if (e == cudaSuccess) e = launch_norm(ctx->d_partials, ctx->nchunks * kGroup, ctx->d_norm_slots, ctx->d_state,
+                                              0.0f, s);
+        if (e != cudaSuccess) return launch_fail(ctx, e, "norm launch");
+        ctx->launches += 1;
+    }
+    e = gate(ctx);
+    if (e == cudaSuccess) e = launch_export(ctx->d_state, d_sumsq, d_flag, s);
+    if (e != cudaSuccess) return launch_fail(ctx, e, "export launch");
     ctx->launches += 1;
+    ctx->phase = kLocal;
+    return TL_OK;
+}
+
+int tl_grad_norm_from(tl_ctx* ctx, const double* d_sumsq, const int32_t* d_flag, float max_norm, tl_stream stream) {
+    if (ctx == nullptr) return TL_EINVAL;
+    if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
+    if (ctx->phase != kLocal) return fail(ctx, TL_ESTATE, "tl_grad_norm_from must follow tl_local_sumsq");
+    if (std::isnan(max_norm)) return fail(ctx, TL_EINVAL, "max_norm is NaN");
+    if (d_sumsq == nullptr || (reinterpret_cast<uintptr_t>(d_sumsq) & 7u) != 0 || d_flag == nullptr ||
+        (reinterpret_cast<uintptr_t>(d_flag) & 3u) != 0)
+        return fail(ctx, TL_EINVAL, "d_sumsq (8-byte aligned) and d_flag (4-byte aligned) must be device addresses");
+    int rc;
+    if ((rc = check_device(ctx)) != TL_OK) return rc;
+    cudaError_t e = gate(ctx);
+    if (e == cudaSuccess) e = launch_import(ctx->d_state, d_sumsq, d_flag, max_norm, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return launch_fail(ctx, e, "import launch");
+    ctx->launches += 1;
+    ctx->max_norm = max_norm;
     ctx->phase = kNormed;
     return TL_OK;
 }
@@ -780,15 +881,20 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         return fail(ctx, TL_EINVAL, "AdamW hyper-parameters out of range");
     int rc;
     if ((rc = check_device(ctx)) != TL_OK) return rc;
-    AdamHP h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, ctx->lr_sched, ctx->lr_len};
+    AdamHP h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, ctx->max_norm, ctx->lr_sched, ctx->lr_len};
     const int pdt = ctx->cfg.param_dtype;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the scaler state machine runs in the last CTA of the update's last AdamW launch
+    auto scaler = [&](bool last) {
+        return ScalerParams{ctx->cfg.scaler_enabled, ctx->cfg.growth, ctx->cfg.backoff, ctx->cfg.interval,
+                            ctx->cfg.min_scale, ctx->cfg.max_scale, last ? 1 : 0};
+    };
     cudaError_t e = cudaSuccess;
     if (ctx->nchunks == 0) {
-        // no elements: still one launch, whose first CTA computes the beta powers
-        // the scaler kernel commits
+        // no elements: still one launch, whose CTA computes the beta powers and runs
+        // the scaler
         e = gate(ctx);
-        if (e == cudaSuccess) e = launch_adamw(pdt, false, ctx->d_chunks, 0, 0, ctx->d_state, h, 1, s);
+        if (e == cudaSuccess) e = launch_adamw(pdt, false, ctx->d_chunks, 0, 0, ctx->d_state, h, scaler(true), 1, s);
         if (e == cudaSuccess) ctx->launches += 1;
     } else if (ctx->remat) {
         // u recomputed from the lists the update was checked on (the same device
@@ -802,15 +908,15 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         ManyArgs a;
         fill_many_args(ctx, ctx->remat_grads.data(), ctx->remat_n, ctx->N_update, 0, k, by_value, tabs, a, inl);
         const int gdt = ctx->cfg.grad_dtype;
-        e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_adamw_remat(pdt, gdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h, inl, a,
+        e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
+            return launch_adamw_remat(pdt, gdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h, scaler(lastl), inl, a,
                                       ctx->grid_remat[pdt][gdt][k <= kFewLists ? 1 : 0][small ? 1 : 0], s);
         });
         if (e == cudaSuccess)
             for (int i = 0; i < k; ++i) mark_used(slots[size_t(i)], s);
     } else {
-        e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1) {
-            return launch_adamw(pdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h,
+        e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
+            return launch_adamw(pdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h, scaler(lastl),
                                 ctx->grid_adam[pdt][small ? 1 : 0], s);
         });
     }
@@ -820,17 +926,10 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
 }
 
 int tl_scaler_update(tl_ctx* ctx, tl_stream stream) {
+    (void)stream;  // the state machine ran in the last CTA of the AdamW launch
     if (ctx == nullptr) return TL_EINVAL;
     if (int rc0 = refuse_if_interrupted(ctx)) return rc0;
     if (ctx->phase != kStepped) return fail(ctx, TL_ESTATE, "tl_scaler_update must follow tl_clip_adamw_step");
-    int rc;
-    if ((rc = check_device(ctx)) != TL_OK) return rc;
-    ScalerParams sp{ctx->cfg.scaler_enabled, ctx->cfg.growth, ctx->cfg.backoff, ctx->cfg.interval,
-                    ctx->cfg.min_scale, ctx->cfg.max_scale};
-    cudaError_t e = gate(ctx);
-    if (e == cudaSuccess) e = launch_scaler(ctx->d_state, sp, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return launch_fail(ctx, e, "scaler launch");
-    ctx->launches += 1;
     ctx->phase = kIdle;
     ctx->n_sum = 0;
     ctx->N_update = 0;
@@ -853,6 +952,14 @@ static int read_dev_state(tl_ctx* ctx, DevState* ds, cudaStream_t s) {
 int tl_read_status(tl_ctx* ctx, tl_status* out, tl_stream stream) {
     if (ctx == nullptr || out == nullptr) return TL_EINVAL;
     DevState ds;
+    if (ctx->phase == kNormed) {
+        // the AdamW launch computes the clip coefficient of the update in flight;
+        // a read before it gets the coefficient computed now from the same norm
+        int rc0 = check_device(ctx);
+        if (rc0 != TL_OK) return rc0;
+        cudaError_t e = launch_coef(ctx->d_state, ctx->max_norm, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient launch");
+    }
     int rc = read_dev_state(ctx, &ds, static_cast<cudaStream_t>(stream));
     if (rc != TL_OK) return rc;
     out->S = ds.S;
@@ -957,6 +1064,50 @@ int tl_set_lr_schedule(tl_ctx* ctx, const float* lr_table, int64_t len) {
     }
     ctx->lr_sched = lr_table;
     ctx->lr_len = len;
+    return TL_OK;
+}
+
+int tl_partition(int64_t ntensors, const int64_t* numel, int32_t nranks, int32_t rank, int64_t align,
+                 int64_t* tensor, int64_t* start, int64_t* len, int64_t cap, int64_t* count) {
+    if (count == nullptr || ntensors < 0 || (ntensors > 0 && numel == nullptr)) return TL_EINVAL;
+    *count = 0;
+    if (nranks < 1 || rank < 0 || rank >= nranks || align < 1 || cap < 0) return TL_EINVAL;
+    int64_t P = 0;
+    for (int64_t i = 0; i < ntensors; ++i) {
+        if (numel[i] < 0 || numel[i] > (int64_t(1) << 62) - P) return TL_EINVAL;
+        P += numel[i];
+    }
+    // boundary b_j: the largest multiple of align not above floor(j * P / nranks),
+    // computed without overflow as j * (P / n) + floor(j * (P mod n) / n)
+    auto bound = [&](int64_t j) -> int64_t {
+        if (j >= nranks) return P;
+        const int64_t n = nranks;
+        const int64_t f = j * (P / n) + (j * (P % n)) / n;
+        return f / align * align;
+    };
+    const int64_t lo = bound(rank), hi = bound(int64_t(rank) + 1);
+    // the tensors that intersect [lo, hi), in tensor order
+    int64_t pieces = 0, pos = 0;
+    for (int64_t i = 0; i < ntensors; ++i) {
+        const int64_t a = std::max(lo, pos), b = std::min(hi, pos + numel[i]);
+        if (a < b) ++pieces;
+        pos += numel[i];
+    }
+    *count = pieces;
+    if (pieces > cap) return TL_EINVAL;
+    if (pieces > 0 && (tensor == nullptr || start == nullptr || len == nullptr)) return TL_EINVAL;
+    int64_t k = 0;
+    pos = 0;
+    for (int64_t i = 0; i < ntensors; ++i) {
+        const int64_t a = std::max(lo, pos), b = std::min(hi, pos + numel[i]);
+        if (a < b) {
+            tensor[k] = i;
+            start[k] = a - pos;
+            len[k] = b - a;
+            ++k;
+        }
+        pos += numel[i];
+    }
     return TL_OK;
 }
 

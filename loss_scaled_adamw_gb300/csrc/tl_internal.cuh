@@ -70,9 +70,9 @@ struct DevState {
     float norm;           // global L2 norm of the unscaled gradient
     float coef;           // clip coefficient
     double sumsq;         // squared norm (fp64)
-    double b1p_next;      // beta powers of the update in flight (committed by the scaler kernel)
-    double b2p_next;
     uint32_t norm_ticket; // CTAs of the second-stage reduce that have finished, modulo 2^32
+    uint32_t pass_ticket; // CTAs of a partial-writing launch that finish the norm in its last CTA (reset by it)
+    uint32_t adam_ticket; // CTAs of the AdamW launch that runs the scaler in its last CTA (reset by it)
     uint32_t pad;
 };
 
@@ -105,13 +105,20 @@ struct ScalerParams {
     int32_t interval;
     float min_scale;
     float max_scale;
+    int32_t run;     // 1: this launch runs the scaler state machine in its last CTA
 };
 
 struct AdamHP {
     float lr, beta1, beta2, eps, wd;
+    float max_norm;         // the clip threshold of the update (<= 0: no clip)
     const float* lr_sched;  // device schedule: lr = lr_sched[min(t, lr_len - 1)] when set
     int64_t lr_len;
 };
+
+// Partial-writing launches whose context has at most this many squared-norm
+// partial slots finish the norm in their last CTA (no separate reduce launch);
+// longer tables keep the 128-CTA second stage, which reads them faster.
+constexpr int64_t kFuseNormSlots = 32768;
 
 // What the a3 kernel reads besides the accumulation buffer.
 enum UnscaleMode : int {
@@ -129,26 +136,38 @@ enum UnscaleMode : int {
 cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, int64_t c0,
                               int64_t c1, const GradTable& inl, const void* const* gtab, float w,
                               int grid, cudaStream_t s);
+// fin > 0: this launch is the last of its pass and its last CTA reduces the fin
+// partial slots of the whole table into the norm (sumsq, norm, overflow on a
+// non-finite sum); fin = 0: a separate launch_norm does that.
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
                            int64_t c1, int run, const GradTable& inl, const void* const* gtab, float w,
-                           DevState* st, double* partials, int grid, cudaStream_t s);
+                           DevState* st, double* partials, int64_t fin, int grid, cudaStream_t s);
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
                               int64_t c0, int64_t c1, int run, const GradTableMany& inl,
-                              const ManyArgs& a, DevState* st, double* partials, int grid, cudaStream_t s);
+                              const ManyArgs& a, DevState* st, double* partials, int64_t fin, int grid,
+                              cudaStream_t s);
 // The many-list pass without the store of u (all lists of the update at once),
 // and the AdamW pass that recomputes u from the same lists.
 cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1, int run,
-                              const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
-                              cudaStream_t s);
+                              const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
+                              int64_t fin, int grid, cudaStream_t s);
+// The AdamW launches compute the clip coefficient from the device norm and
+// hp.max_norm; with sp.run = 1 the launch's last CTA also runs the scaler state
+// machine (the last AdamW launch of an update).
 cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, int64_t c0,
-                               int64_t c1, DevState* st, AdamHP hp, const GradTableMany& inl, const ManyArgs& a,
-                               int grid, cudaStream_t s);
+                               int64_t c1, DevState* st, AdamHP hp, ScalerParams sp, const GradTableMany& inl,
+                               const ManyArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevState* st, float max_norm,
                         cudaStream_t s);
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
-                         DevState* st, AdamHP hp, int grid, cudaStream_t s);
-cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s);
+                         DevState* st, AdamHP hp, ScalerParams sp, int grid, cudaStream_t s);
 cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s);
+// One thread each: the clip coefficient from the device norm; the local squared norm
+// and overflow flag copied out to caller memory; a global squared norm and flag
+// (combined across shards by the caller) taken in as the update's norm.
+cudaError_t launch_coef(DevState* st, float max_norm, cudaStream_t s);
+cudaError_t launch_export(const DevState* st, double* sumsq, int32_t* flag, cudaStream_t s);
+cudaError_t launch_import(DevState* st, const double* sumsq, const int32_t* flag, float max_norm, cudaStream_t s);
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0

@@ -627,6 +627,57 @@ __device__ __forceinline__ void finish_warp(const SumSq& sq, bool bad, int64_t c
     }
 }
 
+// The end of a partial-writing launch that finishes the norm itself (fin > 0 slots):
+// every CTA, when its chunks are done, publishes its partials and overflow flags
+// (a fence per warp) and takes a ticket; the CTA holding the launch's last ticket
+// then reduces every partial slot of the table (those of earlier launches of the
+// pass included: they completed before this launch began) in a fixed order: thread
+// t sums the contiguous slots [t*per, (t+1)*per) with four interleaved
+// accumulators, then the fixed block reduction.  The order depends on the number of
+// slots only, not on the grid.  Nothing waits: the last CTA only runs once every
+// other CTA has published.  The ticket counter is reset by the last CTA.
+__device__ __noinline__ void finish_pass(DevState* __restrict__ st, const double* __restrict__ partials,
+                                         int64_t nslots) {
+    __shared__ double red[kThreads / 32];
+    __shared__ int last;
+    if ((threadIdx.x & 31) == 0) __threadfence();   // this warp's partials and flag, device-wide
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t ticket = atomicAdd(&st->pass_ticket, 1u);
+        last = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const int64_t per = (nslots + kThreads - 1) / kThreads;
+    const int64_t lo = min(nslots, per * threadIdx.x);
+    const int64_t hi = min(nslots, lo + per);
+    double a4[4] = {0.0, 0.0, 0.0, 0.0};
+    int64_t i = lo;
+    for (; i + 3 < hi; i += 4) {
+        double x[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[q] = __ldcg(partials + i + q);   // written by other SMs
+#pragma unroll
+        for (int q = 0; q < 4; ++q) a4[q] = __dadd_rn(a4[q], x[q]);
+    }
+    double s = __dadd_rn(__dadd_rn(a4[0], a4[1]), __dadd_rn(a4[2], a4[3]));
+    for (; i < hi; ++i) s = __dadd_rn(s, __ldcg(partials + i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double v = 0.0;
+#pragma unroll
+        for (int k = 0; k < kThreads / 32; ++k) v = __dadd_rn(v, red[k]);
+        st->pass_ticket = 0;
+        st->sumsq = v;
+        if (!isfinite(v)) st->found_inf = 1;   // an fp32 square overflowed: treated as an overflow
+        st->norm = __double2float_rn(__dsqrt_rn(v));
+    }
+}
+
 template <int NT, int GDT, int MODE>
 __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const void* const* gp, float w, float inv_s,
                                                 SumSq& sq, bool& bad) {
@@ -717,7 +768,8 @@ template <int NT, int GDT, int MODE>
 __global__ void __launch_bounds__(kThreads, NT == kThreads && GDT != kF32 ? 3 : 2)
 k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
           const __grid_constant__ GradTable inl,
-          const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials) {
+          const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials,
+          int64_t fin) {
     const void* const* gp = gtab != nullptr ? gtab : inl.p;
     const float inv_s = __fdiv_rn(1.0f, st->S);
     SumSq sq;
@@ -730,6 +782,7 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
         sq = SumSq();
         bad = false;
     });
+    if (fin > 0) finish_pass(st, partials, fin);
 }
 
 // ---------------------------------------------------------------------------
@@ -867,7 +920,8 @@ __global__ void __launch_bounds__(kThreads, NT != kThreads ? (GDT == kF32 || KM 
                                             : GDT == kE4M3 ? TL_MINB_MANY_E4M3 : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
              const __grid_constant__ GradTableMany inl,
-             const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials) {
+             const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials,
+             int64_t fin) {
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
     SumSq sq;
     bool bad = false;
@@ -884,6 +938,7 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
             bad = false;
         }
     });
+    if (LAST && fin > 0) finish_pass(st, partials, fin);
 }
 
 // ---------------------------------------------------------------------------
@@ -1191,11 +1246,30 @@ __device__ __forceinline__ void adamw_segment(const Chunk& ch, int t, const Adam
     for (; j < len; j += NT) one(j);
 }
 
+// The clip coefficient of [MEG] section 9 from the global norm: max_norm / (norm +
+// 1e-6), applied only below 1; max_norm <= 0 disables clipping.
+__device__ __forceinline__ float clip_coef(float norm, float max_norm) {
+    float coef = 1.0f;
+    if (max_norm > 0.0f) {
+        const float cc = __fdiv_rn(max_norm, __fadd_rn(norm, 1e-6f));
+        if (cc < 1.0f) coef = cc;
+    }
+    return coef;
+}
+
+// What the scaler needs at the end of an AdamW launch (held by thread 0).
+struct AdamTail {
+    double b1n, b2n;   // beta powers of the update in flight
+    float coef;
+    int skip;
+};
+
 // The per-step AdamW scalars (fp64 beta powers, bias corrections rounded to fp32
-// once), computed by one thread and shared through shared memory; CTA 0 also
-// records the beta powers of the update in flight for the scaler kernel to
-// commit.  Returns true when the update is skipped (overflow flag set).
-__device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const AdamHP& hp, AdamConsts& out) {
+// once, the clip coefficient from the device norm), computed by one thread and
+// shared through shared memory.  Returns true when the update is skipped (overflow
+// flag set).  Thread 0 keeps what the scaler needs in `tail`.
+__device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const AdamHP& hp, AdamConsts& out,
+                                            AdamTail& tail) {
     __shared__ AdamConsts sk;
     __shared__ int skip;
     if (threadIdx.x == 0) {
@@ -1216,69 +1290,27 @@ __device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const Ada
         k.b2 = hp.beta2;
         k.omb2 = __fsub_rn(1.0f, hp.beta2);
         k.eps = hp.eps;
-        k.coef = st->coef;
+        k.coef = clip_coef(st->norm, hp.max_norm);
         sk = k;
-        if (blockIdx.x == 0 && !f) {
-            st->b1p_next = b1n;
-            st->b2p_next = b2n;
-        }
+        tail = AdamTail{b1n, b2n, k.coef, f};
     }
     __syncthreads();
     out = sk;
     return skip != 0;
 }
 
-template <int NT, int PDT>
-__global__ void __launch_bounds__(kThreads, NT != kThreads ? TL_MINB_ADAM_GROUP : TL_MINB_ADAM)
-k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
-        DevState* __restrict__ st, AdamHP hp) {
-    AdamConsts k;
-    if (adam_consts(st, hp, k)) return;
-    if (NT == kThreads) {
-        for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
-            adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromAcc(ch));
-        });
-        return;
-    }
-    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const Chunk& ch = group_segment(chunks, c0, c);
-        adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromAcc(ch));
-    }
-}
-
-// The re-materialising AdamW pass: u of every element recomputed from the
-// resident gradient lists (at most KM <= kRematLists of them) instead of read.
-template <int NT, int PDT, int GDT, int KM>
-__global__ void __launch_bounds__(kThreads, NT != kThreads && GDT == kF32 ? 1
-                                            : KM <= kFewLists && GDT != kF32 ? TL_MINB_REMAT_FEW : TL_MINB_REMAT)
-k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
-              DevState* __restrict__ st, AdamHP hp, const __grid_constant__ GradTableMany inl,
-              const __grid_constant__ ManyArgs a) {
-    AdamConsts k;
-    if (adam_consts(st, hp, k)) return;
-    const float inv_s = __fdiv_rn(1.0f, st->S);
-    if (NT == kThreads) {
-        for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
-            adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
-        });
-        return;
-    }
-    for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
-        const Chunk& ch = group_segment(chunks, c0, c);
-        adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
-    }
-}
-
 // ---------------------------------------------------------------------------
-// a6: the scaler state machine.  [MEG] section 5 (skip, back off to at least
-// min_loss_scale, reset the tracker; or count a good step and grow after
-// `interval` of them); [MP] "Dynamic scaling" (the count restarts after every
-// overflow and every growth); [RST] ch. 13 "Discard a failed partial logical
-// update" (a skipped attempt keeps t and the beta powers).  One thread.
+// a6: the scaler state machine, run by the last CTA of the update's last AdamW
+// launch.  [MEG] section 5 (skip, back off to at least min_loss_scale, reset the
+// tracker; or count a good step and grow after `interval` of them); [MP]
+// "Dynamic scaling" (the count restarts after every overflow and every growth);
+// [RST] ch. 13 "Discard a failed partial logical update" (a skipped attempt keeps
+// t and the beta powers).  Every CTA takes a ticket when it is done (after its
+// threads have read S and the flag); the CTA holding the last ticket has seen every
+// other CTA finish, so it may change S, clear the flag and reset the ticket.
 // ---------------------------------------------------------------------------
-__global__ void k_scaler(DevState* __restrict__ st, ScalerParams sp) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    if (st->found_inf) {
+__device__ __forceinline__ void scaler_step(DevState* __restrict__ st, const ScalerParams& sp, const AdamTail& tl_) {
+    if (tl_.skip) {
         if (sp.enabled) {
             const float s = __fmul_rn(st->S, sp.backoff);
             st->S = s > sp.min_scale ? s : sp.min_scale;
@@ -1287,8 +1319,8 @@ __global__ void k_scaler(DevState* __restrict__ st, ScalerParams sp) {
         st->skipped = 1;
     } else {
         st->t += 1;
-        st->b1p = st->b1p_next;
-        st->b2p = st->b2p_next;
+        st->b1p = tl_.b1n;
+        st->b2p = tl_.b2n;
         if (sp.enabled) {
             st->count += 1;
             if (st->count == sp.interval) {
@@ -1299,7 +1331,103 @@ __global__ void k_scaler(DevState* __restrict__ st, ScalerParams sp) {
         }
         st->skipped = 0;
     }
+    st->coef = tl_.coef;
     st->found_inf = 0;
+}
+
+__device__ __noinline__ void adam_finish(DevState* __restrict__ st, const ScalerParams& sp, const AdamTail& tail) {
+    __shared__ int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t ticket = atomicAdd(&st->adam_ticket, 1u);
+        last = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0 || !last) return;
+    __threadfence();
+    st->adam_ticket = 0;
+    scaler_step(st, sp, tail);
+}
+
+template <int NT, int PDT>
+__global__ void __launch_bounds__(kThreads, NT != kThreads ? TL_MINB_ADAM_GROUP : TL_MINB_ADAM)
+k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
+        DevState* __restrict__ st, AdamHP hp, ScalerParams sp) {
+    AdamConsts k;
+    AdamTail tail;
+    if (!adam_consts(st, hp, k, tail)) {
+        if (NT == kThreads) {
+            for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
+                adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromAcc(ch));
+            });
+        } else {
+            for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+                const Chunk& ch = group_segment(chunks, c0, c);
+                adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromAcc(ch));
+            }
+        }
+    }
+    if (sp.run) adam_finish(st, sp, tail);
+}
+
+// The re-materialising AdamW pass: u of every element recomputed from the
+// resident gradient lists (at most KM <= kRematLists of them) instead of read.
+template <int NT, int PDT, int GDT, int KM>
+__global__ void __launch_bounds__(kThreads, NT != kThreads && GDT == kF32 ? 1
+                                            : KM <= kFewLists && GDT != kF32 ? TL_MINB_REMAT_FEW : TL_MINB_REMAT)
+k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
+              DevState* __restrict__ st, AdamHP hp, ScalerParams sp, const __grid_constant__ GradTableMany inl,
+              const __grid_constant__ ManyArgs a) {
+    AdamConsts k;
+    AdamTail tail;
+    const float inv_s = __fdiv_rn(1.0f, st->S);
+    if (!adam_consts(st, hp, k, tail)) {
+        if (NT == kThreads) {
+            for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
+                adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
+            });
+        } else {
+            for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
+                const Chunk& ch = group_segment(chunks, c0, c);
+                adamw_segment<32, PDT>(ch, threadIdx.x & 31, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
+            }
+        }
+    }
+    if (sp.run) adam_finish(st, sp, tail);
+}
+
+// ---------------------------------------------------------------------------
+// Scalars of one update, one thread each: the clip coefficient from the device
+// norm (for a status read before the AdamW launch has computed it); the local
+// squared norm and overflow flag copied out to caller memory, and a global squared
+// norm and flag (combined across the shards of a sharded update by the caller)
+// taken in as the update's: [MEG] section 6 "Overflow must be global" (all ranks of
+// one logical update take the same step-or-skip decision) and section 9 (local
+// squared norms reduced before the root is taken); [ZRO] "Gradient clipping" (each
+// device sums the squares of its own slice, the scalars are all-reduced, then the
+// root is taken and the scale applied).
+// ---------------------------------------------------------------------------
+__global__ void k_coef(DevState* __restrict__ st, float max_norm) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) st->coef = clip_coef(st->norm, max_norm);
+}
+
+__global__ void k_export(const DevState* __restrict__ st, double* __restrict__ sumsq, int32_t* __restrict__ flag) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        sumsq[0] = st->sumsq;
+        flag[0] = st->found_inf;
+    }
+}
+
+__global__ void k_import(DevState* __restrict__ st, const double* __restrict__ sumsq,
+                         const int32_t* __restrict__ flag, float max_norm) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const double v = sumsq[0];
+    st->sumsq = v;
+    if (flag[0] != 0 || !isfinite(v)) st->found_inf = 1;
+    const float norm = __double2float_rn(__dsqrt_rn(v));
+    st->norm = norm;
+    st->coef = clip_coef(norm, max_norm);
 }
 
 // ---------------------------------------------------------------------------
@@ -1317,10 +1445,10 @@ __global__ void k_seed(const DevState* __restrict__ st, float w, float* __restri
 // ---------------------------------------------------------------------------
 using AccFn = void (*)(const Chunk*, int64_t, int64_t, const GradTable, const void* const*, float);
 using UnsFn = void (*)(const Chunk*, int64_t, int64_t, int, const GradTable, const void* const*, float,
-                       DevState*, double*);
+                       DevState*, double*, int64_t);
 using ManyFn = void (*)(const Chunk*, int64_t, int64_t, int, const GradTableMany, const ManyArgs,
-                        DevState*, double*);
-using AdamFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP);
+                        DevState*, double*, int64_t);
+using AdamFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP, ScalerParams);
 
 template <int NT>
 AccFn acc_fn_nt(int gdt, bool first) {
@@ -1400,7 +1528,7 @@ ManyFn check_fn_nt(int gdt, bool few) {
 }
 ManyFn check_fn(int gdt, bool small, bool few) { return small ? check_fn_nt<32>(gdt, few) : check_fn_nt<kThreads>(gdt, few); }
 
-using RematFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP, const GradTableMany,
+using RematFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP, ScalerParams, const GradTableMany,
                          const ManyArgs);
 
 template <int NT, int PDT, int GDT>
@@ -1450,19 +1578,19 @@ cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chun
 
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
                            int64_t c1, int run, const GradTable& inl, const void* const* gtab, float w, DevState* st,
-                           double* partials, int grid, cudaStream_t s) {
+                           double* partials, int64_t fin, int grid, cudaStream_t s) {
     UnsFn f = uns_fn(gdt, mode, small);
     if (f == nullptr || run < 1) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, gtab, w, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, gtab, w, st, partials, fin);
     return cudaGetLastError();
 }
 
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
                               int64_t c0, int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a,
-                              DevState* st, double* partials, int grid, cudaStream_t s) {
+                              DevState* st, double* partials, int64_t fin, int grid, cudaStream_t s) {
     ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, last ? fin : 0);
     return cudaGetLastError();
 }
 
@@ -1475,38 +1603,48 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
 }
 
 cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1, int run,
-                              const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials, int grid,
-                              cudaStream_t s) {
+                              const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
+                              int64_t fin, int grid, cudaStream_t s) {
     ManyFn f = check_fn(gdt, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, fin);
     return cudaGetLastError();
 }
 
 cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, int64_t c0,
-                               int64_t c1, DevState* st, AdamHP hp, const GradTableMany& inl, const ManyArgs& a,
-                               int grid, cudaStream_t s) {
+                               int64_t c1, DevState* st, AdamHP hp, ScalerParams sp, const GradTableMany& inl,
+                               const ManyArgs& a, int grid, cudaStream_t s) {
     RematFn f = remat_fn(pdt, gdt, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kRematLists) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, inl, a);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, sp, inl, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
-                         DevState* st, AdamHP hp, int grid, cudaStream_t s) {
+                         DevState* st, AdamHP hp, ScalerParams sp, int grid, cudaStream_t s) {
     AdamFn f = adam_fn(pdt, small);
     if (f == nullptr) return cudaErrorInvalidValue;
-    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_scaler(DevState* st, ScalerParams sp, cudaStream_t s) {
-    k_scaler<<<1, 32, 0, s>>>(st, sp);
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, sp);
     return cudaGetLastError();
 }
 
 cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s) {
     k_seed<<<1, 32, 0, s>>>(st, w, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_coef(DevState* st, float max_norm, cudaStream_t s) {
+    k_coef<<<1, 32, 0, s>>>(st, max_norm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_export(const DevState* st, double* sumsq, int32_t* flag, cudaStream_t s) {
+    k_export<<<1, 32, 0, s>>>(st, sumsq, flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_import(DevState* st, const double* sumsq, const int32_t* flag, float max_norm, cudaStream_t s) {
+    k_import<<<1, 32, 0, s>>>(st, sumsq, flag, max_norm);
     return cudaGetLastError();
 }
 

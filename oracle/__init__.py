@@ -105,6 +105,10 @@ def _bind(lib):
         "tlo_step": (i32, [vp, vp, vp, vp, i32, vp, i64, ctypes.POINTER(vp), i32, ctypes.POINTER(i64), i32,
                            f32, ctypes.POINTER(AdamWHP), ctypes.POINTER(ScalerCfg), ctypes.POINTER(State),
                            ctypes.POINTER(Result)]),
+        "tlo_partition_bounds": (None, [i64, i32, i64, vp]),
+        "tlo_step_sharded": (i32, [vp, vp, vp, vp, i32, vp, i64, ctypes.POINTER(vp), i32, ctypes.POINTER(i64), i32,
+                                   f32, ctypes.POINTER(AdamWHP), ctypes.POINTER(ScalerCfg), ctypes.POINTER(State),
+                                   ctypes.POINTER(Result), i32, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -162,12 +166,15 @@ class Oracle:
         return int(self.w.size)
 
     def step(self, grads, counts, max_norm: float, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8,
-             weight_decay=0.1, lr_schedule=None) -> Result:
+             weight_decay=0.1, lr_schedule=None, shards=None) -> Result:
         """One attempted logical update over k micro-batches (grads[i] is a flat
         array of P gradient values: uint16 bits for bf16/f16, float32 for f32; for
         e4m3b16 a pair (uint8 codes of P elements, float32 block scales)).  With
         lr_schedule (float32 rates of optimizer steps 1, 2, ...) the rate is the
-        schedule's entry for the step this update would commit, in place of lr."""
+        schedule's entry for the step this update would commit, in place of lr.
+        shards=(nranks, align): the sharded statement of the same update (every rank's
+        slice simulated in turn, flags and squared norms combined across ranks); the
+        per-rank squared norms and flags are left in self.rank_sumsq / self.rank_flag."""
         if lr_schedule is not None:
             table = np.ascontiguousarray(lr_schedule, dtype=np.float32)
             assert table.size > 0
@@ -191,10 +198,16 @@ class Oracle:
         cnts = (ctypes.c_int64 * k)(*[int(c) for c in counts])
         hp = AdamWHP(lr, beta1, beta2, eps, weight_decay)
         res = Result()
-        rc = self.lib.tlo_step(_ptr(self.w), _ptr(self.m), _ptr(self.v), _ptr(self.p), self.pdtype,
-                               _ptr(self.acc), self.P, gptrs, self.gdtype, cnts, k, float(max_norm),
-                               ctypes.byref(hp), ctypes.byref(self.cfg), ctypes.byref(self.state),
-                               ctypes.byref(res))
+        args = (_ptr(self.w), _ptr(self.m), _ptr(self.v), _ptr(self.p), self.pdtype, _ptr(self.acc), self.P, gptrs,
+                self.gdtype, cnts, k, float(max_norm), ctypes.byref(hp), ctypes.byref(self.cfg),
+                ctypes.byref(self.state), ctypes.byref(res))
+        if shards is None:
+            rc = self.lib.tlo_step(*args)
+        else:
+            nranks, align = int(shards[0]), int(shards[1])
+            self.rank_sumsq = np.zeros(nranks, dtype=np.float64)
+            self.rank_flag = np.zeros(nranks, dtype=np.int32)
+            rc = self.lib.tlo_step_sharded(*args, nranks, align, _ptr(self.rank_sumsq), _ptr(self.rank_flag))
         if rc != 0:
             raise ValueError("oracle rejected the logical update (counts must be positive, N <= 2^53)")
         self.last = res
@@ -206,6 +219,13 @@ class Oracle:
 
 
 # ---- element-wise helpers over numpy arrays (loops in C) -------------------
+
+def partition_bounds(P: int, nranks: int, align: int = 1) -> np.ndarray:
+    """Cut points of the sharded statement: slice r is [b[r], b[r+1])."""
+    b = np.zeros(nranks + 1, dtype=np.int64)
+    load().tlo_partition_bounds(int(P), int(nranks), int(align), _ptr(b))
+    return b
+
 
 def recast(x: np.ndarray, dtype: str) -> np.ndarray:
     """rd16: fp32 -> bf16/f16 bits, round to nearest even."""

@@ -23,8 +23,10 @@
  *          gradients is not just casting", section 9 "Gradient clipping under
  *          model parallelism".
  *   [ZRO]  "Your weights fit on one device but Adam's moments do not - how do
- *          you shard the optimizer state?": section "Why the optimizer state is
- *          the thing that overflows".
+ *          you shard the optimizer state?": sections "Why the optimizer state is
+ *          the thing that overflows", "The scheme", "Operational sharp edges"
+ *          ("Gradient clipping", "Partition granularity").
+ *   [MEG]  also section 6 "Overflow must be global" (the sharded step).
  *   [RST]  "Practical LLM in Rust", chapter 13 "Accumulate gradients and
  *          recompute activations": "Weight each mean by the targets it
  *          represents" (equation block), "Discard a failed partial logical
@@ -434,6 +436,112 @@ int tlo_step(float* w, float* m, float* v, uint16_t* p, int pdtype, float* acc, 
         tlo_adamw_recast(w, m, v, p, pdtype, acc, P, coef, &s);
     }
     tlo_scaler_update(st, cfg, found_inf, b1p_next, b2p_next);
+    res->skipped = found_inf;
+    res->found_inf = found_inf;
+    res->norm = norm;
+    res->coef = coef;
+    res->sumsq = sumsq;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The sharded step.  [ZRO] "The scheme": the parameter vector is split into  */
+/* N disjoint slices and device i keeps the master weights and both moments  */
+/* of slice i alone and updates that slice; "Partition granularity": slicing */
+/* the flat vector may split a tensor between owners.  [ZRO] "Operational    */
+/* sharp edges", "Gradient clipping": each device sums the squares over its  */
+/* own slice and those scalars are all-reduced before the root is taken.     */
+/* [MEG] section 6 "Overflow must be global": the overflow flag is           */
+/* all-reduced with max, so every rank steps or skips together; section 9:   */
+/* local squared norms, reduced, then one coefficient for every rank.        */
+/* ------------------------------------------------------------------------ */
+
+/* Cut points of nranks slices of a flattened list of P elements (tensor order,
+ * then element order): bounds[j] = the largest multiple of align that is not
+ * above floor(j * P / nranks), for j < nranks, and bounds[nranks] = P.  Slice r
+ * is [bounds[r], bounds[r+1]). */
+void tlo_partition_bounds(int64_t P, int nranks, int64_t align, int64_t* bounds) {
+    for (int j = 0; j < nranks; ++j) {
+        __int128 f = ((__int128)j * (__int128)P) / (__int128)nranks;
+        bounds[j] = (int64_t)(f - f % (__int128)align);
+    }
+    bounds[nranks] = P;
+}
+
+static int64_t elem_bytes(int dtype) {
+    return dtype == TLO_DT_F32 ? 4 : 2;
+}
+
+/* One attempted logical update of a list sharded over nranks owners, every rank
+ * simulated in turn: each rank accumulates, unscales and checks its own slice
+ * and sums its own squares (rank_flag[r], rank_sumsq[r]); the flags are combined
+ * with max and the squared norms summed in rank order (the all-reduces); every
+ * rank then clips with the one global coefficient and steps its slice, and the
+ * scaler takes the global decision once.  Same arguments as tlo_step plus the
+ * slicing (nranks >= 1, align >= 1) and the per-rank outputs. */
+int tlo_step_sharded(float* w, float* m, float* v, uint16_t* p, int pdtype, float* acc, int64_t P,
+                     const void* const* grads, int gdtype, const int64_t* counts, int k,
+                     float max_norm, const tlo_adamw_hp* hp, const tlo_scaler_cfg* cfg,
+                     tlo_state* st, tlo_result* res, int nranks, int64_t align,
+                     double* rank_sumsq, int* rank_flag) {
+    if (k < 1 || nranks < 1 || align < 1) return -1;
+    int64_t N = 0;
+    for (int i = 0; i < k; ++i) {
+        if (counts[i] <= 0) return -1;
+        N += counts[i];
+    }
+    if (N > ((int64_t)1 << 53)) return -1;
+    int64_t* b = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nranks + 1));
+    if (b == NULL) return -1;
+    tlo_partition_bounds(P, nranks, align, b);
+    float* deq = NULL;
+    if (gdtype == TLO_DT_E4M3B16) {
+        deq = (float*)malloc(sizeof(float) * (size_t)(P > 0 ? P : 1));
+        if (deq == NULL) { free(b); return -1; }
+    }
+    /* every rank accumulates its slice of every micro-batch */
+    for (int i = 0; i < k; ++i) {
+        const char* gi = (const char*)grads[i];
+        int gdt = gdtype;
+        if (deq != NULL) {
+            tlo_dequant_e4m3b16((const tlo_e4m3_list*)grads[i], deq);
+            gi = (const char*)deq;
+            gdt = TLO_DT_F32;
+        }
+        float wi = tlo_microbatch_weight(counts[i], N);
+        for (int r = 0; r < nranks; ++r)
+            tlo_accumulate(acc + b[r], gi + b[r] * elem_bytes(gdt), gdt, b[r + 1] - b[r], wi, i == 0);
+    }
+    free(deq);
+    /* local unscale, check and squared norm of each slice */
+    for (int r = 0; r < nranks; ++r) {
+        rank_flag[r] = tlo_unscale_check(acc + b[r], b[r + 1] - b[r], st->S);
+        rank_sumsq[r] = tlo_sumsq(acc + b[r], b[r + 1] - b[r]);
+    }
+    /* the all-reduces: max of the flags, sum of the squared norms in rank order */
+    int found_inf = 0;
+    double sumsq = 0.0;
+    for (int r = 0; r < nranks; ++r) {
+        if (rank_flag[r]) found_inf = 1;
+        sumsq += rank_sumsq[r];
+    }
+    float norm = 0.0f, coef = 1.0f;
+    if (!found_inf) {
+        found_inf = isfinite(sumsq) ? 0 : 1;        /* READING R4 */
+        norm = tlo_norm_from_sumsq(sumsq);
+        coef = tlo_clip_coef(norm, max_norm);
+    } else {
+        sumsq = 0.0;
+    }
+    const double b1n = (double)hp->beta1 * st->b1p;   /* beta powers of step t+1 */
+    const double b2n = (double)hp->beta2 * st->b2p;
+    if (found_inf == 0) {   /* every rank steps its own slice with the one coefficient */
+        const tlo_adamw_scalars s = tlo_adamw_prepare(hp, b1n, b2n);
+        for (int r = 0; r < nranks; ++r)
+            tlo_adamw_recast(w + b[r], m + b[r], v + b[r], p + b[r], pdtype, acc + b[r], b[r + 1] - b[r], coef, &s);
+    }
+    tlo_scaler_update(st, cfg, found_inf, b1n, b2n);
+    free(b);
     res->skipped = found_inf;
     res->found_inf = found_inf;
     res->norm = norm;

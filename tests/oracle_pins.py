@@ -748,4 +748,68 @@ def pin_e4m3_step_equals_step_on_dequantized(lib):
     assert r.skipped == 1
 
 
+# --------------------------------------------------------------------------
+# The sharded step ([ZRO] "The scheme", "Operational sharp edges"; [MEG] sections 6, 9)
+# --------------------------------------------------------------------------
+
+def pin_partition_covers_every_element_once(lib):
+    """The slices of the sharded statement: disjoint, covering [0, P) in order, cut on
+    multiples of align, and balanced (each cut within align of j*P/N), for lists shorter
+    than the rank count, empty lists and uneven sizes; every element counted once by brute
+    force on small cases."""
+    cases = [(0, 3, 1), (5, 8, 1), (100, 3, 16), (1000, 7, 1), (1000, 7, 16), (12345, 5, 8),
+             (2 ** 40 + 3, 6, 16), (16, 16, 16), (17, 2, 16)]
+    for P, N, align in cases:
+        b = oracle.partition_bounds(P, N, align)
+        assert b[0] == 0 and b[-1] == P and b.size == N + 1, (P, N, align)
+        assert np.all(np.diff(b) >= 0), (P, N, align)
+        for j in range(1, N):
+            assert b[j] % align == 0, (P, N, align)
+            assert 0 <= Fraction(j * P, N) - b[j] < align, (P, N, align, j)
+        if P <= 20000:
+            owners = np.zeros(P, dtype=np.int64)
+            for r in range(N):
+                owners[b[r]:b[r + 1]] += 1
+            assert np.all(owners == 1), (P, N, align)
+
+
+def pin_sharded_step_equals_unsharded(lib):
+    """[ZRO]: N devices each updating their own slice, with the squared norms all-reduced
+    before the root and the overflow flag all-reduced ([MEG] section 6), compute the update
+    of one device holding everything.  Per element the operations are the same, so the
+    state is bit-identical whenever the fp32 norm is (it is here); the squared norm differs
+    only by the fp64 association of the rank sums (equal for one rank).  An overflow in the
+    last rank's slice makes every rank skip; each rank's squared norm is its slice's."""
+    rng = np.random.default_rng(11)
+    numel = [37, 4096, 5, 999, 2048, 1]
+    P = sum(numel)
+    master = rng.standard_normal(P).astype(np.float32) * 0.02
+    for N, align in ((1, 1), (2, 1), (3, 16), (5, 16), (2, 64)):
+        ref = make_oracle(lib, master, pdtype="f16", gdtype="f16", scaler_enabled=True, init_scale=2.0 ** 10,
+                          interval=2, numel=numel)
+        shd = make_oracle(lib, master, pdtype="f16", gdtype="f16", scaler_enabled=True, init_scale=2.0 ** 10,
+                          interval=2, numel=numel)
+        bounds = oracle.partition_bounds(P, N, align)
+        for step in range(5):
+            grads = [oracle.recast(rng.standard_normal(P).astype(np.float32) * 0.05 * ref.state.S, "f16")
+                     for _ in range(3)]
+            if step == 3:
+                grads[1][P - 2] = 0x7C00               # +inf in the last slice only
+            ra = ref.step(grads, [3, 1, 2], 1.0)
+            rb = shd.step(grads, [3, 1, 2], 1.0, shards=(N, align))
+            assert (ra.skipped, ra.found_inf) == (rb.skipped, rb.found_inf) == ((1, 1) if step == 3 else (0, 0))
+            assert shd.rank_flag[-1] == (1 if step == 3 else 0) and not np.any(shd.rank_flag[:-1])
+            if not ra.skipped:
+                assert ra.norm == rb.norm and ra.coef == rb.coef and ra.coef < 1.0
+                assert abs(ra.sumsq - rb.sumsq) <= 1e-12 * ra.sumsq
+                if N == 1:
+                    assert ra.sumsq == rb.sumsq
+                for r in range(N):   # each rank's squared norm is its own slice's
+                    assert shd.rank_sumsq[r] == lib.tlo_sumsq(
+                        shd.acc[bounds[r]:].ctypes.data_as(ctypes.c_void_p), int(bounds[r + 1] - bounds[r]))
+            assert ref.scalars() == shd.scalars()
+            for f in ("w", "m", "v", "p"):
+                assert np.array_equal(getattr(ref, f), getattr(shd, f)), (N, align, step, f)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

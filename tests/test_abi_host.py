@@ -131,3 +131,41 @@ def test_product_path_does_not_reach_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "tlo_" not in text and "libtlo" not in text, f
+
+
+def test_partition_pieces_match_the_oracle_cut_points(lib):
+    """tl_partition (host only): the pieces of every rank, flattened, are exactly the
+    oracle's slice [b_r, b_(r+1)), in tensor order, with no empty piece; bad arguments
+    are rejected."""
+    import numpy as np
+    import oracle
+    cases = [([37, 4096, 5, 999, 2048, 1, 3000], 2, 16), ([10], 4, 1), ([0, 5, 0, 7], 3, 1),
+             ([1] * 50, 7, 1), ([16384] * 8 + [3], 5, 16), ([], 2, 1), ([2 ** 33, 5], 3, 16)]
+    for numel, N, align in cases:
+        P = sum(numel)
+        b = oracle.partition_bounds(P, N, align)
+        starts = np.concatenate([[0], np.cumsum(numel)]).astype(np.int64)
+        covered = 0
+        for r in range(N):
+            pieces = tl.tl_partition(numel, N, r, align)
+            pos = b[r]
+            for t, s, n in pieces:
+                assert n > 0 and 0 <= s and s + n <= numel[t]
+                assert starts[t] + s == pos            # contiguous, in order
+                pos += n
+            assert pos == b[r + 1], (numel, N, align, r)
+            covered += b[r + 1] - b[r]
+        assert covered == P
+    arr = (ctypes.c_int64 * 2)(10, 20)
+    t, s, n = (ctypes.c_int64 * 2)(), (ctypes.c_int64 * 2)(), (ctypes.c_int64 * 2)()
+    cnt = ctypes.c_int64()
+    for args in ((2, arr, 0, 0, 1), (2, arr, 2, 2, 1), (2, arr, 2, -1, 1), (2, arr, 2, 0, 0)):
+        assert lib.tl_partition(*args, t, s, n, 2, ctypes.byref(cnt)) == tl.TL_EINVAL
+    # too small a capacity: the count is still reported
+    assert lib.tl_partition(2, arr, 1, 0, 1, t, s, n, 1, ctypes.byref(cnt)) == tl.TL_EINVAL and cnt.value == 2
+    assert lib.tl_partition(2, arr, 1, 0, 1, t, s, n, 2, ctypes.byref(cnt)) == tl.TL_OK and cnt.value == 2
+
+
+def test_sharded_norm_calls_reject_bad_arguments(lib):
+    assert lib.tl_local_sumsq(None, None, None, None) == tl.TL_EINVAL
+    assert lib.tl_grad_norm_from(None, None, None, 1.0, None) == tl.TL_EINVAL

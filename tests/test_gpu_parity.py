@@ -132,9 +132,30 @@ EDGE_LISTS = {
 @pytest.mark.parametrize("dtypes", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32"), ("f16", "bf16")],
                          ids=lambda d: f"p{d[0]}-g{d[1]}")
 @pytest.mark.parametrize("gaps", [False, True, "packed"], ids=["aligned", "misaligned", "packed"])
-def test_edge_lists(lst, dtypes, gaps):
+@pytest.mark.parametrize("grouped", [False, True], ids=["ungrouped", "grouped"])
+def test_edge_lists(lst, dtypes, gaps, grouped, monkeypatch):
+    """grouped: every small tensor goes to the one-warp-per-tensor group part of the table
+    (as on lists with many small tensors), else the few small tensors of these lists are
+    whole-CTA segments of their own."""
+    if grouped:
+        monkeypatch.setenv("TL_SMALL_GROUP_MIN", "1")
     wl = custom(EDGE_LISTS[lst], pdtype=dtypes[0], gdtype=dtypes[1], k=3, steps=2, counts=[5, 1, 7])
     run_parity(wl, gaps=gaps)
+    for resident in (True, "remat"):
+        run_parity(wl, gaps=gaps, resident=resident)
+
+
+@pytest.mark.parametrize("resident,launches", [(True, 2), ("remat", 2), (False, 5)],
+                         ids=["resident", "remat", "per_microbatch"])
+def test_launches_per_update_on_the_mid_size_list(resident, launches):
+    """The ~10.3M-parameter list (few small tensors, few enough chunks that the pass
+    finishes the norm itself, the scaler running at the end of the AdamW launch): the
+    resident and re-materialising updates are two launches, the per-micro-batch one k + 1
+    (three accumulations, the last micro-batch's pass, AdamW); the results still match the
+    oracle over 2 updates."""
+    wl = W.make("llama_10m")
+    gpu, orc, log = run_parity(wl, steps=2, resident=resident)
+    assert tl.tl_launch_count(gpu.ctx) == 2 * launches
 
 
 @pytest.mark.parametrize("k", [1, 2, 5])
@@ -582,21 +603,34 @@ def test_llama_1b_full_size_sampled(name, resident):
     assert gpu.status().t == 5
 
 
-def test_failed_launch_abandons_the_update(monkeypatch):
-    """Host-side fault injection (no kernel is harmed): the context's 6th launch reports a
-    failure.  The update in flight is abandoned, every update call is refused until
-    tl_set_state restores the scalars, and the redone update matches the oracle."""
-    wl = custom([5000, 300, 17000], k=2, steps=1, counts=[3, 4])   # 3 whole-CTA chunks + 1 group
+@pytest.mark.parametrize("fused", [True, False], ids=["norm_in_pass", "norm_launch"])
+def test_failed_launch_abandons_the_update(monkeypatch, fused):
+    """Host-side fault injection (no kernel is harmed): the launch of the first AdamW part
+    (of two: the small tensor forms a group) reports a failure.  The update in flight is
+    abandoned, every update call is refused until tl_set_state restores the scalars, and
+    the redone update matches the oracle.  Both with the norm finished by the pass and with
+    a separate norm launch (a list of more than 4,096 chunks)."""
+    numel = [5000, 300, 17000] if fused else [5000, 300, 17000, 4100 * 16384]
+    wl = custom(numel, k=2, steps=1, counts=[3, 4])
     master0 = W.master_init(wl)
-    monkeypatch.setenv("TL_TEST_FAIL_LAUNCH", "6")
+    monkeypatch.setenv("TL_SMALL_GROUP_MIN", "1")
+    grads = [W.grad_input(wl, 1, i) for i in range(2)]
+    # the launches before the AdamW call, counted on a context without the fault
+    probe = GpuOptimizer(wl, master0, key=90)
+    pp = [probe.grad_list(i, g) for i, g in enumerate(grads)]
+    tl.tl_accumulate(probe.ctx, pp[0], 3, 7, 1)
+    tl.tl_unscale_check(probe.ctx, pp[1], 4, 7)
+    tl.tl_grad_norm(probe.ctx, 1.0)
+    before_adamw = tl.tl_launch_count(probe.ctx)
+    assert before_adamw == (4 if fused else 5)   # two parts per pass (+ the norm launch)
+    del probe, pp
+    monkeypatch.setenv("TL_TEST_FAIL_LAUNCH", str(before_adamw + 1))
     gpu = GpuOptimizer(wl, master0)
     monkeypatch.delenv("TL_TEST_FAIL_LAUNCH")
     orc = oracle_for(wl, master0)
-    grads = [W.grad_input(wl, 1, i) for i in range(2)]
     pl = [gpu.grad_list(i, g) for i, g in enumerate(grads)]
     hp = tl.tl_adamw_hp(**W.HP)
     snap = tl.tl_get_state(gpu.ctx)
-    # launches: accumulate 1-2, unscale 3-4, norm 5, the first AdamW part 6 (fails, not launched)
     tl.tl_accumulate(gpu.ctx, pl[0], 3, 7, 1)
     tl.tl_unscale_check(gpu.ctx, pl[1], 4, 7)
     tl.tl_grad_norm(gpu.ctx, 1.0)

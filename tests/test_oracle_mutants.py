@@ -83,6 +83,15 @@ MUTANTS = [
     ("block_size_8", "g->scales[b + e / 16];", "g->scales[b + e / 8];"),
     ("scale_not_applied", "out[j] = tlo_e4m3_to_f32(g->codes[j]) * g->scales[b + e / 16];",
      "out[j] = tlo_e4m3_to_f32(g->codes[j]);"),
+    # the sharded step: a rank's squares left out of the sum, each rank clipping with its
+    # own partial norm ([ZRO] "Gradient clipping" warns of exactly this), and cuts off the
+    # alignment.  (A flag combined from one rank only is no mistake the pins can see: a
+    # non-finite element makes its square, hence the all-reduced sum, non-finite, and the
+    # non-finite sum skips the update on every rank anyway.)
+    ("shard_sum_drops_rank", "        sumsq += rank_sumsq[r];\n", "        if (r > 0) sumsq += rank_sumsq[r];\n"),
+    ("shard_local_clip", "b[r + 1] - b[r], coef, &s);",
+     "b[r + 1] - b[r], tlo_clip_coef(tlo_norm_from_sumsq(rank_sumsq[r]), max_norm), &s);"),
+    ("shard_cut_unaligned", "bounds[j] = (int64_t)(f - f % (__int128)align);", "bounds[j] = (int64_t)f;"),
 ]
 
 

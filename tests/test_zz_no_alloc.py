@@ -148,7 +148,7 @@ def test_no_alloc_matches_oracle_twice(case):
                     vals[o + 8:o + 24] = np.float32(1.5 * 2.0 ** 63 * S) * (1 + 0.01 * np.arange(16, dtype=np.float32))
         if call == 1 and case != "large_values":
             vals[offs[5] + 77] = np.nan                  # the second call overflows
-        buf.copy_(torch.from_numpy(vals))
+        buf[:total].copy_(torch.from_numpy(vals))
         torch.cuda.synchronize()
         if call == 1:
             free_before_second = torch.cuda.mem_get_info()[0]
