@@ -377,25 +377,36 @@ def time_graph(args, gw, path, world):
 
 
 def time_path(args, gw, path, world):
-    """K timed steps of one path (after W warm-up steps), with per-kernel events."""
+    """K timed steps of one path (after W warm-up steps), then the same K steps again with
+    a pair of CUDA events around every call for the per-kernel attribution (those events
+    and their host calls are kept out of the headline timing, where on short steps their
+    host time would show up as idle device time)."""
     import torch
     import loss_scaled_adamw_gb300 as tl
     for _ in range(args.warmup):
         gw.step(path)
     torch.cuda.synchronize()
     barrier()
-    events = []
     launches0 = tl.tl_launch_count(gw.ctx)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(args.steps):
-        gw.step(path, events)
+        gw.step(path)
     t1.record()
     torch.cuda.synchronize()
     barrier()
     elapsed = t0.elapsed_time(t1) / 1e3
     launches = tl.tl_launch_count(gw.ctx) - launches0
     elapsed_max = max_over_ranks(elapsed, gw.device)
+    events = []
+    i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    i0.record()
+    for _ in range(args.steps):
+        gw.step(path, events)
+    i1.record()
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_instr = i0.elapsed_time(i1) / 1e3
     peak, peak_kind = hbm_peak()
     per = {}
     for name, a, b in events:
@@ -404,7 +415,7 @@ def time_path(args, gw, path, world):
     kernels = {}
     for name, ts in per.items():
         avg = sum(ts) / len(ts)
-        entry = {"launches": len(ts), "avg_ms": avg * 1e3, "share": sum(ts) / elapsed}
+        entry = {"launches": len(ts), "avg_ms": avg * 1e3, "share": sum(ts) / elapsed_instr}
         if bytes_of.get(name):
             gbs = bytes_of[name] * gw.P / avg / 1e9
             entry.update({"bytes_per_param": bytes_of[name], "bytes_per_launch": bytes_of[name] * gw.P,
@@ -412,6 +423,7 @@ def time_path(args, gw, path, world):
         kernels[name] = entry
     sb = gw.step_bytes(path)
     return {"elapsed_max": elapsed_max, "launches": launches, "kernels": kernels,
+            "instrumented_ms_per_step": elapsed_instr / args.steps * 1e3,
             "value": whole_job_rate(gw.P, args.steps, world, elapsed_max),
             "ms_per_step": elapsed_max / args.steps * 1e3,
             "hbm": {"algorithmic_bytes_per_step": sb, "bytes_per_param": sb / gw.P,
@@ -469,6 +481,8 @@ def run_gpu(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_kind": peak_kind,
                      "traffic": recorded_traffic(TRAFFIC_KEYS.get(dom, dom), wl.name, args.layout)},
         "kernels": kernels,
+        "kernel_timing": "per-call CUDA events on the launching stream, from a second run of the same K steps "
+                         "(the headline timing has no per-call events)",
         "gpu_launches": head["launches"],
         "paths": {p: {k2: timed[p][k2] for k2 in (("value", "ms_per_step", "hbm") if p == args.path else
                                                    ("value", "ms_per_step", "hbm", "kernels"))} for p in names},
@@ -630,29 +644,113 @@ def oracle_sample(wl, n_params: int):
     return master, p0, grads
 
 
-def time_oracle(wl, seconds: float, steps=None):
+def host_cores() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+class SlicedOracle:
+    """The oracle's element-wise functions (tlo_accumulate, tlo_unscale_check, tlo_sumsq,
+    tlo_adamw_recast), unchanged, run on `threads` disjoint contiguous slices of one flat
+    list from host threads (ctypes releases the GIL during each call); the slices'
+    squared norms are added in slice order, and the per-update scalars are the oracle's
+    own (tlo_adamw_prepare, tlo_scaler_update).  A timing baseline on all host cores, not
+    a parity reference."""
+
+    def __init__(self, master, p0, wl, threads: int):
+        import ctypes
+        import oracle
+        self.ct = ctypes
+        self.lib = oracle.load()
+        self.oracle = oracle
+        self.w = np.ascontiguousarray(master, np.float32).copy()
+        self.m = np.zeros_like(self.w)
+        self.v = np.zeros_like(self.w)
+        self.p = np.ascontiguousarray(p0, np.uint16).copy()
+        self.acc = np.empty_like(self.w)
+        self.n = self.w.size
+        self.wl = wl
+        self.pdt = oracle.dtype_code(wl.param_dtype)
+        self.threads = max(1, int(threads))
+        step = (self.n + self.threads - 1) // self.threads
+        self.slices = [(lo, min(self.n, lo + step)) for lo in range(0, self.n, step)]
+        self.state = oracle.State(1.0, 0, 0, 1.0, 1.0)
+        self.cfg = oracle.ScalerCfg(0, 2.0, 0.5, 2000, 1.0, 2.0 ** 127)
+        self.hp = oracle.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1)
+        from concurrent.futures import ThreadPoolExecutor
+        self.pool = ThreadPoolExecutor(self.threads)
+
+    def _at(self, a, lo):
+        return self.ct.c_void_p(a.ctypes.data + a.itemsize * lo)
+
+    def _par(self, fn):
+        return list(self.pool.map(lambda s: fn(*s), self.slices))
+
+    def step(self, grads, counts, max_norm):
+        lib, ct, orc = self.lib, self.ct, self.oracle
+        N = sum(counts)
+        for i, g in enumerate(grads):
+            if isinstance(g, tuple):            # 8-bit: the oracle's dequantization of the sample first
+                g = orc.dequant_e4m3b16(g[0], g[1], [g[0].size])
+                dt = orc.DT_F32
+            else:
+                dt = orc.DT_F32 if g.dtype == np.float32 else orc.dtype_code(self.wl.grad_dtype)
+            wi = lib.tlo_microbatch_weight(counts[i], N)
+            self._par(lambda lo, hi: lib.tlo_accumulate(self._at(self.acc, lo), self._at(g, lo), dt, hi - lo, wi,
+                                                        1 if i == 0 else 0))
+        found = any(self._par(lambda lo, hi: lib.tlo_unscale_check(self._at(self.acc, lo), hi - lo, self.state.S)))
+        sums = self._par(lambda lo, hi: lib.tlo_sumsq(self._at(self.acc, lo), hi - lo))
+        sumsq = 0.0
+        for x in sums:
+            sumsq += x
+        st = self.state
+        b1n = st.b1p * float(np.float32(self.hp.beta1))
+        b2n = st.b2p * float(np.float32(self.hp.beta2))
+        if not found and np.isfinite(sumsq):
+            coef = lib.tlo_clip_coef(lib.tlo_norm_from_sumsq(sumsq), max_norm)
+            sc = lib.tlo_adamw_prepare(ct.byref(self.hp), b1n, b2n)
+            self._par(lambda lo, hi: lib.tlo_adamw_recast(self._at(self.w, lo), self._at(self.m, lo),
+                                                          self._at(self.v, lo), self._at(self.p, lo), self.pdt,
+                                                          self._at(self.acc, lo), hi - lo, coef, ct.byref(sc)))
+        else:
+            found = True
+        lib.tlo_scaler_update(ct.byref(st), ct.byref(self.cfg), 1 if found else 0, b1n, b2n)
+
+
+def time_oracle(wl, seconds: float, steps=None, threads: int = 1):
     """Time the oracle's logical update on a contiguous sample of the workload sized for
-    about `seconds` of CPU time (at most 2^27 parameters, repeated over several logical
-    updates when the cap binds, unless `steps` is given)."""
+    about `seconds` of CPU time (at most 2^27 parameters per thread and 2^30 in all,
+    repeated over several logical updates when the cap binds, unless `steps` is given).
+    threads = 1: the plain single-threaded oracle (tlo_step); threads > 1: its element
+    functions on disjoint slices on that many host cores (SlicedOracle)."""
     import oracle
-    n = 1 << 20
-    master, p0, grads = oracle_sample(wl, n)
-    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype, numel=[master.size])
+
+    def make(n):
+        master, p0, grads = oracle_sample(wl, n)
+        if threads == 1:
+            return oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype, numel=[master.size]), grads
+        return SlicedOracle(master, p0, wl, threads), grads
+
+    n = (1 << 20) * threads
+    o, grads = make(n)
     t = time.perf_counter()
     o.step(grads, wl.counts(1), wl.max_norm)
     per_param = (time.perf_counter() - t) / n
-    n = int(min(max(seconds / per_param / (steps or 1), 1 << 20), 1 << 27, wl.P))
+    n = int(min(max(seconds / per_param / (steps or 1), 1 << 20), (1 << 27) * threads, 1 << 30, wl.P))
     if steps is None:
         steps = max(1, int(round(seconds / (per_param * n))))
-    master, p0, grads = oracle_sample(wl, n)
-    o = oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype, numel=[master.size])
+    o, grads = make(n)
     t = time.perf_counter()
     for s in range(steps):
         o.step(grads, wl.counts(s + 1), wl.max_norm)
     el = time.perf_counter() - t
-    return {"value": n * steps / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+    how = "single-threaded C oracle (tlo_step)" if threads == 1 else \
+        f"the C oracle's element functions on {threads} disjoint slices, one host thread each"
+    return {"value": n * steps / el / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} parameters (a contiguous slice of the {wl.name} tensor list), k={wl.k}, "
-                      f"{steps} logical update(s), {el:.1f} s, single-threaded C oracle"}
+                      f"{steps} logical update(s), {el:.1f} s, {how}"}
 
 
 def run_reference(args, rank, world):
@@ -661,10 +759,11 @@ def run_reference(args, rank, world):
     oracle.build()
     wl = W.make(args.workload)
     per_step = max(args.cpu_seconds / max(args.steps, 1), 1.0)
+    cores = host_cores()
     for _ in range(min(args.warmup, 1)):
-        time_oracle(wl, 0.5)
+        time_oracle(wl, 0.5, threads=cores)
     t = time.perf_counter()
-    res = time_oracle(wl, per_step * args.steps, steps=args.steps)
+    res = time_oracle(wl, per_step * args.steps, steps=args.steps, threads=cores)
     el = time.perf_counter() - t
     return {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
@@ -697,7 +796,11 @@ def main(argv=None):
             from loss_scaled_adamw_gb300 import workloads as W
             import oracle
             oracle.build()
-            out["cpu_baseline"] = time_oracle(W.make(args.workload), args.cpu_seconds)
+            wl = W.make(args.workload)
+            # the oracle on every host core (its element functions on disjoint slices),
+            # and the plain single-threaded oracle beside it
+            out["cpu_baseline"] = time_oracle(wl, args.cpu_seconds, threads=host_cores())
+            out["cpu_baseline_single_core"] = time_oracle(wl, args.cpu_seconds)
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist

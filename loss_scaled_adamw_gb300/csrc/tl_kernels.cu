@@ -82,6 +82,13 @@ namespace {
 constexpr int kVec = 8;     // elements per vector access (16 B of a 16-bit stream)
 constexpr int kUnroll = 4;  // vectors in flight per thread in the accumulate/unscale kernels
 constexpr int kScalar = 8;  // elements per thread in flight on the scalar path (streams of unequal phase)
+// ... in the many-list kernel's forms for one or two lists, and for more lists
+#ifndef TL_SCALAR_FEW
+#define TL_SCALAR_FEW 2
+#endif
+#ifndef TL_SCALAR_MANY
+#define TL_SCALAR_MANY 1
+#endif
 
 // ---------------------------------------------------------------------------
 // 8-element vector access
@@ -632,8 +639,9 @@ __device__ __forceinline__ void finish_warp(const SumSq& sq, bool bad, int64_t c
 // (a fence per warp) and takes a ticket; the CTA holding the launch's last ticket
 // then reduces every partial slot of the table (those of earlier launches of the
 // pass included: they completed before this launch began) in a fixed order: thread
-// t sums the contiguous slots [t*per, (t+1)*per) with four interleaved
-// accumulators, then the fixed block reduction.  The order depends on the number of
+// t sums slots t, t + 256, t + 512, ... (coalesced, 8 loads in flight) into eight
+// accumulators, slot j going to accumulator (j / 256) mod 8, then the accumulators
+// in order and the fixed block reduction.  The order depends on the number of
 // slots only, not on the grid.  Nothing waits: the last CTA only runs once every
 // other CTA has published.  The ticket counter is reset by the last CTA.
 __device__ __noinline__ void finish_pass(DevState* __restrict__ st, const double* __restrict__ partials,
@@ -649,20 +657,20 @@ __device__ __noinline__ void finish_pass(DevState* __restrict__ st, const double
     __syncthreads();
     if (!last) return;
     __threadfence();
-    const int64_t per = (nslots + kThreads - 1) / kThreads;
-    const int64_t lo = min(nslots, per * threadIdx.x);
-    const int64_t hi = min(nslots, lo + per);
-    double a4[4] = {0.0, 0.0, 0.0, 0.0};
-    int64_t i = lo;
-    for (; i + 3 < hi; i += 4) {
-        double x[4];
+    constexpr int kBatch = 8;
+    double a8[8] = {0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0};
+    int64_t j = threadIdx.x;
+    for (; j + (kBatch - 1) * kThreads < nslots; j += kBatch * kThreads) {
+        double x[kBatch];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) x[q] = __ldcg(partials + i + q);   // written by other SMs
+        for (int q = 0; q < kBatch; ++q) x[q] = __ldcg(partials + j + q * kThreads);   // written by other SMs
 #pragma unroll
-        for (int q = 0; q < 4; ++q) a4[q] = __dadd_rn(a4[q], x[q]);
+        for (int q = 0; q < kBatch; ++q) a8[q & 7] = __dadd_rn(a8[q & 7], x[q]);
     }
-    double s = __dadd_rn(__dadd_rn(a4[0], a4[1]), __dadd_rn(a4[2], a4[3]));
-    for (; i < hi; ++i) s = __dadd_rn(s, __ldcg(partials + i));
+    for (int q = 0; j < nslots; j += kThreads, ++q) a8[q & 7] = __dadd_rn(a8[q & 7], __ldcg(partials + j));
+    double s = 0.0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s = __dadd_rn(s, a8[q]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s = __dadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
@@ -885,7 +893,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     // tail, or the whole segment without a vector part: with one or two lists,
     // S elements per thread loaded first, then finished in element order (more
     // lists already put that many loads in flight)
-    constexpr int S = KM <= kFewLists ? kScalar / 4 : 1;
+    constexpr int S = KM <= kFewLists ? TL_SCALAR_FEW : TL_SCALAR_MANY;
     int j = done + t;
     for (; S > 1 && j + (S - 1) * NT < len; j += S * NT) {
         float gx[S][KM], ax[S];
@@ -1257,19 +1265,24 @@ __device__ __forceinline__ float clip_coef(float norm, float max_norm) {
     return coef;
 }
 
-// What the scaler needs at the end of an AdamW launch (held by thread 0).
+// What the scaler needs at the end of an AdamW launch, kept in shared memory (so
+// that nothing of it stays live in registers across the element loops).
 struct AdamTail {
     double b1n, b2n;   // beta powers of the update in flight
     float coef;
     int skip;
 };
 
+__device__ __forceinline__ AdamTail& adam_tail() {
+    __shared__ AdamTail t;
+    return t;
+}
+
 // The per-step AdamW scalars (fp64 beta powers, bias corrections rounded to fp32
 // once, the clip coefficient from the device norm), computed by one thread and
 // shared through shared memory.  Returns true when the update is skipped (overflow
-// flag set).  Thread 0 keeps what the scaler needs in `tail`.
-__device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const AdamHP& hp, AdamConsts& out,
-                                            AdamTail& tail) {
+// flag set).  Thread 0 also leaves what the scaler needs in adam_tail().
+__device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const AdamHP& hp, AdamConsts& out) {
     __shared__ AdamConsts sk;
     __shared__ int skip;
     if (threadIdx.x == 0) {
@@ -1292,7 +1305,7 @@ __device__ __forceinline__ bool adam_consts(DevState* __restrict__ st, const Ada
         k.eps = hp.eps;
         k.coef = clip_coef(st->norm, hp.max_norm);
         sk = k;
-        tail = AdamTail{b1n, b2n, k.coef, f};
+        adam_tail() = AdamTail{b1n, b2n, k.coef, f};
     }
     __syncthreads();
     out = sk;
@@ -1335,7 +1348,7 @@ __device__ __forceinline__ void scaler_step(DevState* __restrict__ st, const Sca
     st->found_inf = 0;
 }
 
-__device__ __noinline__ void adam_finish(DevState* __restrict__ st, const ScalerParams& sp, const AdamTail& tail) {
+__device__ __noinline__ void adam_finish(DevState* __restrict__ st, const ScalerParams& sp) {
     __shared__ int last;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1347,7 +1360,7 @@ __device__ __noinline__ void adam_finish(DevState* __restrict__ st, const Scaler
     if (threadIdx.x != 0 || !last) return;
     __threadfence();
     st->adam_ticket = 0;
-    scaler_step(st, sp, tail);
+    scaler_step(st, sp, adam_tail());
 }
 
 template <int NT, int PDT>
@@ -1355,8 +1368,7 @@ __global__ void __launch_bounds__(kThreads, NT != kThreads ? TL_MINB_ADAM_GROUP 
 k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
         DevState* __restrict__ st, AdamHP hp, ScalerParams sp) {
     AdamConsts k;
-    AdamTail tail;
-    if (!adam_consts(st, hp, k, tail)) {
+    if (!adam_consts(st, hp, k)) {
         if (NT == kThreads) {
             for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
                 adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromAcc(ch));
@@ -1368,7 +1380,7 @@ k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
             }
         }
     }
-    if (sp.run) adam_finish(st, sp, tail);
+    if (sp.run) adam_finish(st, sp);
 }
 
 // The re-materialising AdamW pass: u of every element recomputed from the
@@ -1380,9 +1392,8 @@ k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
               DevState* __restrict__ st, AdamHP hp, ScalerParams sp, const __grid_constant__ GradTableMany inl,
               const __grid_constant__ ManyArgs a) {
     AdamConsts k;
-    AdamTail tail;
     const float inv_s = __fdiv_rn(1.0f, st->S);
-    if (!adam_consts(st, hp, k, tail)) {
+    if (!adam_consts(st, hp, k)) {
         if (NT == kThreads) {
             for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
                 adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
@@ -1394,7 +1405,7 @@ k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
             }
         }
     }
-    if (sp.run) adam_finish(st, sp, tail);
+    if (sp.run) adam_finish(st, sp);
 }
 
 // ---------------------------------------------------------------------------

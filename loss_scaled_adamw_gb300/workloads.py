@@ -21,6 +21,8 @@ Workloads (all seeded with 39):
   ragged_100k     100,000 tensors with lognormal sizes (median 512, max 2^20, ~400M total);
                   fp16 params and grads, grads N(0, 1e-2) * S with S = 2^14; k=2; inf in
                   one element of micro-batch 1 at step 2; 3 steps.
+  ragged_25k      25,000 tensors of the ragged list's size distribution (~100M parameters), as
+                  ragged_100k without the injected inf: a small case for counter captures.
   stream_64m      16 x 4M = 64M parameters, bf16, k=3: a small case of the same kernels for
                   hardware-counter captures (each list larger than L2).
   fp8_small       8-bit gradients ("Training at Scale" section 41.5: E4M3 codes with one fp32
@@ -133,6 +135,12 @@ def make(name: str) -> Workload:
     if name == "stream_64m_fp8":
         # the same small case with 8-bit gradients, k = 8 (lists of 80 MB each)
         return Workload(name, [1 << 22] * 16, "bf16", "e4m3b16", steps=2, k=8, grad_std=1e-3)
+    if name == "ragged_25k":
+        # a small case of the ragged list's kernels for counter captures: 25,000 tensors of
+        # the same size distribution, ~100M parameters (about 2.2 GB of device memory)
+        nm = ragged_numel(25_000, target_total=100_000_000)
+        return Workload(name, nm, "f16", "f16", steps=3, k=2, grad_std=1e-2, scaler_enabled=True,
+                        init_scale=2.0 ** 14, interval=2000, grads_prescaled=True)
     if name == "stream_64m":
         # a small case of the 1.24B workload's kernels for counter captures: every list
         # is larger than the 129 MB L2 while the whole case holds ~1.5 GB of HBM

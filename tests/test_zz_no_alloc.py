@@ -160,7 +160,11 @@ def test_no_alloc_matches_oracle_twice(case):
         u_ref, found, sumsq, norm, coef = _oracle_reference(flat, S, MAX_NORM)
         res = buf.cpu().numpy()
         u_gpu = np.concatenate([res[o:o + n] for o, n in zip(offs, NUMEL)])
-        assert np.array_equal(u_gpu.view(np.uint32), u_ref.view(np.uint32)), f"{case} call {call}: u differs"
+        # bit for bit, except that a NaN's payload is not fixed by IEEE arithmetic: NaN
+        # positions must agree
+        nan = np.isnan(u_ref)
+        assert np.array_equal(np.isnan(u_gpu), nan), f"{case} call {call}: NaN positions differ"
+        assert np.array_equal(u_gpu[~nan].view(np.uint32), u_ref[~nan].view(np.uint32)), f"{case} call {call}: u differs"
         assert got.found_inf == found, (case, call, got.found_inf, found)
         if not found:
             assert abs(got.sumsq - sumsq) <= 2e-6 * sumsq, (got.sumsq, sumsq)
