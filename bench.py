@@ -721,8 +721,8 @@ class SlicedOracle:
 
 def time_oracle(wl, seconds: float, steps=None, threads: int = 1):
     """Time the oracle's logical update on a contiguous sample of the workload sized for
-    about `seconds` of CPU time (at most 2^27 parameters per thread and 2^30 in all,
-    repeated over several logical updates when the cap binds, unless `steps` is given).
+    about `seconds` of CPU time (at most 2^27 parameters, repeated over several logical
+    updates when the cap binds, unless `steps` is given).
     threads = 1: the plain single-threaded oracle (tlo_step); threads > 1: its element
     functions on disjoint slices on that many host cores (SlicedOracle)."""
     import oracle
@@ -733,12 +733,13 @@ def time_oracle(wl, seconds: float, steps=None, threads: int = 1):
             return oracle.Oracle(master, p0, wl.param_dtype, wl.grad_dtype, numel=[master.size]), grads
         return SlicedOracle(master, p0, wl, threads), grads
 
-    n = (1 << 20) * threads
+    n = 1 << 20
     o, grads = make(n)
     t = time.perf_counter()
     o.step(grads, wl.counts(1), wl.max_norm)
     per_param = (time.perf_counter() - t) / n
-    n = int(min(max(seconds / per_param / (steps or 1), 1 << 20), (1 << 27) * threads, 1 << 30, wl.P))
+    # at most 2^27 parameters: drawing the sample's inputs costs more than stepping them
+    n = int(min(max(seconds / per_param / (steps or 1), 1 << 20), 1 << 27, wl.P))
     if steps is None:
         steps = max(1, int(round(seconds / (per_param * n))))
     o, grads = make(n)

@@ -114,8 +114,12 @@ struct tl_ctx {
     int grid_acc[kGradTypes][2][2] = {};
     int grid_uns[kGradTypes][3][2] = {};
     int grid_adam[3][2] = {};
-    int grid_many[kGradTypes][8][2] = {};
-    int grid_check[kGradTypes][2][2] = {};        // [grad dtype][few lists][part]
+    int grid_many[kGradTypes][16][2] = {};
+    int grid_check[kGradTypes][2][2][2] = {};     // [grad dtype][few lists][rotated form][part]
+    // the state lists hold tensors whose streams share no element phase (a gapped
+    // layout): the one- and two-list many-list launches take their rotated form,
+    // taking the gradient lists to follow the same kind of layout
+    bool gapped = false;
     // chunks per run of the kernels that write norm partials, per part: 1 where the
     // chunks are mostly full segments, kRun where they are short (one warp
     // reduction per run instead of per chunk)
@@ -434,6 +438,22 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
             iv.push_back({a, a + uintptr_t(numel[i]) * es});
         }
     }
+    // a gapped layout: some tensor's state streams are neither all on a 16-byte boundary
+    // nor all at one element phase modulo 8
+    bool gapped = false;
+    for (int64_t i = 0; i < ntensors && !gapped; ++i) {
+        if (numel[i] == 0) continue;
+        const uintptr_t a[5] = {reinterpret_cast<uintptr_t>(param[i]), reinterpret_cast<uintptr_t>(master[i]),
+                                reinterpret_cast<uintptr_t>(m[i]), reinterpret_cast<uintptr_t>(v[i]),
+                                reinterpret_cast<uintptr_t>(acc[i])};
+        bool al = true, same = true;
+        const uintptr_t r0 = (a[1] / 4) & 7;
+        for (int l = 0; l < 5; ++l) {
+            al = al && (a[l] & 15u) == 0;
+            same = same && ((a[l] / (l == 0 ? uintptr_t(pes) : 4)) & 7) == r0;
+        }
+        gapped = !al && !same;
+    }
     std::sort(iv.begin(), iv.end(), [](const Interval& a, const Interval& b) { return a.lo < b.lo; });
     for (size_t k = 1; k < iv.size(); ++k)
         if (iv[k].lo < iv[k - 1].hi) return TL_EINVAL;  // two tensors share memory
@@ -441,6 +461,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     tl_ctx* ctx = new (std::nothrow) tl_ctx();
     if (ctx == nullptr) return TL_ENOMEM;
     ctx->cfg = *cfg;
+    ctx->gapped = gapped;
     ctx->ntensors = ntensors;
     ctx->P = P;
     ctx->nchunks = nchunks;
@@ -590,8 +611,12 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
         ctx->grid_adam[pdt][part] = grid_for(ctx, blocks_per_sm(2, pdt, 0, small), n);
         for (int vr = 0; vr < 8; ++vr)
             ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr, small), nruns);
+        for (int vr = 8; vr < 16; ++vr)
+            ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr, small), nruns);
         for (int few = 0; few < 2; ++few) {
-            ctx->grid_check[gdt][few][part] = grid_for(ctx, blocks_per_sm(4, gdt, few ? 4 : 0, small), nruns);
+            for (int rt = 0; rt < 2; ++rt)
+                ctx->grid_check[gdt][few][rt][part] =
+                    grid_for(ctx, blocks_per_sm(4, gdt, (few ? 4 : 0) | (rt ? 8 : 0), small), nruns);
             ctx->grid_remat[pdt][gdt][few][part] =
                 grid_for(ctx, blocks_per_sm(5, pdt, gdt | (few ? 4 : 0), small), n);
         }
@@ -738,10 +763,10 @@ int tl_accumulate_many(tl_ctx* ctx, int k, const void* const* grads, const int64
         const bool f = first && j == 0;
         const bool l = last && j + kk == k;
         if (ctx->nchunks > 0) {
-            const int vr = (f ? 1 : 0) | (l ? 2 : 0) | (kk <= kFewLists ? 4 : 0);
+            const int vr = (f ? 1 : 0) | (l ? 2 : 0) | (kk <= kFewLists ? 4 : 0) | (ctx->gapped ? 8 : 0);
             const int gdt = ctx->cfg.grad_dtype;
             cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
-                return launch_accum_many(gdt, f, l, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a,
+                return launch_accum_many(gdt, f, l, small, ctx->gapped, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a,
                                          ctx->d_state, ctx->d_partials, fin_slots(ctx, lastl),
                                          ctx->grid_many[gdt][vr][small ? 1 : 0], s);
             });
@@ -786,8 +811,9 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
         const int gdt = ctx->cfg.grad_dtype;
         const int few = k <= kFewLists ? 1 : 0;
         cudaError_t e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
-            return launch_check_many(gdt, small, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a, ctx->d_state,
-                                     ctx->d_partials, fin_slots(ctx, lastl), ctx->grid_check[gdt][few][small ? 1 : 0],
+            return launch_check_many(gdt, small, ctx->gapped, ctx->d_chunks, c0, c1, ctx->run[small ? 1 : 0], inl, a,
+                                     ctx->d_state, ctx->d_partials, fin_slots(ctx, lastl),
+                                     ctx->grid_check[gdt][few][ctx->gapped ? 1 : 0][small ? 1 : 0],
                                      s);
         });
         if (e != cudaSuccess) return launch_fail(ctx, e, "many-list check launch");

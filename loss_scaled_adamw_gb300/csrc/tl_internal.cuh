@@ -142,13 +142,15 @@ cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chun
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
                            int64_t c1, int run, const GradTable& inl, const void* const* gtab, float w,
                            DevState* st, double* partials, int64_t fin, int grid, cudaStream_t s);
-cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
+// rot: the lists' element phases differ in some tensor (the rotated form, for the
+// one- and two-list launches of 16-bit lists over whole-CTA segments).
+cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, bool rot, const Chunk* chunks,
                               int64_t c0, int64_t c1, int run, const GradTableMany& inl,
                               const ManyArgs& a, DevState* st, double* partials, int64_t fin, int grid,
                               cudaStream_t s);
 // The many-list pass without the store of u (all lists of the update at once),
 // and the AdamW pass that recomputes u from the same lists.
-cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+cudaError_t launch_check_many(int gdt, bool small, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
                               int64_t fin, int grid, cudaStream_t s);
 // The AdamW launches compute the clip coefficient from the device norm and
@@ -171,8 +173,9 @@ cudaError_t launch_import(DevState* st, const double* sumsq, const int32_t* flag
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0
-// FIRST, bit 1 LAST, bit 2 at most kFewLists lists), 4 many-list pass without the
-// store (variant bit 2 as for kind 3), 5 re-materialising adamw (dt = param dtype,
+// FIRST, bit 1 LAST, bit 2 at most kFewLists lists, bit 3 the rotated form), 4
+// many-list pass without the store (variant bits 2, 3 as for kind 3), 5
+// re-materialising adamw (dt = param dtype,
 // variant bits 0-1 = grad dtype, bit 2 at most kFewLists lists).
 int blocks_per_sm(int kind, int dt, int variant, bool small);
 

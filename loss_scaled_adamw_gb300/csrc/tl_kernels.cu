@@ -89,6 +89,9 @@ constexpr int kScalar = 8;  // elements per thread in flight on the scalar path 
 #ifndef TL_SCALAR_MANY
 #define TL_SCALAR_MANY 1
 #endif
+#ifndef TL_SCALAR_FEW_GROUP
+#define TL_SCALAR_FEW_GROUP 2
+#endif
 
 // ---------------------------------------------------------------------------
 // 8-element vector access
@@ -389,6 +392,50 @@ __device__ __forceinline__ int edge_element(int t, int head, int done, int len) 
     if (t < head) return t;
     if (t >= 8 && t - 8 < len - done) return done + (t - 8);
     return -1;
+}
+
+// ---------------------------------------------------------------------------
+// Rotated vectors: 16-bit streams whose element phase differs from the frame's
+// (the read side of the many-list forms of one or two lists, whole-CTA segments).
+// The frame is one stream's alignment; lanes 0-30 of a warp work 31 consecutive
+// 8-element vectors o = head + 8 i, and lane 31 only helps.  For a stream whose
+// phase is d elements past the frame's (1..7), every lane loads the aligned 16-byte
+// block that starts d elements before its vector (lane 31: before the vector after
+// lane 30's), takes the next block from lane L + 1 with a shuffle, and picks its 8
+// values out of the two; so each block is loaded once and no load waits for
+// another.  A block that holds any byte of a tensor lies in that byte's memory
+// pages, so the loads are always safe, and the bytes outside the vector are never
+// used.  (The same on the AdamW pass, with its three rotated fp32 stores, measured
+// slower than element-by-element access: the shuffles and selects of four streams
+// outweigh the wider accesses.)
+// ---------------------------------------------------------------------------
+constexpr int kRotLanes = 31;   // vectors per warp and trip on the rotated path
+
+// 8 consecutive 16-bit values (as a raw 16-byte word) at element o of a stream d
+// elements (0..7) past the frame's phase, read-only data.  act: this lane works a
+// vector; ld: this lane's block is needed (its vector, or the vector before it,
+// exists).  Every lane of the warp calls this (shuffles).  The words from word d / 2
+// on are taken with a shifter of selects (a switch over d would cost branch
+// resolution on every vector), and an odd rotation joins half-words with funnel
+// shifts.
+__device__ __forceinline__ uint4 ld16_rot(const unsigned short* x, int o, int d, bool act, bool ld) {
+    if (d == 0) return act ? __ldg(reinterpret_cast<const uint4*>(x + o)) : make_uint4(0u, 0u, 0u, 0u);
+    uint4 b = make_uint4(0u, 0u, 0u, 0u), n;
+    if (ld) b = __ldg(reinterpret_cast<const uint4*>(x + o - d));   // 16-byte aligned
+    n.x = __shfl_down_sync(0xffffffffu, b.x, 1);
+    n.y = __shfl_down_sync(0xffffffffu, b.y, 1);
+    n.z = __shfl_down_sync(0xffffffffu, b.z, 1);
+    n.w = __shfl_down_sync(0xffffffffu, b.w, 1);
+    const uint32_t w[8] = {b.x, b.y, b.z, b.w, n.x, n.y, n.z, n.w};
+    const bool s2 = (d & 4) != 0, s1 = (d & 2) != 0;
+    uint32_t y[6], r[5];
+#pragma unroll
+    for (int k = 0; k < 6; ++k) y[k] = s2 ? w[k + 2] : w[k];
+#pragma unroll
+    for (int k = 0; k < 5; ++k) r[k] = s1 ? y[k + 1] : y[k];
+    const uint32_t sh = (d & 1) ? 16u : 0u;
+    return make_uint4(__funnelshift_r(r[0], r[1], sh), __funnelshift_r(r[1], r[2], sh), __funnelshift_r(r[2], r[3], sh),
+                      __funnelshift_r(r[3], r[4], sh));
 }
 
 template <int NT, int GDT, bool FIRST>
@@ -801,13 +848,42 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
 // of once per micro-batch.  FIRST: no partial sum in acc yet.  LAST: finish
 // with the unscale, overflow check and squared-norm partial of a3.
 // ---------------------------------------------------------------------------
-template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
+// acc = w_0 g_0 + w_1 g_1 + ... (per element in list order) over one 8-element vector
+// of each of the kk lists, then (LAST) the unscale and the overflow / squared-norm
+// bookkeeping of the last micro-batch
+template <int GDT, bool FIRST, bool LAST, int KM>
+__device__ __forceinline__ void mix_lists(const typename GradRaw<GDT>::T (&raw)[KM], const ManyArgs& a, int kk,
+                                          float inv_s, SumSq& sq, bool& bad, float (&ax)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
+                      : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
+#pragma unroll
+    for (int q = 1; q < KM; ++q)
+        if (q < kk) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
+        }
+    if (LAST) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            ax[e] = __fmul_rn(ax[e], inv_s);
+            bad |= !isfinite(ax[e]);
+        }
+        sq.vec8(ax);
+    }
+}
+
+template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE, bool ROT>
 __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradTableMany& inl, const ManyArgs& a,
                                              float inv_s, SumSq& sq, bool& bad) {
     const int kk = a.k;
     float* __restrict__ acc0 = ch.acc;
     const char* g[KM];
-    const float* gs[KM];  // block scales (8-bit gradients)
+    // 8-bit gradients: the block scales of list q start soff bytes after its codes (the
+    // same offset for every list: it depends on the tensor and the segment only)
+    const int64_t soff = GDT == kE4M3 ? ch.gscale - ch.start + (ch.start >> 2) : 0;
+    auto gs = [&](int q) { return GDT == kE4M3 ? reinterpret_cast<const float*>(g[q] + soff) : nullptr; };
     // without the store of u the accumulation buffer is not touched: the lists
     // alone decide the vector plan
     bool al = !STORE || aligned16(acc0);
@@ -818,13 +894,11 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         if (q < kk) {
             const void* base = a.tabs[q] != nullptr ? a.tabs[q][ch.tensor] : inl.p[q * a.ntensors + ch.tensor];
             g[q] = static_cast<const char*>(base) + ch.start * Grad<GDT>::kBytes;
-            gs[q] = grad_scales<GDT>(base, ch);
             if (!STORE && q == 0) r = ephase<Grad<GDT>::kBytes>(g[0]);
             al = al && aligned16(g[q]);
             same = same && ephase<Grad<GDT>::kBytes>(g[q]) == r;
         } else {
             g[q] = nullptr;
-            gs[q] = nullptr;
         }
     }
     const int len = ch.len;
@@ -832,35 +906,48 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     if (al) pl = VecPlan{0, true, !STORE || aligned32(acc0)};
     else if (same) pl = VecPlan{(8 - r) & 7, true, true};
     if (GDT == kE4M3 && pl.head != 0) pl.vec = false;  // an 8-bit vector must not straddle two blocks
+    // streams of unequal phase (16-bit lists, whole-CTA segments): rotated vectors in
+    // the frame of the accumulation buffer (or of list 0 when it is not written)
+    constexpr bool kRotForm = ROT && NT == kThreads && KM <= kFewLists && (GDT == kBF16 || GDT == kF16);
+    const bool rot = kRotForm && !pl.vec;
+    const int fr = STORE ? ephase<4>(acc0) : ephase<2>(g[0]);
+    if (rot) pl = VecPlan{(8 - fr) & 7, true, true};
     int head = 0, done = 0;
-    if (pl.vec) {
+    if constexpr (kRotForm) {
+      if (rot) {
+        head = min(pl.head, len);
+        const int nv = (len - head) / kVec;
+        const int lane = t & 31;
+        int dq[KM];
+#pragma unroll
+        for (int q = 0; q < KM; ++q) dq[q] = q < kk ? (ephase<2>(g[q]) - fr) & 7 : 0;
+        for (int base = (t >> 5) * kRotLanes; base < nv; base += (NT / 32) * kRotLanes) {   // warp-uniform trips
+            const int i = base + lane;
+            const bool act = lane < kRotLanes && i < nv;
+            const bool ld = i <= nv;
+            const int o = head + i * kVec;
+            typename GradRaw<GDT>::T raw[KM];
+#pragma unroll
+            for (int q = 0; q < KM; ++q)
+                if (q < kk) raw[q] = ld16_rot(reinterpret_cast<const unsigned short*>(g[q]), o, dq[q], act, ld);
+            if (act) {
+                float ax[8];
+                if (!FIRST) ld8_f32(acc0 + o, ax, true);
+                mix_lists<GDT, FIRST, LAST>(raw, a, kk, inv_s, sq, bad, ax);
+                if (STORE) st8_f32(acc0 + o, ax, true);
+            }
+        }
+        done = head + nv * kVec;
+      }
+    }
+    if (!rot && pl.vec) {
         head = min(pl.head, len);
         const bool wide = pl.wide;
         float* __restrict__ acc = acc0 + head;
         const int gofs = head * Grad<GDT>::kBytes;
         const int nv = (len - head) / kVec;
-        // acc = w_0 g_0 + w_1 g_1 + ... (per element in list order), then unscale
-        // and the overflow / squared-norm bookkeeping of the last micro-batch
-        auto mix = [&](const auto& raw, float (&ax)[8]) {
-            constexpr int kq = sizeof(raw) / sizeof(raw[0]);  // lists this form can hold
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
-                              : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
-#pragma unroll
-            for (int q = 1; q < kq; ++q)
-                if (q < kk) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
-                }
-            if (LAST) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ax[e] = __fmul_rn(ax[e], inv_s);
-                    bad |= !isfinite(ax[e]);
-                }
-                sq.vec8(ax);
-            }
+        auto mix = [&](const typename GradRaw<GDT>::T (&raw)[KM], float (&ax)[8]) {
+            mix_lists<GDT, FIRST, LAST>(raw, a, kk, inv_s, sq, bad, ax);
         };
         for (int i = t; i < nv; i += NT) {
             // all kk loads in flight first; each stream's 8 values are unpacked
@@ -868,7 +955,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
             typename GradRaw<GDT>::T raw[KM];
 #pragma unroll
             for (int q = 0; q < KM; ++q)
-                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q] + gofs, int64_t(i) * kVec, gs[q]);
+                if (q < kk) raw[q] = GradRaw<GDT>::ld(g[q] + gofs, int64_t(i) * kVec, gs(q));
             float ax[8];
             if (!FIRST) ld8_f32(acc + i * kVec, ax, wide);
             mix(raw, ax);
@@ -877,11 +964,11 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         done = head + nv * kVec;
     }
     auto one = [&](int j) {
-        float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j, gs[0]))
-                        : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j, gs[0]), acc0[j]);
+        float v = FIRST ? __fmul_rn(a.w[0], Grad<GDT>::ld1(g[0], j, gs(0)))
+                        : __fmaf_rn(a.w[0], Grad<GDT>::ld1(g[0], j, gs(0)), acc0[j]);
 #pragma unroll
         for (int q = 1; q < KM; ++q)
-            if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j, gs[q]), v);
+            if (q < kk) v = __fmaf_rn(a.w[q], Grad<GDT>::ld1(g[q], j, gs(q)), v);
         if (LAST) {
             v = __fmul_rn(v, inv_s);
             bad |= !isfinite(v);
@@ -893,7 +980,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     // tail, or the whole segment without a vector part: with one or two lists,
     // S elements per thread loaded first, then finished in element order (more
     // lists already put that many loads in flight)
-    constexpr int S = KM <= kFewLists ? TL_SCALAR_FEW : TL_SCALAR_MANY;
+    constexpr int S = KM <= kFewLists ? (NT == kThreads ? TL_SCALAR_FEW : TL_SCALAR_FEW_GROUP) : TL_SCALAR_MANY;
     int j = done + t;
     for (; S > 1 && j + (S - 1) * NT < len; j += S * NT) {
         float gx[S][KM], ax[S];
@@ -901,7 +988,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
         for (int e = 0; e < S; ++e) {
 #pragma unroll
             for (int q = 0; q < KM; ++q)
-                if (q < kk) gx[e][q] = Grad<GDT>::ld1(g[q], j + e * NT, gs[q]);
+                if (q < kk) gx[e][q] = Grad<GDT>::ld1(g[q], j + e * NT, gs(q));
             if (!FIRST) ax[e] = acc0[j + e * NT];
         }
 #pragma unroll
@@ -921,10 +1008,12 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     for (; j < len; j += NT) one(j);
 }
 
-template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE>
+// ROT: the form for lists of unequal element phase (rotated 16-bit loads; the
+// registers they need cost it one resident CTA per SM).
+template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE, bool ROT>
 __global__ void __launch_bounds__(kThreads, NT != kThreads ? (GDT == kF32 || KM > kFewLists ? 1 : GDT == kE4M3 ? TL_MINB_GROUP_FEW - 1 : TL_MINB_GROUP_FEW)
                                             : GDT == kF32 ? 2
-                                            : KM <= kFewLists ? (GDT == kE4M3 || (LAST && !FIRST) ? TL_MINB_FEW - 1 : TL_MINB_FEW)
+                                            : KM <= kFewLists ? (GDT == kE4M3 || (LAST && !FIRST) || ROT ? TL_MINB_FEW - 1 : TL_MINB_FEW)
                                             : GDT == kE4M3 ? TL_MINB_MANY_E4M3 : TL_MINB_MANY)
 k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
              const __grid_constant__ GradTableMany inl,
@@ -935,9 +1024,9 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
     bool bad = false;
     for_runs(c0, c1, run, [&](int64_t c) {
         if (NT == kThreads)
-            many_segment<kThreads, GDT, FIRST, LAST, KM, STORE>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
+            many_segment<kThreads, GDT, FIRST, LAST, KM, STORE, ROT>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
         else
-            many_segment<32, GDT, FIRST, LAST, KM, STORE>(group_segment(chunks, c0, c), threadIdx.x & 31, inl, a,
+            many_segment<32, GDT, FIRST, LAST, KM, STORE, false>(group_segment(chunks, c0, c), threadIdx.x & 31, inl, a,
                                                           inv_s, sq, bad);
     }, [&](int64_t r0) {
         if (LAST) {
@@ -1497,47 +1586,63 @@ UnsFn uns_fn_nt(int gdt, int mode) {
 
 UnsFn uns_fn(int gdt, int mode, bool small) { return small ? uns_fn_nt<32>(gdt, mode) : uns_fn_nt<kThreads>(gdt, mode); }
 
-template <int NT, int GDT, int KM>
+template <int NT, int GDT, int KM, bool ROT>
 ManyFn many_fn_km(bool first, bool last) {
-    if (first) return last ? k_accum_many<NT, GDT, true, true, KM, true> : k_accum_many<NT, GDT, true, false, KM, true>;
-    return last ? k_accum_many<NT, GDT, false, true, KM, true> : k_accum_many<NT, GDT, false, false, KM, true>;
+    if (first)
+        return last ? k_accum_many<NT, GDT, true, true, KM, true, ROT> : k_accum_many<NT, GDT, true, false, KM, true, ROT>;
+    return last ? k_accum_many<NT, GDT, false, true, KM, true, ROT> : k_accum_many<NT, GDT, false, false, KM, true, ROT>;
+}
+// the rotated form exists for whole-CTA segments of one or two 16-bit lists only
+template <int NT, int GDT>
+constexpr bool has_rot() {
+    return NT == kThreads && (GDT == kBF16 || GDT == kF16);
 }
 template <int NT, int GDT>
-ManyFn many_fn_dt(bool first, bool last, bool few) {
-    return few ? many_fn_km<NT, GDT, kFewLists>(first, last) : many_fn_km<NT, GDT, kMaxMany>(first, last);
+ManyFn many_fn_dt(bool first, bool last, bool few, bool rot) {
+    if (!few) return many_fn_km<NT, GDT, kMaxMany, false>(first, last);
+    if constexpr (has_rot<NT, GDT>()) {
+        if (rot) return many_fn_km<NT, GDT, kFewLists, true>(first, last);
+    }
+    return many_fn_km<NT, GDT, kFewLists, false>(first, last);
 }
 
 template <int NT>
-ManyFn many_fn_nt(int gdt, bool first, bool last, bool few) {
+ManyFn many_fn_nt(int gdt, bool first, bool last, bool few, bool rot) {
     switch (gdt) {
-        case kBF16: return many_fn_dt<NT, kBF16>(first, last, few);
-        case kF16: return many_fn_dt<NT, kF16>(first, last, few);
-        case kF32: return many_fn_dt<NT, kF32>(first, last, few);
-        case kE4M3: return many_fn_dt<NT, kE4M3>(first, last, few);
+        case kBF16: return many_fn_dt<NT, kBF16>(first, last, few, rot);
+        case kF16: return many_fn_dt<NT, kF16>(first, last, few, rot);
+        case kF32: return many_fn_dt<NT, kF32>(first, last, few, rot);
+        case kE4M3: return many_fn_dt<NT, kE4M3>(first, last, few, rot);
         default: return nullptr;
     }
 }
 
-ManyFn many_fn(int gdt, bool first, bool last, bool small, bool few) {
-    return small ? many_fn_nt<32>(gdt, first, last, few) : many_fn_nt<kThreads>(gdt, first, last, few);
+ManyFn many_fn(int gdt, bool first, bool last, bool small, bool few, bool rot) {
+    return small ? many_fn_nt<32>(gdt, first, last, few, rot) : many_fn_nt<kThreads>(gdt, first, last, few, rot);
 }
 
 // the many-list pass without the store of u (first and last micro-batch at once)
+template <int NT, int GDT>
+ManyFn check_fn_dt(bool few, bool rot) {
+    if (!few) return k_accum_many<NT, GDT, true, true, kMaxMany, false, false>;
+    if constexpr (has_rot<NT, GDT>()) {
+        if (rot) return k_accum_many<NT, GDT, true, true, kFewLists, false, true>;
+    }
+    return k_accum_many<NT, GDT, true, true, kFewLists, false, false>;
+}
 template <int NT>
-ManyFn check_fn_nt(int gdt, bool few) {
+ManyFn check_fn_nt(int gdt, bool few, bool rot) {
     switch (gdt) {
-        case kBF16: return few ? k_accum_many<NT, kBF16, true, true, kFewLists, false>
-                               : k_accum_many<NT, kBF16, true, true, kMaxMany, false>;
-        case kF16: return few ? k_accum_many<NT, kF16, true, true, kFewLists, false>
-                              : k_accum_many<NT, kF16, true, true, kMaxMany, false>;
-        case kF32: return few ? k_accum_many<NT, kF32, true, true, kFewLists, false>
-                              : k_accum_many<NT, kF32, true, true, kMaxMany, false>;
-        case kE4M3: return few ? k_accum_many<NT, kE4M3, true, true, kFewLists, false>
-                               : k_accum_many<NT, kE4M3, true, true, kMaxMany, false>;
+        case kBF16: return check_fn_dt<NT, kBF16>(few, rot);
+        case kF16: return check_fn_dt<NT, kF16>(few, rot);
+        case kF32: return check_fn_dt<NT, kF32>(few, rot);
+        case kE4M3: return check_fn_dt<NT, kE4M3>(few, rot);
         default: return nullptr;
     }
 }
-ManyFn check_fn(int gdt, bool small, bool few) { return small ? check_fn_nt<32>(gdt, few) : check_fn_nt<kThreads>(gdt, few); }
+ManyFn check_fn(int gdt, bool small, bool few, bool rot) {
+    return small ? check_fn_nt<32>(gdt, few, rot) : check_fn_nt<kThreads>(gdt, few, rot);
+}
 
 using RematFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP, ScalerParams, const GradTableMany,
                          const ManyArgs);
@@ -1596,10 +1701,10 @@ cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, const Chunk* chunks,
+cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, bool rot, const Chunk* chunks,
                               int64_t c0, int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a,
                               DevState* st, double* partials, int64_t fin, int grid, cudaStream_t s) {
-    ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists);
+    ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, last ? fin : 0);
     return cudaGetLastError();
@@ -1613,10 +1718,10 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
     return cudaGetLastError();
 }
 
-cudaError_t launch_check_many(int gdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+cudaError_t launch_check_many(int gdt, bool small, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
                               int64_t fin, int grid, cudaStream_t s) {
-    ManyFn f = check_fn(gdt, small, a.k <= kFewLists);
+    ManyFn f = check_fn(gdt, small, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, fin);
     return cudaGetLastError();
@@ -1665,8 +1770,9 @@ int blocks_per_sm(int kind, int dt, int variant, bool small) {
     else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn(dt, variant, small));
     else if (kind == 2) f = reinterpret_cast<const void*>(adam_fn(dt, small));
     else if (kind == 3)
-        f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0, small, (variant & 4) != 0));
-    else if (kind == 4) f = reinterpret_cast<const void*>(check_fn(dt, small, (variant & 4) != 0));
+        f = reinterpret_cast<const void*>(many_fn(dt, (variant & 1) != 0, (variant & 2) != 0, small, (variant & 4) != 0,
+                                                  (variant & 8) != 0));
+    else if (kind == 4) f = reinterpret_cast<const void*>(check_fn(dt, small, (variant & 4) != 0, (variant & 8) != 0));
     else if (kind == 5) f = reinterpret_cast<const void*>(remat_fn(dt, variant & 3, small, (variant & 4) != 0));
     if (f == nullptr) return 1;
     int n = 0;
