@@ -92,6 +92,10 @@ constexpr int kScalar = 8;  // elements per thread in flight on the scalar path 
 #ifndef TL_SCALAR_FEW_GROUP
 #define TL_SCALAR_FEW_GROUP 2
 #endif
+// 8-bit lists: products and weighted sums two fp32 lanes per instruction
+#ifndef TL_PAIRS
+#define TL_PAIRS 1
+#endif
 
 // ---------------------------------------------------------------------------
 // 8-element vector access
@@ -851,19 +855,52 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
 // acc = w_0 g_0 + w_1 g_1 + ... (per element in list order) over one 8-element vector
 // of each of the kk lists, then (LAST) the unscale and the overflow / squared-norm
 // bookkeeping of the last micro-batch
+// Two fp32 lanes per instruction (sm_100+ packed fp32): each lane is one IEEE
+// operation rounded to nearest even, the same result as the scalar forms.
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float& d0,
+                                        float& d1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 template <int GDT, bool FIRST, bool LAST, int KM>
 __device__ __forceinline__ void mix_lists(const typename GradRaw<GDT>::T (&raw)[KM], const ManyArgs& a, int kk,
                                           float inv_s, SumSq& sq, bool& bad, float (&ax)[8]) {
+    if constexpr (GDT == kE4M3 && TL_PAIRS) {
+        // 8-bit lists (issue-bound): decode two codes at a time and take the scale
+        // product and the weighted sum two lanes per instruction
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-        ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
-                      : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
+        for (int q = 0; q < KM; ++q)
+            if (q == 0 || q < kk) {
 #pragma unroll
-    for (int q = 1; q < KM; ++q)
-        if (q < kk) {
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t wd = k < 2 ? raw[q].c.x : raw[q].c.y;
+                    float lo, hi;
+                    unpack_e4m3x2((k & 1) ? (wd >> 16) : wd, lo, hi);
+                    mul2_rn(lo, hi, raw[q].s, raw[q].s, lo, hi);      // code value x block scale
+                    if (q == 0 && FIRST) mul2_rn(a.w[0], a.w[0], lo, hi, ax[2 * k], ax[2 * k + 1]);
+                    else fma2_rn(a.w[q], a.w[q], lo, hi, ax[2 * k], ax[2 * k + 1], ax[2 * k], ax[2 * k + 1]);
+                }
+            }
+    } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
-        }
+        for (int e = 0; e < 8; ++e)
+            ax[e] = FIRST ? __fmul_rn(a.w[0], GradRaw<GDT>::at(raw[0], e))
+                          : __fmaf_rn(a.w[0], GradRaw<GDT>::at(raw[0], e), ax[e]);
+#pragma unroll
+        for (int q = 1; q < KM; ++q)
+            if (q < kk) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ax[e] = __fmaf_rn(a.w[q], GradRaw<GDT>::at(raw[q], e), ax[e]);
+            }
+    }
     if (LAST) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
