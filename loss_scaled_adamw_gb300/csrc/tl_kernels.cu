@@ -92,7 +92,7 @@ constexpr int kScalar = 8;  // elements per thread in flight on the scalar path 
 #ifndef TL_SCALAR_FEW_GROUP
 #define TL_SCALAR_FEW_GROUP 2
 #endif
-// 8-bit lists: products and weighted sums two fp32 lanes per instruction
+// many-list pass: products and weighted sums two fp32 lanes per instruction
 #ifndef TL_PAIRS
 #define TL_PAIRS 1
 #endif
@@ -597,7 +597,9 @@ __device__ __forceinline__ float unscale1(float a, float gj, float w, float inv_
 // fp32 norm by an ulp, hence the clip coefficient, hence masters close to zero
 // by many ulps.)  A vector holding a larger or infinite value is summed in fp64
 // instead, so the total is infinite exactly when some fp32 square is; NaN
-// propagates through the float-float path.
+// propagates through the float-float path, and a NaN accumulator at the end of
+// a warp's run raises the overflow flag (so the vector path checks no value one
+// by one unless the vector holds a large one).
 // d + q in fp64 for the rare large-value case of the squared-norm sum, kept out
 // of line: inlined into a per-element loop it may be if-converted, and then every
 // element issues the fp64 instructions, which this GPU runs at a small fraction
@@ -606,36 +608,95 @@ __device__ __noinline__ double dadd_out_of_line(double d, float q) {
     return __dadd_rn(d, static_cast<double>(q));
 }
 
-struct SumSq {
-    float hi = 0.0f;
-    float lo = 0.0f;
+// Two fp32 lanes per instruction (sm_100 and later): each lane rounds as the
+// scalar instruction does.
+__device__ __forceinline__ void add2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+    asm("{ .reg .b64 a, b, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %5}; add.rn.f32x2 d, a, b; mov.b64 {%0, %1}, d; }"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+    asm("{ .reg .b64 a, b, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %5}; sub.rn.f32x2 d, a, b; mov.b64 {%0, %1}, d; }"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+    asm("{ .reg .b64 a, b, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %5}; mul.rn.f32x2 d, a, b; mov.b64 {%0, %1}, d; }"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float& d0, float& d1) {
+    asm("{ .reg .b64 a, b, c, d; mov.b64 a, {%2, %3}; mov.b64 b, {%4, %5}; mov.b64 c, {%6, %7}; "
+        "fma.rn.f32x2 d, a, b, c; mov.b64 {%0, %1}, d; }"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// P = false: one float-float accumulator (hi0, lo0) per lane.  P = true: two,
+// (hi0, lo0) for the even and (hi1, lo1) for the odd elements of the lane's
+// vectors, updated together by two-lane instructions (about half the
+// instructions per element, two more registers; a scalar element goes to the
+// first).
+template <bool P>
+struct SumSqT {
+    float hi0 = 0.0f, hi1 = 0.0f;
+    float lo0 = 0.0f, lo1 = 0.0f;
     double d = 0.0;   // vectors with large values only
     bool big = false;
 
     __device__ __forceinline__ void add(float q) {
-        const float s = __fadd_rn(hi, q);
-        const float bb = __fsub_rn(s, hi);
-        const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(q, bb));  // hi + q - s, exactly
-        hi = s;
-        lo = __fadd_rn(lo, err);
+        const float s = __fadd_rn(hi0, q);
+        const float bb = __fsub_rn(s, hi0);
+        const float err = __fadd_rn(__fsub_rn(hi0, __fsub_rn(s, bb)), __fsub_rn(q, bb));  // hi + q - s, exactly
+        hi0 = s;
+        lo0 = __fadd_rn(lo0, err);
     }
-    __device__ __forceinline__ void vec8(const float (&u)[8]) {
-        float q[8];
-        float mx = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            q[e] = __fmul_rn(u[e], u[e]);
-            mx = fmaxf(mx, fabsf(u[e]));
+    // TwoSum of (q0, q1) into the two accumulators (P), or of q0 then q1 into the one
+    __device__ __forceinline__ void add2(float q0, float q1) {
+        if constexpr (P) {
+            float s0, s1, b0, b1, t0, t1, e0, e1, f0, f1;
+            add2_rn(hi0, hi1, q0, q1, s0, s1);
+            sub2_rn(s0, s1, hi0, hi1, b0, b1);
+            sub2_rn(s0, s1, b0, b1, t0, t1);
+            sub2_rn(hi0, hi1, t0, t1, e0, e1);
+            sub2_rn(q0, q1, b0, b1, f0, f1);
+            add2_rn(e0, e1, f0, f1, e0, e1);
+            hi0 = s0;
+            hi1 = s1;
+            add2_rn(lo0, lo1, e0, e1, lo0, lo1);
+        } else {
+            add(q0);
+            add(q1);
         }
-        if (mx >= 72057594037927936.0f) {  // 2^56 (or inf)
+    }
+    // Eight values of u.  When every |u| is below 2^56 their squares (below 2^112,
+    // so a lane's sum stays finite) go to the float-float accumulators; a NaN among
+    // them is not looked for here: it makes the accumulator NaN, which nan() reports
+    // when the warp finishes.  Otherwise (a large or infinite value, or a NaN beside
+    // one) the squares are summed in fp64 and each value is checked: bad is raised
+    // for a value that is not finite.
+    __device__ __forceinline__ void vec8(const float (&u)[8], bool& bad) {
+        const float um = fmaxf(fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])), fmaxf(fabsf(u[2]), fabsf(u[3]))),
+                               fmaxf(fmaxf(fabsf(u[4]), fabsf(u[5])), fmaxf(fabsf(u[6]), fabsf(u[7]))));
+        if (!(um < 72057594037927936.0f)) {  // 2^56 or inf (fmaxf drops NaN unless all are)
             big = true;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) d = __dadd_rn(d, static_cast<double>(q[e]));
+            for (int e = 0; e < 8; ++e) {
+                bad |= !isfinite(u[e]);
+                d = __dadd_rn(d, static_cast<double>(__fmul_rn(u[e], u[e])));
+            }
             return;
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) add(q[e]);
+        for (int e = 0; e < 8; e += 2) {
+            float q0, q1;
+            if constexpr (P) {
+                mul2_rn(u[e], u[e + 1], u[e], u[e + 1], q0, q1);
+            } else {
+                q0 = __fmul_rn(u[e], u[e]);
+                q1 = __fmul_rn(u[e + 1], u[e + 1]);
+            }
+            add2(q0, q1);
+        }
     }
+    // A NaN reached the float-float accumulators (once NaN, hi stays NaN).
+    __device__ __forceinline__ bool nan() const { return isnan(hi0) || (P && isnan(hi1)); }
     __device__ __forceinline__ void one(float u) {
         const float q = __fmul_rn(u, u);
         if (fabsf(u) >= 72057594037927936.0f) {
@@ -646,6 +707,7 @@ struct SumSq {
         add(q);
     }
 };
+using SumSq = SumSqT<false>;
 
 // Fixed-order reduction of a SumSq within a warp: a float-float butterfly
 // (TwoSum gives the same exact error term in both lanes of a pair, so every lane
@@ -653,8 +715,16 @@ struct SumSq {
 // warp writes its own partial (kGroup partials per chunk), so finishing a chunk
 // needs no block barrier; the partial of warp w of chunk c is always the same
 // elements' sum, whatever the grid.
-__device__ __forceinline__ double warp_sumsq(const SumSq& acc) {
-    float hi = acc.hi, lo = acc.lo;
+template <bool P>
+__device__ __forceinline__ double warp_sumsq(const SumSqT<P>& acc) {
+    float hi = acc.hi0, lo = acc.lo0;
+    if (P) {
+        const float s = __fadd_rn(acc.hi0, acc.hi1);
+        const float bb = __fsub_rn(s, acc.hi0);
+        const float err = __fadd_rn(__fsub_rn(acc.hi0, __fsub_rn(s, bb)), __fsub_rn(acc.hi1, bb));
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(acc.lo0, acc.lo1), err);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
@@ -676,9 +746,10 @@ __device__ __forceinline__ double warp_sumsq(const SumSq& acc) {
 
 // Write warp w's partial of chunk c and raise the overflow flag if any lane saw a
 // non-finite value.
-__device__ __forceinline__ void finish_warp(const SumSq& sq, bool bad, int64_t c, DevState* st, double* partials) {
+template <bool P>
+__device__ __forceinline__ void finish_warp(const SumSqT<P>& sq, bool bad, int64_t c, DevState* st, double* partials) {
     const double part = warp_sumsq(sq);
-    const bool any_bad = __any_sync(0xffffffffu, bad);
+    const bool any_bad = __any_sync(0xffffffffu, bad || sq.nan());
     if ((threadIdx.x & 31) == 0) {
         partials[c * kGroup + (threadIdx.x >> 5)] = part;
         if (any_bad) st->found_inf = 1;
@@ -772,11 +843,9 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < 8; ++e)
                     ax[u][e] = unscale1<MODE>(kReadAcc ? ax[u][e] : 0.0f, kReadG ? gx[u][e] : 0.0f, w, inv_s);
-                    bad |= !isfinite(ax[u][e]);
-                }
-                sq.vec8(ax[u]);
+                sq.vec8(ax[u], bad);
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) st8_f32(acc + (i + u * NT) * kVec, ax[u], wide);
@@ -786,11 +855,8 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
             if (kReadG) Grad<GDT>::ld8(g, int64_t(i) * kVec, gx, sc);
             if (kReadAcc) ld8_f32(acc + i * kVec, ax, wide);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                ax[e] = unscale1<MODE>(kReadAcc ? ax[e] : 0.0f, kReadG ? gx[e] : 0.0f, w, inv_s);
-                bad |= !isfinite(ax[e]);
-            }
-            sq.vec8(ax);
+            for (int e = 0; e < 8; ++e) ax[e] = unscale1<MODE>(kReadAcc ? ax[e] : 0.0f, kReadG ? gx[e] : 0.0f, w, inv_s);
+            sq.vec8(ax, bad);
             st8_f32(acc + i * kVec, ax, wide);
         }
         done = head + nv * kVec;
@@ -855,24 +921,9 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
 // acc = w_0 g_0 + w_1 g_1 + ... (per element in list order) over one 8-element vector
 // of each of the kk lists, then (LAST) the unscale and the overflow / squared-norm
 // bookkeeping of the last micro-batch
-// Two fp32 lanes per instruction (sm_100+ packed fp32): each lane is one IEEE
-// operation rounded to nearest even, the same result as the scalar forms.
-__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-__device__ __forceinline__ void fma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float& d0,
-                                        float& d1) {
-    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-
-template <int GDT, bool FIRST, bool LAST, int KM>
+template <int GDT, bool FIRST, bool LAST, int KM, class SQ>
 __device__ __forceinline__ void mix_lists(const typename GradRaw<GDT>::T (&raw)[KM], const ManyArgs& a, int kk,
-                                          float inv_s, SumSq& sq, bool& bad, float (&ax)[8]) {
+                                          float inv_s, SQ& sq, bool& bad, float (&ax)[8]) {
     if constexpr (GDT == kE4M3 && TL_PAIRS) {
         // 8-bit lists (issue-bound): decode two codes at a time and take the scale
         // product and the weighted sum two lanes per instruction
@@ -889,6 +940,22 @@ __device__ __forceinline__ void mix_lists(const typename GradRaw<GDT>::T (&raw)[
                     else fma2_rn(a.w[q], a.w[q], lo, hi, ax[2 * k], ax[2 * k + 1], ax[2 * k], ax[2 * k + 1]);
                 }
             }
+    } else if constexpr (TL_PAIRS) {
+        // the weighted sum two lanes per instruction (elements 2k and 2k + 1)
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const float x0 = GradRaw<GDT>::at(raw[0], e), x1 = GradRaw<GDT>::at(raw[0], e + 1);
+            if (FIRST) mul2_rn(a.w[0], a.w[0], x0, x1, ax[e], ax[e + 1]);
+            else fma2_rn(a.w[0], a.w[0], x0, x1, ax[e], ax[e + 1], ax[e], ax[e + 1]);
+        }
+#pragma unroll
+        for (int q = 1; q < KM; ++q)
+            if (q < kk) {
+#pragma unroll
+                for (int e = 0; e < 8; e += 2)
+                    fma2_rn(a.w[q], a.w[q], GradRaw<GDT>::at(raw[q], e), GradRaw<GDT>::at(raw[q], e + 1), ax[e],
+                            ax[e + 1], ax[e], ax[e + 1]);
+            }
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -903,17 +970,14 @@ __device__ __forceinline__ void mix_lists(const typename GradRaw<GDT>::T (&raw)[
     }
     if (LAST) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            ax[e] = __fmul_rn(ax[e], inv_s);
-            bad |= !isfinite(ax[e]);
-        }
-        sq.vec8(ax);
+        for (int e = 0; e < 8; e += 2) mul2_rn(ax[e], ax[e + 1], inv_s, inv_s, ax[e], ax[e + 1]);
+        sq.vec8(ax, bad);
     }
 }
 
-template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE, bool ROT>
+template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE, bool ROT, class SQ>
 __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradTableMany& inl, const ManyArgs& a,
-                                             float inv_s, SumSq& sq, bool& bad) {
+                                             float inv_s, SQ& sq, bool& bad) {
     const int kk = a.k;
     float* __restrict__ acc0 = ch.acc;
     const char* g[KM];
@@ -1057,7 +1121,9 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials,
              int64_t fin) {
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
-    SumSq sq;
+    // two accumulators in the whole-CTA check pass of one or two lists (5-6 % faster
+    // there: it is issue-bound); the other forms keep one, as two would cost them spills
+    SumSqT<(NT == kThreads && KM <= kFewLists && !STORE)> sq;
     bool bad = false;
     for_runs(c0, c1, run, [&](int64_t c) {
         if (NT == kThreads)
@@ -1068,7 +1134,7 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
     }, [&](int64_t r0) {
         if (LAST) {
             finish_warp(sq, bad, r0, st, partials);
-            sq = SumSq();
+            sq = decltype(sq)();
             bad = false;
         }
     });
