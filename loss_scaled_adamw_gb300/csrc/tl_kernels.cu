@@ -92,6 +92,13 @@ constexpr int kScalar = 8;  // elements per thread in flight on the scalar path 
 #ifndef TL_SCALAR_FEW_GROUP
 #define TL_SCALAR_FEW_GROUP 2
 #endif
+// squared-norm partials: two float-float accumulators per lane (SumSqT's P).  Off:
+// with them the ragged list's check pass was 1 % faster but the 8-list pass over the
+// 1.24B list 7 % slower (register spills), and every partial-writing kernel must take
+// the same form for the passes to agree bit for bit.
+#ifndef TL_SQ_PAIRS
+#define TL_SQ_PAIRS 0
+#endif
 // many-list pass: products and weighted sums two fp32 lanes per instruction
 #ifndef TL_PAIRS
 #define TL_PAIRS 1
@@ -707,7 +714,7 @@ struct SumSqT {
         add(q);
     }
 };
-using SumSq = SumSqT<false>;
+using SumSq = SumSqT<TL_SQ_PAIRS != 0>;
 
 // Fixed-order reduction of a SumSq within a warp: a float-float butterfly
 // (TwoSum gives the same exact error term in both lanes of a pair, so every lane
@@ -1121,9 +1128,9 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
              const __grid_constant__ ManyArgs a, DevState* __restrict__ st, double* __restrict__ partials,
              int64_t fin) {
     const float inv_s = LAST ? __fdiv_rn(1.0f, st->S) : 1.0f;
-    // two accumulators in the whole-CTA check pass of one or two lists (5-6 % faster
-    // there: it is issue-bound); the other forms keep one, as two would cost them spills
-    SumSqT<(NT == kThreads && KM <= kFewLists && !STORE)> sq;
+    // (one accumulator structure in every partial-writing kernel: the passes that
+    // reach the same u give the same norm bit for bit)
+    SumSqT<TL_SQ_PAIRS != 0> sq;
     bool bad = false;
     for_runs(c0, c1, run, [&](int64_t c) {
         if (NT == kThreads)
