@@ -46,10 +46,12 @@ namespace {
 #ifndef TL_MINB_MANY
 #define TL_MINB_MANY 3
 #endif
-// 8-bit lists put fewer bytes in flight per thread (8 codes and a shared scale
-// per list and vector): more resident warps make up for it
+// 8-bit lists: with whole 16-element blocks per lane (TL_E4M3_BLOCKS) the 8-list
+// forms run at 3 CTAs per SM, where ptxas keeps part of the loop-invariant state in
+// local memory (L1); measured on the 1.24B list: 2.64 ms against 2.83 at 2 CTAs per
+// SM without spills (and 2.83 for 8-element vectors at 4 CTAs per SM)
 #ifndef TL_MINB_MANY_E4M3
-#define TL_MINB_MANY_E4M3 4
+#define TL_MINB_MANY_E4M3 (TL_E4M3_BLOCKS ? 3 : 4)
 #endif
 // Small-tensor groups (a warp per tensor, a few hundred elements each) are
 // latency-bound: more resident CTAs keep more tensors in flight.  The one- and
@@ -91,6 +93,11 @@ constexpr int kScalar = 8;  // elements per thread in flight on the scalar path 
 #endif
 #ifndef TL_SCALAR_FEW_GROUP
 #define TL_SCALAR_FEW_GROUP 2
+#endif
+// 8-bit lists in whole-CTA segments: a lane takes whole 16-element blocks (16 codes
+// and their scale per list and load) where every stream is 16-byte aligned
+#ifndef TL_E4M3_BLOCKS
+#define TL_E4M3_BLOCKS 1
 #endif
 // squared-norm partials: two float-float accumulators per lane (SumSqT's P).  Off:
 // with them the ragged list's check pass was 1 % faster but the 8-list pass over the
@@ -830,6 +837,40 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
     else if (!kReadG || ephase<4>(acc0) == ephase<Grad<GDT>::kBytes>(g0)) pl = VecPlan{(8 - ephase<4>(acc0)) & 7, true, true};
     if (kReadG && GDT == kE4M3 && pl.head != 0) pl.vec = false;  // an 8-bit vector must not straddle two blocks
     int head = 0, done = 0;
+    if constexpr (GDT == kE4M3 && NT == kThreads && TL_E4M3_BLOCKS) {
+        // 8-bit lists, every stream 16-byte aligned: whole 16-element blocks, one
+        // scale and 16 codes per load (the lanes take the elements as k_accum_many
+        // does, so that both give the same partials)
+        if (pl.vec && aligned16(acc0) && (!kReadG || aligned16(g0))) {
+            const int nb = len / 16;
+            for (int i = t; i < nb; i += NT) {
+                float ax[2][8];
+                uint4 c = make_uint4(0u, 0u, 0u, 0u);
+                float sb = 0.0f;
+                if (kReadG) {
+                    c = __ldg(reinterpret_cast<const uint4*>(g0) + i);
+                    sb = __ldg(sc + i);
+                }
+                if (kReadAcc) {
+                    ld8_f32(acc0 + 16 * i, ax[0], pl.wide);
+                    ld8_f32(acc0 + 16 * i + 8, ax[1], pl.wide);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const GradRaw<kE4M3>::T r{h == 0 ? make_uint2(c.x, c.y) : make_uint2(c.z, c.w), sb};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        ax[h][e] = unscale1<MODE>(kReadAcc ? ax[h][e] : 0.0f, kReadG ? GradRaw<kE4M3>::at(r, e) : 0.0f,
+                                                  w, inv_s);
+                    sq.vec8(ax[h], bad);
+                }
+                st8_f32(acc0 + 16 * i, ax[0], pl.wide);
+                st8_f32(acc0 + 16 * i + 8, ax[1], pl.wide);
+            }
+            done = nb * 16;
+            pl.vec = false;
+        }
+    }
     if (pl.vec) {
         head = min(pl.head, len);
         const bool wide = pl.wide;
@@ -1014,13 +1055,45 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     if (al) pl = VecPlan{0, true, !STORE || aligned32(acc0)};
     else if (same) pl = VecPlan{(8 - r) & 7, true, true};
     if (GDT == kE4M3 && pl.head != 0) pl.vec = false;  // an 8-bit vector must not straddle two blocks
+    int head = 0, done = 0;
+    if constexpr (GDT == kE4M3 && NT == kThreads && TL_E4M3_BLOCKS) {
+        // 8-bit lists, every stream 16-byte aligned: whole 16-element blocks, one
+        // scale and 16 codes per list and load, each half as one 8-element vector (the
+        // lanes take the elements as k_unscale does, so that both give the same partials)
+        if (pl.vec && al) {
+            const int nb = len / 16;
+            for (int i = t; i < nb; i += NT) {
+                typename GradRaw<GDT>::T lo[KM], hi[KM];
+#pragma unroll
+                for (int q = 0; q < KM; ++q)
+                    if (q < kk) {
+                        const uint4 c = __ldg(reinterpret_cast<const uint4*>(g[q]) + i);
+                        const float sb = __ldg(gs(q) + i);
+                        lo[q] = typename GradRaw<GDT>::T{make_uint2(c.x, c.y), sb};
+                        hi[q] = typename GradRaw<GDT>::T{make_uint2(c.z, c.w), sb};
+                    }
+                float a0[8], a1[8];
+                if (!FIRST) {
+                    ld8_f32(acc0 + 16 * i, a0, pl.wide);
+                    ld8_f32(acc0 + 16 * i + 8, a1, pl.wide);
+                }
+                mix_lists<GDT, FIRST, LAST>(lo, a, kk, inv_s, sq, bad, a0);
+                mix_lists<GDT, FIRST, LAST>(hi, a, kk, inv_s, sq, bad, a1);
+                if (STORE) {
+                    st8_f32(acc0 + 16 * i, a0, pl.wide);
+                    st8_f32(acc0 + 16 * i + 8, a1, pl.wide);
+                }
+            }
+            done = nb * 16;
+            pl.vec = false;
+        }
+    }
     // streams of unequal phase (16-bit lists, whole-CTA segments): rotated vectors in
     // the frame of the accumulation buffer (or of list 0 when it is not written)
     constexpr bool kRotForm = ROT && NT == kThreads && KM <= kFewLists && (GDT == kBF16 || GDT == kF16);
     const bool rot = kRotForm && !pl.vec;
     const int fr = STORE ? ephase<4>(acc0) : ephase<2>(g[0]);
     if (rot) pl = VecPlan{(8 - fr) & 7, true, true};
-    int head = 0, done = 0;
     if constexpr (kRotForm) {
       if (rot) {
         head = min(pl.head, len);
