@@ -605,18 +605,18 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
         const bool small = part == 1;
         const int64_t n = small ? nchunks - nbig : nbig;
         const int64_t nruns = (n + ctx->run[part] - 1) / ctx->run[part];
+        // the partial-writing passes over runs of several chunks take their half-CTA form
+        const int hf = !small && ctx->run[part] > 1 ? 16 : 0;
         for (int f = 0; f < 2; ++f) ctx->grid_acc[gdt][f][part] = grid_for(ctx, blocks_per_sm(0, gdt, f, small), n);
         for (int md = 0; md < 3; ++md)
-            ctx->grid_uns[gdt][md][part] = grid_for(ctx, blocks_per_sm(1, gdt, md, small), nruns);
+            ctx->grid_uns[gdt][md][part] = grid_for(ctx, blocks_per_sm(1, gdt, md | hf, small), nruns);
         ctx->grid_adam[pdt][part] = grid_for(ctx, blocks_per_sm(2, pdt, 0, small), n);
-        for (int vr = 0; vr < 8; ++vr)
-            ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr, small), nruns);
-        for (int vr = 8; vr < 16; ++vr)
-            ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr, small), nruns);
+        for (int vr = 0; vr < 16; ++vr)
+            ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr | hf, small), nruns);
         for (int few = 0; few < 2; ++few) {
             for (int rt = 0; rt < 2; ++rt)
                 ctx->grid_check[gdt][few][rt][part] =
-                    grid_for(ctx, blocks_per_sm(4, gdt, (few ? 4 : 0) | (rt ? 8 : 0), small), nruns);
+                    grid_for(ctx, blocks_per_sm(4, gdt, (few ? 4 : 0) | (rt ? 8 : 0) | hf, small), nruns);
             ctx->grid_remat[pdt][gdt][few][part] =
                 grid_for(ctx, blocks_per_sm(5, pdt, gdt | (few ? 4 : 0), small), n);
         }

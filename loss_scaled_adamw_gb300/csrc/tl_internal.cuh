@@ -28,6 +28,10 @@ constexpr int kGroup = 8;            // = warps per CTA
 #endif
 constexpr int kRun = TL_RUN;         // chunks per run where chunks are short (see launch_unscale)
 constexpr int kThreads = 256;        // streaming kernels: 8 warps per CTA
+#ifndef TL_HALF_THREADS
+#define TL_HALF_THREADS 128
+#endif
+constexpr int kHalfCTA = TL_HALF_THREADS;  // threads per segment in the half-CTA forms
 constexpr int kNormThreads = 256;    // threads per CTA of the second-stage reduce
 constexpr int kNormBlocks = 128;     // CTAs of the second-stage reduce: fixed, so its order is device-independent
 constexpr int kInlineGrads = 512;    // gradient pointer tables up to this size travel in the kernel parameters
@@ -171,12 +175,29 @@ cudaError_t launch_coef(DevState* st, float max_norm, cudaStream_t s);
 cudaError_t launch_export(const DevState* st, double* sumsq, int32_t* flag, cudaStream_t s);
 cudaError_t launch_import(DevState* st, const double* sumsq, const int32_t* flag, float max_norm, cudaStream_t s);
 
+// The half-CTA forms of the partial-writing passes (tl_kernels_half.cu): the two
+// halves of each CTA work two chunks of a run at once.  launch_unscale,
+// launch_accum_many and launch_check_many hand them their whole-CTA launches with
+// runs of several chunks.
+cudaError_t launch_unscale_half(int gdt, int mode, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+                                const GradTable& inl, const void* const* gtab, float w, DevState* st, double* partials,
+                                int64_t fin, int grid, cudaStream_t s);
+cudaError_t launch_accum_many_half(int gdt, bool first, bool last, bool rot, const Chunk* chunks, int64_t c0,
+                                   int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a, DevState* st,
+                                   double* partials, int64_t fin, int grid, cudaStream_t s);
+cudaError_t launch_check_many_half(int gdt, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+                                   const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
+                                   int64_t fin, int grid, cudaStream_t s);
+int blocks_per_sm_half(int kind, int dt, int variant);
+
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0
 // FIRST, bit 1 LAST, bit 2 at most kFewLists lists, bit 3 the rotated form), 4
 // many-list pass without the store (variant bits 2, 3 as for kind 3), 5
 // re-materialising adamw (dt = param dtype,
-// variant bits 0-1 = grad dtype, bit 2 at most kFewLists lists).
+// variant bits 0-1 = grad dtype, bit 2 at most kFewLists lists).  For kinds 1, 3
+// and 4, variant bit 4 asks for the form that a whole-CTA launch with runs of
+// several chunks takes (the half-CTA form).
 int blocks_per_sm(int kind, int dt, int variant, bool small);
 
 }  // namespace tl

@@ -543,6 +543,34 @@ __device__ __forceinline__ void for_runs(int64_t c0, int64_t c1, int run, Work w
     }
 }
 
+// Lists of short segments take the half-CTA forms (TL_PAIR_SEGS).
+#ifndef TL_PAIR_SEGS
+#define TL_PAIR_SEGS 1
+#endif
+constexpr bool kPairSegs = TL_PAIR_SEGS != 0;
+
+// The runs of a partial-writing kernel by its form: NT = kThreads, every chunk by
+// the whole CTA; NT = kHalfCTA, the two halves of the CTA on two chunks of a run at
+// once (half h: chunks r0 + h, r0 + h + 2, ...), for lists of short segments (runs
+// of several chunks), where a thread's share of a segment's setup then comes with
+// twice the vectors; NT = 32, small-tensor groups (one warp per tensor).  A thread
+// works chunk c as thread threadIdx.x % NT of its segment.  The partials stay one
+// per warp per run, and every partial-writing kernel of a context takes the same
+// form, so the passes that reach the same u give their lanes the same elements.
+template <int NT, class Work, class Done>
+__device__ __forceinline__ void for_runs_nt(int64_t c0, int64_t c1, int run, Work work, Done done) {
+    if (NT != kHalfCTA) {
+        for_runs(c0, c1, run, work, done);
+        return;
+    }
+    const int h = threadIdx.x / kHalfCTA;
+    for (int64_t r0 = c0 + int64_t(blockIdx.x) * run; r0 < c1; r0 += int64_t(gridDim.x) * run) {
+        const int64_t r1 = r0 + run < c1 ? r0 + run : c1;
+        for (int64_t c = r0 + h; c < r1; c += kThreads / kHalfCTA) work(c);
+        done(r0);
+    }
+}
+
 // The whole-CTA chunks of a persistent CTA (c0 + blockIdx.x, then every gridDim.x),
 // each descriptor handed to work(c, ch).  With PF the next descriptor is loaded
 // into registers before the current chunk is worked, so that its load overlaps the
@@ -938,7 +966,7 @@ __device__ __forceinline__ void unscale_segment(const Chunk& ch, int t, const vo
 }
 
 template <int NT, int GDT, int MODE>
-__global__ void __launch_bounds__(kThreads, NT == kThreads && GDT != kF32 ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, NT != 32 && GDT != kF32 ? 3 : 2)
 k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
           const __grid_constant__ GradTable inl,
           const void* const* __restrict__ gtab, float w, DevState* __restrict__ st, double* __restrict__ partials,
@@ -947,8 +975,8 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
     const float inv_s = __fdiv_rn(1.0f, st->S);
     SumSq sq;
     bool bad = false;
-    for_runs(c0, c1, run, [&](int64_t c) {
-        if (NT == kThreads) unscale_segment<kThreads, GDT, MODE>(chunks[c], threadIdx.x, gp, w, inv_s, sq, bad);
+    for_runs_nt<NT>(c0, c1, run, [&](int64_t c) {
+        if (NT != 32) unscale_segment<NT, GDT, MODE>(chunks[c], threadIdx.x % NT, gp, w, inv_s, sq, bad);
         else unscale_segment<32, GDT, MODE>(group_segment(chunks, c0, c), threadIdx.x & 31, gp, w, inv_s, sq, bad);
     }, [&](int64_t r0) {
         finish_warp(sq, bad, r0, st, partials);
@@ -1090,7 +1118,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     }
     // streams of unequal phase (16-bit lists, whole-CTA segments): rotated vectors in
     // the frame of the accumulation buffer (or of list 0 when it is not written)
-    constexpr bool kRotForm = ROT && NT == kThreads && KM <= kFewLists && (GDT == kBF16 || GDT == kF16);
+    constexpr bool kRotForm = ROT && NT != 32 && KM <= kFewLists && (GDT == kBF16 || GDT == kF16);
     const bool rot = kRotForm && !pl.vec;
     const int fr = STORE ? ephase<4>(acc0) : ephase<2>(g[0]);
     if (rot) pl = VecPlan{(8 - fr) & 7, true, true};
@@ -1161,7 +1189,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
     // tail, or the whole segment without a vector part: with one or two lists,
     // S elements per thread loaded first, then finished in element order (more
     // lists already put that many loads in flight)
-    constexpr int S = KM <= kFewLists ? (NT == kThreads ? TL_SCALAR_FEW : TL_SCALAR_FEW_GROUP) : TL_SCALAR_MANY;
+    constexpr int S = KM <= kFewLists ? (NT != 32 ? TL_SCALAR_FEW : TL_SCALAR_FEW_GROUP) : TL_SCALAR_MANY;
     int j = done + t;
     for (; S > 1 && j + (S - 1) * NT < len; j += S * NT) {
         float gx[S][KM], ax[S];
@@ -1192,7 +1220,7 @@ __device__ __forceinline__ void many_segment(const Chunk& ch, int t, const GradT
 // ROT: the form for lists of unequal element phase (rotated 16-bit loads; the
 // registers they need cost it one resident CTA per SM).
 template <int NT, int GDT, bool FIRST, bool LAST, int KM, bool STORE, bool ROT>
-__global__ void __launch_bounds__(kThreads, NT != kThreads ? (GDT == kF32 || KM > kFewLists ? 1 : GDT == kE4M3 ? TL_MINB_GROUP_FEW - 1 : TL_MINB_GROUP_FEW)
+__global__ void __launch_bounds__(kThreads, NT == 32 ? (GDT == kF32 || KM > kFewLists ? 1 : GDT == kE4M3 ? TL_MINB_GROUP_FEW - 1 : TL_MINB_GROUP_FEW)
                                             : GDT == kF32 ? 2
                                             : KM <= kFewLists ? (GDT == kE4M3 || (LAST && !FIRST) || ROT ? TL_MINB_FEW - 1 : TL_MINB_FEW)
                                             : GDT == kE4M3 ? TL_MINB_MANY_E4M3 : TL_MINB_MANY)
@@ -1205,9 +1233,9 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
     // reach the same u give the same norm bit for bit)
     SumSqT<TL_SQ_PAIRS != 0> sq;
     bool bad = false;
-    for_runs(c0, c1, run, [&](int64_t c) {
-        if (NT == kThreads)
-            many_segment<kThreads, GDT, FIRST, LAST, KM, STORE, ROT>(chunks[c], threadIdx.x, inl, a, inv_s, sq, bad);
+    for_runs_nt<NT>(c0, c1, run, [&](int64_t c) {
+        if (NT != 32)
+            many_segment<NT, GDT, FIRST, LAST, KM, STORE, ROT>(chunks[c], threadIdx.x % NT, inl, a, inv_s, sq, bad);
         else
             many_segment<32, GDT, FIRST, LAST, KM, STORE, false>(group_segment(chunks, c0, c), threadIdx.x & 31, inl, a,
                                                           inv_s, sq, bad);
@@ -1744,7 +1772,9 @@ AccFn acc_fn_nt(int gdt, bool first) {
     }
 }
 
+#ifndef TL_HALF_TU
 AccFn acc_fn(int gdt, bool first, bool small) { return small ? acc_fn_nt<32>(gdt, first) : acc_fn_nt<kThreads>(gdt, first); }
+#endif
 
 template <int NT, int GDT>
 UnsFn uns_fn_dt(int mode) {
@@ -1767,7 +1797,9 @@ UnsFn uns_fn_nt(int gdt, int mode) {
     }
 }
 
+#ifndef TL_HALF_TU
 UnsFn uns_fn(int gdt, int mode, bool small) { return small ? uns_fn_nt<32>(gdt, mode) : uns_fn_nt<kThreads>(gdt, mode); }
+#endif
 
 template <int NT, int GDT, int KM, bool ROT>
 ManyFn many_fn_km(bool first, bool last) {
@@ -1778,7 +1810,7 @@ ManyFn many_fn_km(bool first, bool last) {
 // the rotated form exists for whole-CTA segments of one or two 16-bit lists only
 template <int NT, int GDT>
 constexpr bool has_rot() {
-    return NT == kThreads && (GDT == kBF16 || GDT == kF16);
+    return NT != 32 && (GDT == kBF16 || GDT == kF16);
 }
 template <int NT, int GDT>
 ManyFn many_fn_dt(bool first, bool last, bool few, bool rot) {
@@ -1800,9 +1832,11 @@ ManyFn many_fn_nt(int gdt, bool first, bool last, bool few, bool rot) {
     }
 }
 
+#ifndef TL_HALF_TU
 ManyFn many_fn(int gdt, bool first, bool last, bool small, bool few, bool rot) {
     return small ? many_fn_nt<32>(gdt, first, last, few, rot) : many_fn_nt<kThreads>(gdt, first, last, few, rot);
 }
+#endif
 
 // the many-list pass without the store of u (first and last micro-batch at once)
 template <int NT, int GDT>
@@ -1823,9 +1857,11 @@ ManyFn check_fn_nt(int gdt, bool few, bool rot) {
         default: return nullptr;
     }
 }
+#ifndef TL_HALF_TU
 ManyFn check_fn(int gdt, bool small, bool few, bool rot) {
     return small ? check_fn_nt<32>(gdt, few, rot) : check_fn_nt<kThreads>(gdt, few, rot);
 }
+#endif
 
 using RematFn = void (*)(const Chunk*, int64_t, int64_t, DevState*, AdamHP, ScalerParams, const GradTableMany,
                          const ManyArgs);
@@ -1852,6 +1888,7 @@ RematFn remat_fn_nt(int pdt, int gdt, bool few) {
         default: return nullptr;
     }
 }
+#ifndef TL_HALF_TU
 RematFn remat_fn(int pdt, int gdt, bool small, bool few) {
     return small ? remat_fn_nt<32>(pdt, gdt, few) : remat_fn_nt<kThreads>(pdt, gdt, few);
 }
@@ -1863,8 +1900,63 @@ AdamFn adam_fn(int pdt, bool small) {
         default: return nullptr;
     }
 }
+#endif
+
+int occupancy(const void* f) {
+    int n = 0;
+    if (f == nullptr || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
 
 }  // namespace
+
+#ifdef TL_HALF_TU
+// The half-CTA forms of the partial-writing passes (this file compiled a second
+// time, by tl_kernels_half.cu): the launchers of tl_kernels.cu hand them the
+// whole-CTA launches of contexts whose runs hold several chunks.
+cudaError_t launch_unscale_half(int gdt, int mode, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+                                const GradTable& inl, const void* const* gtab, float w, DevState* st, double* partials,
+                                int64_t fin, int grid, cudaStream_t s) {
+    UnsFn f = uns_fn_nt<kHalfCTA>(gdt, mode);
+    if (f == nullptr || run < 1) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, gtab, w, st, partials, fin);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accum_many_half(int gdt, bool first, bool last, bool rot, const Chunk* chunks, int64_t c0,
+                                   int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a, DevState* st,
+                                   double* partials, int64_t fin, int grid, cudaStream_t s) {
+    ManyFn f = many_fn_nt<kHalfCTA>(gdt, first, last, a.k <= kFewLists, rot);
+    if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, last ? fin : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_check_many_half(int gdt, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+                                   const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
+                                   int64_t fin, int grid, cudaStream_t s) {
+    ManyFn f = check_fn_nt<kHalfCTA>(gdt, a.k <= kFewLists, rot);
+    if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, fin);
+    return cudaGetLastError();
+}
+
+int blocks_per_sm_half(int kind, int dt, int variant) {
+    const void* f = nullptr;
+    if (kind == 1) f = reinterpret_cast<const void*>(uns_fn_nt<kHalfCTA>(dt, variant));
+    else if (kind == 3)
+        f = reinterpret_cast<const void*>(many_fn_nt<kHalfCTA>(dt, (variant & 1) != 0, (variant & 2) != 0,
+                                                               (variant & 4) != 0, (variant & 8) != 0));
+    else if (kind == 4) f = reinterpret_cast<const void*>(check_fn_nt<kHalfCTA>(dt, (variant & 4) != 0, (variant & 8) != 0));
+    return occupancy(f);
+}
+
+#else  // the whole-CTA and group forms, and the other kernels
+
+// Whole-CTA launches of the partial-writing passes over runs of several chunks go
+// to the half-CTA forms.
+bool half_form(bool small, int run) { return kPairSegs && !small && run > 1; }
 
 cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, int64_t c0,
                               int64_t c1, const GradTable& inl, const void* const* gtab, float w, int grid,
@@ -1878,6 +1970,8 @@ cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chun
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
                            int64_t c1, int run, const GradTable& inl, const void* const* gtab, float w, DevState* st,
                            double* partials, int64_t fin, int grid, cudaStream_t s) {
+    if (half_form(small, run))
+        return launch_unscale_half(gdt, mode, chunks, c0, c1, run, inl, gtab, w, st, partials, fin, grid, s);
     UnsFn f = uns_fn(gdt, mode, small);
     if (f == nullptr || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, gtab, w, st, partials, fin);
@@ -1887,6 +1981,8 @@ cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, i
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, bool rot, const Chunk* chunks,
                               int64_t c0, int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a,
                               DevState* st, double* partials, int64_t fin, int grid, cudaStream_t s) {
+    if (half_form(small, run))
+        return launch_accum_many_half(gdt, first, last, rot, chunks, c0, c1, run, inl, a, st, partials, fin, grid, s);
     ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, last ? fin : 0);
@@ -1904,6 +2000,8 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
 cudaError_t launch_check_many(int gdt, bool small, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
                               int64_t fin, int grid, cudaStream_t s) {
+    if (half_form(small, run))
+        return launch_check_many_half(gdt, rot, chunks, c0, c1, run, inl, a, st, partials, fin, grid, s);
     ManyFn f = check_fn(gdt, small, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, fin);
@@ -1948,6 +2046,9 @@ cudaError_t launch_import(DevState* st, const double* sumsq, const int32_t* flag
 }
 
 int blocks_per_sm(int kind, int dt, int variant, bool small) {
+    if ((variant & 16) != 0 && (kind == 1 || kind == 3 || kind == 4) && half_form(small, 2))
+        return blocks_per_sm_half(kind, dt, variant & 15);
+    variant &= 15;
     const void* f = nullptr;
     if (kind == 0) f = reinterpret_cast<const void*>(acc_fn(dt, variant != 0, small));
     else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn(dt, variant, small));
@@ -1957,10 +2058,9 @@ int blocks_per_sm(int kind, int dt, int variant, bool small) {
                                                   (variant & 8) != 0));
     else if (kind == 4) f = reinterpret_cast<const void*>(check_fn(dt, small, (variant & 4) != 0, (variant & 8) != 0));
     else if (kind == 5) f = reinterpret_cast<const void*>(remat_fn(dt, variant & 3, small, (variant & 4) != 0));
-    if (f == nullptr) return 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess || n < 1) return 1;
-    return n;
+    return occupancy(f);
 }
+
+#endif  // TL_HALF_TU
 
 }  // namespace tl
