@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtl_gb300.so")
-SOURCES = ["tl_kernels.cu", "tl_kernels_half.cu", "tl_api.cu", "tl_noalloc.cu"]
+SOURCES = ["tl_kernels.cu", "tl_kernels_split.cu", "tl_api.cu", "tl_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "tl_internal.cuh"), os.path.join(ROOT, "include", "tl.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",

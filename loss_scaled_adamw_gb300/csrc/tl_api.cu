@@ -605,12 +605,12 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
         const bool small = part == 1;
         const int64_t n = small ? nchunks - nbig : nbig;
         const int64_t nruns = (n + ctx->run[part] - 1) / ctx->run[part];
-        // the partial-writing passes over runs of several chunks take their half-CTA form
+        // the partial-writing passes over runs of several chunks take their split form
         const int hf = !small && ctx->run[part] > 1 ? 16 : 0;
         for (int f = 0; f < 2; ++f) ctx->grid_acc[gdt][f][part] = grid_for(ctx, blocks_per_sm(0, gdt, f, small), n);
         for (int md = 0; md < 3; ++md)
             ctx->grid_uns[gdt][md][part] = grid_for(ctx, blocks_per_sm(1, gdt, md | hf, small), nruns);
-        ctx->grid_adam[pdt][part] = grid_for(ctx, blocks_per_sm(2, pdt, 0, small), n);
+        ctx->grid_adam[pdt][part] = grid_for(ctx, blocks_per_sm(2, pdt, hf, small), n);
         for (int vr = 0; vr < 16; ++vr)
             ctx->grid_many[gdt][vr][part] = grid_for(ctx, blocks_per_sm(3, gdt, vr | hf, small), nruns);
         for (int few = 0; few < 2; ++few) {
@@ -618,7 +618,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
                 ctx->grid_check[gdt][few][rt][part] =
                     grid_for(ctx, blocks_per_sm(4, gdt, (few ? 4 : 0) | (rt ? 8 : 0) | hf, small), nruns);
             ctx->grid_remat[pdt][gdt][few][part] =
-                grid_for(ctx, blocks_per_sm(5, pdt, gdt | (few ? 4 : 0), small), n);
+                grid_for(ctx, blocks_per_sm(5, pdt, gdt | (few ? 4 : 0) | hf, small), n);
         }
     }
     *out = ctx;
@@ -920,7 +920,7 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         // no elements: still one launch, whose CTA computes the beta powers and runs
         // the scaler
         e = gate(ctx);
-        if (e == cudaSuccess) e = launch_adamw(pdt, false, ctx->d_chunks, 0, 0, ctx->d_state, h, scaler(true), 1, s);
+        if (e == cudaSuccess) e = launch_adamw(pdt, false, 1, ctx->d_chunks, 0, 0, ctx->d_state, h, scaler(true), 1, s);
         if (e == cudaSuccess) ctx->launches += 1;
     } else if (ctx->remat) {
         // u recomputed from the lists the update was checked on (the same device
@@ -935,14 +935,16 @@ int tl_clip_adamw_step(tl_ctx* ctx, const tl_adamw_hp* hp, tl_stream stream) {
         fill_many_args(ctx, ctx->remat_grads.data(), ctx->remat_n, ctx->N_update, 0, k, by_value, tabs, a, inl);
         const int gdt = ctx->cfg.grad_dtype;
         e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
-            return launch_adamw_remat(pdt, gdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h, scaler(lastl), inl, a,
+            return launch_adamw_remat(pdt, gdt, small, ctx->run[small ? 1 : 0], ctx->d_chunks, c0, c1, ctx->d_state, h,
+                                      scaler(lastl), inl, a,
                                       ctx->grid_remat[pdt][gdt][k <= kFewLists ? 1 : 0][small ? 1 : 0], s);
         });
         if (e == cudaSuccess)
             for (int i = 0; i < k; ++i) mark_used(slots[size_t(i)], s);
     } else {
         e = over_parts(ctx, [&](bool small, int64_t c0, int64_t c1, bool lastl) {
-            return launch_adamw(pdt, small, ctx->d_chunks, c0, c1, ctx->d_state, h, scaler(lastl),
+            return launch_adamw(pdt, small, ctx->run[small ? 1 : 0], ctx->d_chunks, c0, c1, ctx->d_state, h,
+                                scaler(lastl),
                                 ctx->grid_adam[pdt][small ? 1 : 0], s);
         });
     }

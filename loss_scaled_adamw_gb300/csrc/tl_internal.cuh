@@ -28,10 +28,15 @@ constexpr int kGroup = 8;            // = warps per CTA
 #endif
 constexpr int kRun = TL_RUN;         // chunks per run where chunks are short (see launch_unscale)
 constexpr int kThreads = 256;        // streaming kernels: 8 warps per CTA
-#ifndef TL_HALF_THREADS
-#define TL_HALF_THREADS 128
+// Threads per segment in the split forms (lists of short segments), where a CTA
+// works several segments at once: 64 measured faster than 128 on the ragged
+// 100k list (check pass 0.271 -> 0.259 ms, 0.380 -> 0.358 ms with gapped lists).
+#ifndef TL_SPLIT_THREADS
+#define TL_SPLIT_THREADS 64
 #endif
-constexpr int kHalfCTA = TL_HALF_THREADS;  // threads per segment in the half-CTA forms
+constexpr int kSplitThreads = TL_SPLIT_THREADS;
+static_assert(kSplitThreads % 32 == 0 && kSplitThreads > 32 && kThreads % kSplitThreads == 0,
+              "a split form works a segment with whole warps (32 is the small-tensor form)");
 constexpr int kNormThreads = 256;    // threads per CTA of the second-stage reduce
 constexpr int kNormBlocks = 128;     // CTAs of the second-stage reduce: fixed, so its order is device-independent
 constexpr int kInlineGrads = 512;    // gradient pointer tables up to this size travel in the kernel parameters
@@ -159,13 +164,14 @@ cudaError_t launch_check_many(int gdt, bool small, bool rot, const Chunk* chunks
                               int64_t fin, int grid, cudaStream_t s);
 // The AdamW launches compute the clip coefficient from the device norm and
 // hp.max_norm; with sp.run = 1 the launch's last CTA also runs the scaler state
-// machine (the last AdamW launch of an update).
-cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, int64_t c0,
+// machine (the last AdamW launch of an update).  run: the part's run length (a
+// whole-CTA launch with runs of several chunks takes the split form).
+cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, int run, const Chunk* chunks, int64_t c0,
                                int64_t c1, DevState* st, AdamHP hp, ScalerParams sp, const GradTableMany& inl,
                                const ManyArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevState* st, float max_norm,
                         cudaStream_t s);
-cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
+cudaError_t launch_adamw(int pdt, bool small, int run, const Chunk* chunks, int64_t c0, int64_t c1,
                          DevState* st, AdamHP hp, ScalerParams sp, int grid, cudaStream_t s);
 cudaError_t launch_seed(const DevState* st, float w, float* out, cudaStream_t s);
 // One thread each: the clip coefficient from the device norm; the local squared norm
@@ -175,20 +181,25 @@ cudaError_t launch_coef(DevState* st, float max_norm, cudaStream_t s);
 cudaError_t launch_export(const DevState* st, double* sumsq, int32_t* flag, cudaStream_t s);
 cudaError_t launch_import(DevState* st, const double* sumsq, const int32_t* flag, float max_norm, cudaStream_t s);
 
-// The half-CTA forms of the partial-writing passes (tl_kernels_half.cu): the two
-// halves of each CTA work two chunks of a run at once.  launch_unscale,
-// launch_accum_many and launch_check_many hand them their whole-CTA launches with
-// runs of several chunks.
-cudaError_t launch_unscale_half(int gdt, int mode, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+// The split forms of the streaming passes (tl_kernels_split.cu): each CTA works
+// kThreads / kSplitThreads chunks at once.  launch_unscale, launch_accum_many,
+// launch_check_many, launch_adamw and launch_adamw_remat hand them their whole-CTA
+// launches of contexts with runs of several chunks (lists of short segments).
+cudaError_t launch_unscale_split(int gdt, int mode, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                                 const GradTable& inl, const void* const* gtab, float w, DevState* st, double* partials,
                                 int64_t fin, int grid, cudaStream_t s);
-cudaError_t launch_accum_many_half(int gdt, bool first, bool last, bool rot, const Chunk* chunks, int64_t c0,
+cudaError_t launch_accum_many_split(int gdt, bool first, bool last, bool rot, const Chunk* chunks, int64_t c0,
                                    int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a, DevState* st,
                                    double* partials, int64_t fin, int grid, cudaStream_t s);
-cudaError_t launch_check_many_half(int gdt, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+cudaError_t launch_check_many_split(int gdt, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                                    const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
                                    int64_t fin, int grid, cudaStream_t s);
-int blocks_per_sm_half(int kind, int dt, int variant);
+cudaError_t launch_adamw_split(int pdt, const Chunk* chunks, int64_t c0, int64_t c1, DevState* st, AdamHP hp,
+                               ScalerParams sp, int grid, cudaStream_t s);
+cudaError_t launch_adamw_remat_split(int pdt, int gdt, const Chunk* chunks, int64_t c0, int64_t c1, DevState* st,
+                                     AdamHP hp, ScalerParams sp, const GradTableMany& inl, const ManyArgs& a, int grid,
+                                     cudaStream_t s);
+int blocks_per_sm_split(int kind, int dt, int variant);
 
 // Resident CTAs per SM of each streaming kernel (for persistent grid sizing).
 // kind: 0 accumulate, 1 unscale, 2 adamw, 3 many-list accumulate (variant bit 0
@@ -197,7 +208,7 @@ int blocks_per_sm_half(int kind, int dt, int variant);
 // re-materialising adamw (dt = param dtype,
 // variant bits 0-1 = grad dtype, bit 2 at most kFewLists lists).  For kinds 1, 3
 // and 4, variant bit 4 asks for the form that a whole-CTA launch with runs of
-// several chunks takes (the half-CTA form).
+// several chunks takes (the split form); kinds 2 and 5 likewise.
 int blocks_per_sm(int kind, int dt, int variant, bool small);
 
 }  // namespace tl

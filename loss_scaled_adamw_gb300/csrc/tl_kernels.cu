@@ -543,32 +543,47 @@ __device__ __forceinline__ void for_runs(int64_t c0, int64_t c1, int run, Work w
     }
 }
 
-// Lists of short segments take the half-CTA forms (TL_PAIR_SEGS).
+// Lists of short segments take the split forms (TL_PAIR_SEGS).
 #ifndef TL_PAIR_SEGS
 #define TL_PAIR_SEGS 1
 #endif
 constexpr bool kPairSegs = TL_PAIR_SEGS != 0;
+// ... and so do the AdamW passes (TL_SPLIT_ADAM)
+#ifndef TL_SPLIT_ADAM
+#define TL_SPLIT_ADAM 1
+#endif
+constexpr bool kSplitAdam = TL_SPLIT_ADAM != 0;
 
 // The runs of a partial-writing kernel by its form: NT = kThreads, every chunk by
-// the whole CTA; NT = kHalfCTA, the two halves of the CTA on two chunks of a run at
-// once (half h: chunks r0 + h, r0 + h + 2, ...), for lists of short segments (runs
-// of several chunks), where a thread's share of a segment's setup then comes with
-// twice the vectors; NT = 32, small-tensor groups (one warp per tensor).  A thread
+// the whole CTA; NT = kSplitThreads, the CTA split into kThreads / NT parts that work
+// as many chunks of a run at once (part h: chunks r0 + h, r0 + h + kThreads / NT,
+// ...), for lists of short segments (runs of several chunks), where a thread's
+// share of a segment's setup then comes with several times the vectors; NT = 32, small-tensor groups (one warp per tensor).  A thread
 // works chunk c as thread threadIdx.x % NT of its segment.  The partials stay one
 // per warp per run, and every partial-writing kernel of a context takes the same
 // form, so the passes that reach the same u give their lanes the same elements.
 template <int NT, class Work, class Done>
 __device__ __forceinline__ void for_runs_nt(int64_t c0, int64_t c1, int run, Work work, Done done) {
-    if (NT != kHalfCTA) {
+    if (NT != kSplitThreads) {
         for_runs(c0, c1, run, work, done);
         return;
     }
-    const int h = threadIdx.x / kHalfCTA;
+    const int h = threadIdx.x / kSplitThreads;
     for (int64_t r0 = c0 + int64_t(blockIdx.x) * run; r0 < c1; r0 += int64_t(gridDim.x) * run) {
         const int64_t r1 = r0 + run < c1 ? r0 + run : c1;
-        for (int64_t c = r0 + h; c < r1; c += kThreads / kHalfCTA) work(c);
+        for (int64_t c = r0 + h; c < r1; c += kThreads / kSplitThreads) work(c);
         done(r0);
     }
+}
+
+// The chunks of a split form of a pass without partials (AdamW): the CTA's
+// kThreads / NT parts take chunks c0 + P b + h, then every P gridDim.x (P parts,
+// CTA b, part h).
+template <int NT, class Work>
+__device__ __forceinline__ void for_split_chunks(int64_t c0, int64_t c1, Work work) {
+    constexpr int P = kThreads / NT;
+    const int h = threadIdx.x / NT;
+    for (int64_t c = c0 + int64_t(blockIdx.x) * P + h; c < c1; c += int64_t(gridDim.x) * P) work(c);
 }
 
 // The whole-CTA chunks of a persistent CTA (c0 + blockIdx.x, then every gridDim.x),
@@ -1664,7 +1679,7 @@ __device__ __noinline__ void adam_finish(DevState* __restrict__ st, const Scaler
 }
 
 template <int NT, int PDT>
-__global__ void __launch_bounds__(kThreads, NT != kThreads ? TL_MINB_ADAM_GROUP : TL_MINB_ADAM)
+__global__ void __launch_bounds__(kThreads, NT == 32 ? TL_MINB_ADAM_GROUP : TL_MINB_ADAM)
 k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
         DevState* __restrict__ st, AdamHP hp, ScalerParams sp) {
     AdamConsts k;
@@ -1672,6 +1687,11 @@ k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
         if (NT == kThreads) {
             for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
                 adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromAcc(ch));
+            });
+        } else if (NT != 32) {
+            for_split_chunks<NT>(c0, c1, [&](int64_t c) {
+                const Chunk& ch = chunks[c];
+                adamw_segment<NT, PDT>(ch, threadIdx.x % NT, k, UFromAcc(ch));
             });
         } else {
             for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
@@ -1686,7 +1706,7 @@ k_adamw(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
 // The re-materialising AdamW pass: u of every element recomputed from the
 // resident gradient lists (at most KM <= kRematLists of them) instead of read.
 template <int NT, int PDT, int GDT, int KM>
-__global__ void __launch_bounds__(kThreads, NT != kThreads && GDT == kF32 ? 1
+__global__ void __launch_bounds__(kThreads, NT == 32 && GDT == kF32 ? 1
                                             : KM <= kFewLists && GDT != kF32 ? TL_MINB_REMAT_FEW : TL_MINB_REMAT)
 k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
               DevState* __restrict__ st, AdamHP hp, ScalerParams sp, const __grid_constant__ GradTableMany inl,
@@ -1697,6 +1717,11 @@ k_adamw_remat(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1,
         if (NT == kThreads) {
             for_chunks<true>(chunks, c0, c1, [&](int64_t, const Chunk& ch) {
                 adamw_segment<kThreads, PDT>(ch, threadIdx.x, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
+            });
+        } else if (NT != 32) {
+            for_split_chunks<NT>(c0, c1, [&](int64_t c) {
+                const Chunk& ch = chunks[c];
+                adamw_segment<NT, PDT>(ch, threadIdx.x % NT, k, UFromLists<GDT, KM>(ch, inl, a, inv_s));
             });
         } else {
             for (int64_t c = c0 + blockIdx.x; c < c1; c += gridDim.x) {
@@ -1772,7 +1797,7 @@ AccFn acc_fn_nt(int gdt, bool first) {
     }
 }
 
-#ifndef TL_HALF_TU
+#ifndef TL_SPLIT_TU
 AccFn acc_fn(int gdt, bool first, bool small) { return small ? acc_fn_nt<32>(gdt, first) : acc_fn_nt<kThreads>(gdt, first); }
 #endif
 
@@ -1797,7 +1822,7 @@ UnsFn uns_fn_nt(int gdt, int mode) {
     }
 }
 
-#ifndef TL_HALF_TU
+#ifndef TL_SPLIT_TU
 UnsFn uns_fn(int gdt, int mode, bool small) { return small ? uns_fn_nt<32>(gdt, mode) : uns_fn_nt<kThreads>(gdt, mode); }
 #endif
 
@@ -1832,7 +1857,7 @@ ManyFn many_fn_nt(int gdt, bool first, bool last, bool few, bool rot) {
     }
 }
 
-#ifndef TL_HALF_TU
+#ifndef TL_SPLIT_TU
 ManyFn many_fn(int gdt, bool first, bool last, bool small, bool few, bool rot) {
     return small ? many_fn_nt<32>(gdt, first, last, few, rot) : many_fn_nt<kThreads>(gdt, first, last, few, rot);
 }
@@ -1857,7 +1882,7 @@ ManyFn check_fn_nt(int gdt, bool few, bool rot) {
         default: return nullptr;
     }
 }
-#ifndef TL_HALF_TU
+#ifndef TL_SPLIT_TU
 ManyFn check_fn(int gdt, bool small, bool few, bool rot) {
     return small ? check_fn_nt<32>(gdt, few, rot) : check_fn_nt<kThreads>(gdt, few, rot);
 }
@@ -1888,7 +1913,7 @@ RematFn remat_fn_nt(int pdt, int gdt, bool few) {
         default: return nullptr;
     }
 }
-#ifndef TL_HALF_TU
+#ifndef TL_SPLIT_TU
 RematFn remat_fn(int pdt, int gdt, bool small, bool few) {
     return small ? remat_fn_nt<32>(pdt, gdt, few) : remat_fn_nt<kThreads>(pdt, gdt, few);
 }
@@ -1911,52 +1936,73 @@ int occupancy(const void* f) {
 
 }  // namespace
 
-#ifdef TL_HALF_TU
-// The half-CTA forms of the partial-writing passes (this file compiled a second
-// time, by tl_kernels_half.cu): the launchers of tl_kernels.cu hand them the
+#ifdef TL_SPLIT_TU
+// The split forms of the partial-writing passes (this file compiled a second
+// time, by tl_kernels_split.cu): the launchers of tl_kernels.cu hand them the
 // whole-CTA launches of contexts whose runs hold several chunks.
-cudaError_t launch_unscale_half(int gdt, int mode, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+cudaError_t launch_unscale_split(int gdt, int mode, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                                 const GradTable& inl, const void* const* gtab, float w, DevState* st, double* partials,
                                 int64_t fin, int grid, cudaStream_t s) {
-    UnsFn f = uns_fn_nt<kHalfCTA>(gdt, mode);
+    UnsFn f = uns_fn_nt<kSplitThreads>(gdt, mode);
     if (f == nullptr || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, gtab, w, st, partials, fin);
     return cudaGetLastError();
 }
 
-cudaError_t launch_accum_many_half(int gdt, bool first, bool last, bool rot, const Chunk* chunks, int64_t c0,
+cudaError_t launch_accum_many_split(int gdt, bool first, bool last, bool rot, const Chunk* chunks, int64_t c0,
                                    int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a, DevState* st,
                                    double* partials, int64_t fin, int grid, cudaStream_t s) {
-    ManyFn f = many_fn_nt<kHalfCTA>(gdt, first, last, a.k <= kFewLists, rot);
+    ManyFn f = many_fn_nt<kSplitThreads>(gdt, first, last, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, last ? fin : 0);
     return cudaGetLastError();
 }
 
-cudaError_t launch_check_many_half(int gdt, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
+cudaError_t launch_check_many_split(int gdt, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                                    const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
                                    int64_t fin, int grid, cudaStream_t s) {
-    ManyFn f = check_fn_nt<kHalfCTA>(gdt, a.k <= kFewLists, rot);
+    ManyFn f = check_fn_nt<kSplitThreads>(gdt, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, fin);
     return cudaGetLastError();
 }
 
-int blocks_per_sm_half(int kind, int dt, int variant) {
+cudaError_t launch_adamw_split(int pdt, const Chunk* chunks, int64_t c0, int64_t c1, DevState* st, AdamHP hp,
+                               ScalerParams sp, int grid, cudaStream_t s) {
+    AdamFn f = pdt == kBF16 ? k_adamw<kSplitThreads, kBF16> : pdt == kF16 ? k_adamw<kSplitThreads, kF16> : nullptr;
+    if (f == nullptr) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, sp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw_remat_split(int pdt, int gdt, const Chunk* chunks, int64_t c0, int64_t c1, DevState* st,
+                                     AdamHP hp, ScalerParams sp, const GradTableMany& inl, const ManyArgs& a, int grid,
+                                     cudaStream_t s) {
+    RematFn f = remat_fn_nt<kSplitThreads>(pdt, gdt, a.k <= kFewLists);
+    if (f == nullptr || a.k < 1 || a.k > kRematLists) return cudaErrorInvalidValue;
+    f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, sp, inl, a);
+    return cudaGetLastError();
+}
+
+int blocks_per_sm_split(int kind, int dt, int variant) {
     const void* f = nullptr;
-    if (kind == 1) f = reinterpret_cast<const void*>(uns_fn_nt<kHalfCTA>(dt, variant));
+    if (kind == 2)
+        f = dt == kBF16 ? reinterpret_cast<const void*>(k_adamw<kSplitThreads, kBF16>)
+            : dt == kF16 ? reinterpret_cast<const void*>(k_adamw<kSplitThreads, kF16>) : nullptr;
+    else if (kind == 5) f = reinterpret_cast<const void*>(remat_fn_nt<kSplitThreads>(dt, variant & 3, (variant & 4) != 0));
+    else if (kind == 1) f = reinterpret_cast<const void*>(uns_fn_nt<kSplitThreads>(dt, variant));
     else if (kind == 3)
-        f = reinterpret_cast<const void*>(many_fn_nt<kHalfCTA>(dt, (variant & 1) != 0, (variant & 2) != 0,
+        f = reinterpret_cast<const void*>(many_fn_nt<kSplitThreads>(dt, (variant & 1) != 0, (variant & 2) != 0,
                                                                (variant & 4) != 0, (variant & 8) != 0));
-    else if (kind == 4) f = reinterpret_cast<const void*>(check_fn_nt<kHalfCTA>(dt, (variant & 4) != 0, (variant & 8) != 0));
+    else if (kind == 4) f = reinterpret_cast<const void*>(check_fn_nt<kSplitThreads>(dt, (variant & 4) != 0, (variant & 8) != 0));
     return occupancy(f);
 }
 
 #else  // the whole-CTA and group forms, and the other kernels
 
 // Whole-CTA launches of the partial-writing passes over runs of several chunks go
-// to the half-CTA forms.
-bool half_form(bool small, int run) { return kPairSegs && !small && run > 1; }
+// to the split forms.
+bool split_form(bool small, int run) { return kPairSegs && !small && run > 1; }
 
 cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chunks, int64_t c0,
                               int64_t c1, const GradTable& inl, const void* const* gtab, float w, int grid,
@@ -1970,8 +2016,8 @@ cudaError_t launch_accumulate(int gdt, bool first, bool small, const Chunk* chun
 cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, int64_t c0,
                            int64_t c1, int run, const GradTable& inl, const void* const* gtab, float w, DevState* st,
                            double* partials, int64_t fin, int grid, cudaStream_t s) {
-    if (half_form(small, run))
-        return launch_unscale_half(gdt, mode, chunks, c0, c1, run, inl, gtab, w, st, partials, fin, grid, s);
+    if (split_form(small, run))
+        return launch_unscale_split(gdt, mode, chunks, c0, c1, run, inl, gtab, w, st, partials, fin, grid, s);
     UnsFn f = uns_fn(gdt, mode, small);
     if (f == nullptr || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, gtab, w, st, partials, fin);
@@ -1981,8 +2027,8 @@ cudaError_t launch_unscale(int gdt, int mode, bool small, const Chunk* chunks, i
 cudaError_t launch_accum_many(int gdt, bool first, bool last, bool small, bool rot, const Chunk* chunks,
                               int64_t c0, int64_t c1, int run, const GradTableMany& inl, const ManyArgs& a,
                               DevState* st, double* partials, int64_t fin, int grid, cudaStream_t s) {
-    if (half_form(small, run))
-        return launch_accum_many_half(gdt, first, last, rot, chunks, c0, c1, run, inl, a, st, partials, fin, grid, s);
+    if (split_form(small, run))
+        return launch_accum_many_split(gdt, first, last, rot, chunks, c0, c1, run, inl, a, st, partials, fin, grid, s);
     ManyFn f = many_fn(gdt, first, last, small, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, last ? fin : 0);
@@ -2000,25 +2046,28 @@ cudaError_t launch_norm(const double* partials, int64_t n, double* slots, DevSta
 cudaError_t launch_check_many(int gdt, bool small, bool rot, const Chunk* chunks, int64_t c0, int64_t c1, int run,
                               const GradTableMany& inl, const ManyArgs& a, DevState* st, double* partials,
                               int64_t fin, int grid, cudaStream_t s) {
-    if (half_form(small, run))
-        return launch_check_many_half(gdt, rot, chunks, c0, c1, run, inl, a, st, partials, fin, grid, s);
+    if (split_form(small, run))
+        return launch_check_many_split(gdt, rot, chunks, c0, c1, run, inl, a, st, partials, fin, grid, s);
     ManyFn f = check_fn(gdt, small, a.k <= kFewLists, rot);
     if (f == nullptr || a.k < 1 || a.k > kMaxMany || run < 1) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, run, inl, a, st, partials, fin);
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, const Chunk* chunks, int64_t c0,
+cudaError_t launch_adamw_remat(int pdt, int gdt, bool small, int run, const Chunk* chunks, int64_t c0,
                                int64_t c1, DevState* st, AdamHP hp, ScalerParams sp, const GradTableMany& inl,
                                const ManyArgs& a, int grid, cudaStream_t s) {
+    if (kSplitAdam && split_form(small, run))
+        return launch_adamw_remat_split(pdt, gdt, chunks, c0, c1, st, hp, sp, inl, a, grid, s);
     RematFn f = remat_fn(pdt, gdt, small, a.k <= kFewLists);
     if (f == nullptr || a.k < 1 || a.k > kRematLists) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, sp, inl, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_adamw(int pdt, bool small, const Chunk* chunks, int64_t c0, int64_t c1,
+cudaError_t launch_adamw(int pdt, bool small, int run, const Chunk* chunks, int64_t c0, int64_t c1,
                          DevState* st, AdamHP hp, ScalerParams sp, int grid, cudaStream_t s) {
+    if (kSplitAdam && split_form(small, run)) return launch_adamw_split(pdt, chunks, c0, c1, st, hp, sp, grid, s);
     AdamFn f = adam_fn(pdt, small);
     if (f == nullptr) return cudaErrorInvalidValue;
     f<<<grid, kThreads, 0, s>>>(chunks, c0, c1, st, hp, sp);
@@ -2046,8 +2095,9 @@ cudaError_t launch_import(DevState* st, const double* sumsq, const int32_t* flag
 }
 
 int blocks_per_sm(int kind, int dt, int variant, bool small) {
-    if ((variant & 16) != 0 && (kind == 1 || kind == 3 || kind == 4) && half_form(small, 2))
-        return blocks_per_sm_half(kind, dt, variant & 15);
+    if ((variant & 16) != 0 && kind >= 1 && kind <= 5 && (kSplitAdam || (kind != 2 && kind != 5)) &&
+        split_form(small, 2))
+        return blocks_per_sm_split(kind, dt, variant & 15);
     variant &= 15;
     const void* f = nullptr;
     if (kind == 0) f = reinterpret_cast<const void*>(acc_fn(dt, variant != 0, small));
@@ -2061,6 +2111,6 @@ int blocks_per_sm(int kind, int dt, int variant, bool small) {
     return occupancy(f);
 }
 
-#endif  // TL_HALF_TU
+#endif  // TL_SPLIT_TU
 
 }  // namespace tl
