@@ -110,7 +110,7 @@ def kernel_source_digest() -> str:
     count, so recorded counters stay valid across edits that cannot change a kernel."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("tl_kernels.cu", "tl_internal.cuh"):
+    for f in ("tl_kernels.cu", "tl_kernels_split.cu", "tl_internal.cuh"):
         with open(os.path.join(ROOT, "loss_scaled_adamw_gb300", "csrc", f)) as fh:
             for line in fh:
                 cut = line.find("//")
