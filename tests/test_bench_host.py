@@ -15,6 +15,7 @@ def _tree(tmp_path, kernels: str, internal: str = "struct X { int a; };\n"):
     d = tmp_path / "loss_scaled_adamw_gb300" / "csrc"
     d.mkdir(parents=True, exist_ok=True)
     (d / "tl_kernels.cu").write_text(kernels)
+    (d / "tl_kernels_split.cu").write_text('#define TL_SPLIT_TU 1\n#include "tl_kernels.cu"\n')
     (d / "tl_internal.cuh").write_text(internal)
     (tmp_path / "profiles").mkdir(exist_ok=True)
     return tmp_path
