@@ -2,7 +2,7 @@
 //
 // Holds the opaque context: argument validation (all of it before any work is
 // enqueued), the chunk table of the multi-tensor-apply launcher (built once per
-// tensor list and kept on the device), the per-warp norm partials, the device
+// tensor list and kept on the device), the norm partials, the device
 // scalars, a cache of device-resident gradient pointer tables for lists too
 // long to pass by value, and the order of the calls of one logical update.
 #include "tl_internal.cuh"
@@ -339,7 +339,7 @@ cudaError_t over_parts(tl_ctx* ctx, Launch launch) {
 // Partial slots the last launch of a partial-writing pass reduces itself (0: the
 // norm is left to the second-stage launch of tl_grad_norm).
 int64_t fin_slots(const tl_ctx* ctx, bool last) {
-    return ctx->fuse_norm && last ? ctx->nchunks * kGroup : 0;
+    return ctx->fuse_norm && last ? ctx->nchunks : 0;   // one slot per run (DevState::run_slots)
 }
 
 // Resolve (and validate) k gradient lists (list-major, ntensors pointers each)
@@ -584,7 +584,9 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     ds.norm_ticket = 0;
     ds.pass_ticket = 0;
     ds.adam_ticket = 0;
-    ds.pad = 0;
+    // contexts that finish the norm in the pass write one partial slot per run
+    ctx->fuse_norm = nchunks > 0 && nchunks <= kFuseNormSlots;
+    ds.run_slots = ctx->fuse_norm ? 1 : 0;
     e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
     // partial slots not at the start of a run stay zero for good
     if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d_partials, 0, sizeof(double) * nc_alloc * kGroup, s);
@@ -600,7 +602,6 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     for (int64_t c = 0; c < nbig; ++c) big_elems += chunks[size_t(c)].len;
     ctx->run[0] = nbig > 0 && big_elems < nbig * (seg_len / 2) ? kRun : 1;
     ctx->run[1] = kRun;
-    ctx->fuse_norm = nchunks > 0 && nchunks * kGroup <= kFuseNormSlots;
     for (int part = 0; part < 2; ++part) {
         const bool small = part == 1;
         const int64_t n = small ? nchunks - nbig : nbig;

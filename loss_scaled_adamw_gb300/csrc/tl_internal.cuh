@@ -15,8 +15,9 @@ namespace tl {
 // whole-CTA chunks come first in the table, then the groups, each part ordered
 // by work, largest first, so that every round of a persistent grid (CTA b takes
 // chunks b, b + G, b + 2G, ...) is balanced; the two parts run as separate
-// launches.  Every chunk writes its own squared-norm partial, so the reduction
-// order (and the norm) does not depend on the grid size.
+// launches.  Every run of chunks (a fixed piece of the table) writes its own
+// squared-norm partials, so the reduction order (and the norm) does not depend on
+// the grid size.
 constexpr int kChunk = 16384;
 #ifndef TL_SMALL
 #define TL_SMALL 1024
@@ -82,7 +83,8 @@ struct DevState {
     uint32_t norm_ticket; // CTAs of the second-stage reduce that have finished, modulo 2^32
     uint32_t pass_ticket; // CTAs of a partial-writing launch that finish the norm in its last CTA (reset by it)
     uint32_t adam_ticket; // CTAs of the AdamW launch that runs the scaler in its last CTA (reset by it)
-    uint32_t pad;
+    int32_t run_slots;    // 1: one squared-norm slot per run (contexts that finish the norm in the pass),
+                          // 0: one per warp per run (the 128-CTA second stage reads them)
 };
 
 // Gradient pointers passed by value (kernel parameter space).
@@ -124,10 +126,16 @@ struct AdamHP {
     int64_t lr_len;
 };
 
-// Partial-writing launches whose context has at most this many squared-norm
-// partial slots finish the norm in their last CTA (no separate reduce launch);
-// longer tables keep the 128-CTA second stage, which reads them faster.
-constexpr int64_t kFuseNormSlots = 32768;
+// Partial-writing launches of a context with at most this many chunks finish the
+// norm in their last CTA (no separate reduce launch), and their runs write one
+// squared-norm slot each (the warps' sums added by the CTA at the end of the run:
+// fewer slots for the last CTA to read, for a block barrier per run); longer tables
+// write one slot per warp per run, which the 128-CTA second stage reads, so that
+// their warps never wait for each other at the end of a chunk.
+#ifndef TL_FUSE_NORM_SLOTS
+#define TL_FUSE_NORM_SLOTS 8192
+#endif
+constexpr int64_t kFuseNormSlots = TL_FUSE_NORM_SLOTS;
 
 // What the a3 kernel reads besides the accumulation buffer.
 enum UnscaleMode : int {
@@ -137,8 +145,8 @@ enum UnscaleMode : int {
 };
 
 // Launchers (tl_kernels.cu).  Each streaming launcher covers chunks [c0, c1); the
-// ones that write squared-norm partials take the chunks in runs of `run` (one
-// partial per warp per run, in the slots of the run's first chunk):
+// ones that write squared-norm partials take the chunks in runs of `run` (slots of
+// the run's first chunk c: c, or c * kGroup + warp; see DevState::run_slots):
 // small = false for whole-CTA chunks (one segment of a large tensor each),
 // small = true for groups of small tensors (one warp per tensor).  `grid` is
 // the persistent grid size; a gtab of nullptr means the pointers are in `inl`.

@@ -807,8 +807,10 @@ __device__ __forceinline__ double warp_sumsq(const SumSqT<P>& acc) {
     return __dadd_rn(__dadd_rn(static_cast<double>(hi), static_cast<double>(lo)), d);
 }
 
-// Write warp w's partial of chunk c and raise the overflow flag if any lane saw a
-// non-finite value.
+// The squared-norm partials of a run (its first chunk c) in the contexts that keep
+// one slot per warp: warp w writes slot c * kGroup + w, and raises the overflow flag
+// if any lane saw a non-finite value.  No barrier: the warps of a CTA never wait for
+// each other at the end of a run.
 template <bool P>
 __device__ __forceinline__ void finish_warp(const SumSqT<P>& sq, bool bad, int64_t c, DevState* st, double* partials) {
     const double part = warp_sumsq(sq);
@@ -816,6 +818,32 @@ __device__ __forceinline__ void finish_warp(const SumSqT<P>& sq, bool bad, int64
     if ((threadIdx.x & 31) == 0) {
         partials[c * kGroup + (threadIdx.x >> 5)] = part;
         if (any_bad) st->found_inf = 1;
+    }
+}
+
+// The squared-norm partial of a run (slot c, its first chunk) in the contexts with
+// one slot per run: each warp's sum
+// reduced by the fixed butterfly above, then the CTA's warps added in warp order by
+// thread 0 after one block barrier (every thread of the CTA ends each of its runs
+// together), one fp64 slot per run.  The warp sums sit in one of two shared buffers
+// by run parity, so the next run's writes never meet thread 0's reads and one
+// barrier per run suffices (the other warps go on with the next run meanwhile).  A warp that saw a non-finite value raises the overflow flag.
+template <bool P>
+__device__ __forceinline__ void finish_run(const SumSqT<P>& sq, bool bad, int64_t c, int parity, DevState* st,
+                                           double* partials) {
+    __shared__ double part_w[2][kThreads / 32];
+    const double part = warp_sumsq(sq);
+    const bool any_bad = __any_sync(0xffffffffu, bad || sq.nan());
+    if ((threadIdx.x & 31) == 0) {
+        part_w[parity][threadIdx.x >> 5] = part;
+        if (any_bad) st->found_inf = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double x = part_w[parity][0];
+#pragma unroll
+        for (int k = 1; k < kThreads / 32; ++k) x = __dadd_rn(x, part_w[parity][k]);
+        partials[c] = x;
     }
 }
 
@@ -996,11 +1024,14 @@ k_unscale(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
     const float inv_s = __fdiv_rn(1.0f, st->S);
     SumSq sq;
     bool bad = false;
+    int nrun = 0;   // runs finished by this CTA (the parity of finish_run's buffer)
+    const bool run_slots = st->run_slots != 0;
     for_runs_nt<NT>(c0, c1, run, [&](int64_t c) {
         if (NT != 32) unscale_segment<NT, GDT, MODE>(chunks[c], threadIdx.x % NT, gp, w, inv_s, sq, bad);
         else unscale_segment<32, GDT, MODE>(group_segment(chunks, c0, c), threadIdx.x & 31, gp, w, inv_s, sq, bad);
     }, [&](int64_t r0) {
-        finish_warp(sq, bad, r0, st, partials);
+        if (run_slots) finish_run(sq, bad, r0, nrun++ & 1, st, partials);
+        else finish_warp(sq, bad, r0, st, partials);
         sq = SumSq();
         bad = false;
     });
@@ -1254,6 +1285,8 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
     // reach the same u give the same norm bit for bit)
     SumSqT<TL_SQ_PAIRS != 0> sq;
     bool bad = false;
+    int nrun = 0;   // runs finished by this CTA (the parity of finish_run's buffer)
+    const bool run_slots = st->run_slots != 0;
     for_runs_nt<NT>(c0, c1, run, [&](int64_t c) {
         if (NT != 32)
             many_segment<NT, GDT, FIRST, LAST, KM, STORE, ROT>(chunks[c], threadIdx.x % NT, inl, a, inv_s, sq, bad);
@@ -1262,7 +1295,8 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
                                                           inv_s, sq, bad);
     }, [&](int64_t r0) {
         if (LAST) {
-            finish_warp(sq, bad, r0, st, partials);
+            if (run_slots) finish_run(sq, bad, r0, nrun++ & 1, st, partials);
+            else finish_warp(sq, bad, r0, st, partials);
             sq = decltype(sq)();
             bad = false;
         }

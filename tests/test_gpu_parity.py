@@ -609,8 +609,8 @@ def test_failed_launch_abandons_the_update(monkeypatch, fused):
     (of two: the small tensor forms a group) reports a failure.  The update in flight is
     abandoned, every update call is refused until tl_set_state restores the scalars, and
     the redone update matches the oracle.  Both with the norm finished by the pass and with
-    a separate norm launch (a list of more than 4,096 chunks)."""
-    numel = [5000, 300, 17000] if fused else [5000, 300, 17000, 4100 * 16384]
+    a separate norm launch (a list of more than 8,192 chunks)."""
+    numel = [5000, 300, 17000] if fused else [5000, 300, 17000, 8200 * 16384]
     wl = custom(numel, k=2, steps=1, counts=[3, 4])
     master0 = W.master_init(wl)
     monkeypatch.setenv("TL_SMALL_GROUP_MIN", "1")
