@@ -239,7 +239,7 @@ int tl_unscale_check_many(tl_ctx* ctx, int k, const void* const* grads, const in
  * disables clipping (coef = 1, the norm is still computed).  The partials
  * are reduced in a fixed order, so the norm is deterministic.  A non-finite
  * squared norm raises the overflow flag.  Where the device work happens: for
- * a context of at most 4,096 chunks the pass of tl_unscale_check (or of the
+ * a context of at most 8,192 chunks the pass of tl_unscale_check (or of the
  * last tl_accumulate_many, or tl_unscale_check_many) reduces the norm in its
  * last CTA and this call launches nothing; longer tables get a second-stage
  * launch here.  Either way the AdamW launch derives the coefficient from the
