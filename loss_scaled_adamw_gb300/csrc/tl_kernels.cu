@@ -564,10 +564,11 @@ constexpr bool kSplitAdam = TL_SPLIT_ADAM != 0;
 // the whole CTA; NT = kSplitThreads, the CTA split into kThreads / NT parts that work
 // as many chunks of a run at once (part h: chunks r0 + h, r0 + h + kThreads / NT,
 // ...), for lists of short segments (runs of several chunks), where a thread's
-// share of a segment's setup then comes with several times the vectors; NT = 32, small-tensor groups (one warp per tensor).  A thread
-// works chunk c as thread threadIdx.x % NT of its segment.  The partials stay one
-// per warp per run, and every partial-writing kernel of a context takes the same
-// form, so the passes that reach the same u give their lanes the same elements.
+// share of a segment's setup then comes with several times the vectors; NT = 32,
+// small-tensor groups (one warp per tensor).  A thread works chunk c as thread
+// threadIdx.x % NT of its segment.  The partials stay per run (finish_warp,
+// finish_run), and every partial-writing kernel of a context takes the same form,
+// so the passes that reach the same u give their lanes the same elements.
 template <int NT, class Work, class Done>
 __device__ __forceinline__ void for_runs_nt(int64_t c0, int64_t c1, int run, Work work, Done done) {
     if (NT != kSplitThreads) {
@@ -1308,7 +1309,7 @@ k_accum_many(const Chunk* __restrict__ chunks, int64_t c0, int64_t c1, int run,
 // a4: deterministic second stage.  [MEG] section 9: global_norm =
 // sqrt(sum ||g||^2), clip_coef = max_norm / (global_norm + eps), applied only
 // below 1 (eps = 1e-6).  kNormBlocks CTAs each reduce a fixed contiguous range
-// of the per-warp partials (per thread eight interleaved accumulators, then a
+// of the partial slots (per thread eight interleaved accumulators, then a
 // fixed butterfly and a fixed warp-order sum) into one slot.  Each CTA then
 // takes a ticket; the CTA holding the last ticket of the launch adds the slots
 // in slot order and finishes.  Nothing waits: the last CTA only runs after every
