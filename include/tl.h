@@ -289,6 +289,35 @@ int tl_grad_norm_from(tl_ctx* ctx, const double* d_sumsq, const int32_t* d_flag,
 int tl_partition(int64_t ntensors, const int64_t* numel, int32_t nranks, int32_t rank, int64_t align,
                  int64_t* tensor, int64_t* start, int64_t* len, int64_t cap, int64_t* count);
 
+/* How tl_create lays out a tensor list, from its sizes alone (host only: no
+ * CUDA call).  The list becomes a table of chunks: whole-CTA segments (pieces
+ * of at most `seg` elements of one tensor; seg is the longest power of two from
+ * 16,384 down to 4,096 that still gives at least 24 segments per SM) and, when
+ * the list holds at least 128 tensors of at most 1,024 elements, groups of up
+ * to 8 such tensors worked one per warp.  Runs of chunks write the squared-norm
+ * partials: one chunk per run where the segments are mostly full, 4 where they
+ * are short, and then the passes take the split forms (several segments per
+ * CTA).  A table of at most 8,192 chunks finishes the norm in the last CTA of
+ * the partial-writing pass (tl_grad_norm then launches nothing).
+ * sm_count: the SM count of the device the context will run on (152 on a
+ * GB300; tl_create reads it from the device).  The environment variable
+ * TL_SMALL_GROUP_MIN, when set, replaces the 128 (as it does for tl_create).
+ * Errors: TL_EINVAL (ntensors < 0, NULL arrays, a negative size, sm_count < 1,
+ * a list too large to index). */
+typedef struct {
+    int64_t nchunks;     /* chunks of the table: nbig + ngroups */
+    int64_t nbig;        /* whole-CTA segments */
+    int64_t ngroups;     /* groups of up to 8 small tensors */
+    int64_t seg;         /* segment length, elements */
+    int64_t nsmall;      /* tensors in the groups */
+    int32_t run_big;     /* chunks per squared-norm run, whole-CTA part (1 or 4) */
+    int32_t run_small;   /* ... in the groups (4) */
+    int32_t split_forms; /* 1: the whole-CTA part takes the split forms */
+    int32_t fused_norm;  /* 1: the partial-writing pass finishes the norm */
+} tl_plan_info;
+
+int tl_plan(int64_t ntensors, const int64_t* numel, int32_t sm_count, tl_plan_info* out);
+
 /* Clip + AdamW on the fp32 masters + recast to the model dtype (a5).
  * [MEG] sections 7 and 9 (clip with the global coefficient, step the fp32
  * masters, copy back to model precision); [ZRO] "Why the optimizer state is

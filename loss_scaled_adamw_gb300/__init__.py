@@ -34,7 +34,7 @@ EXPORTED = ("tl_create", "tl_destroy", "tl_accumulate", "tl_accumulate_many", "t
             "tl_clip_adamw_step", "tl_scaler_update", "tl_read_status", "tl_get_state", "tl_set_state",
             "tl_scale_ptr", "tl_num_params", "tl_num_chunks", "tl_launch_count", "tl_status_string",
             "tl_last_error", "tl_unscale_norm_noalloc", "tl_loss_seed", "tl_set_lr_schedule",
-            "tl_local_sumsq", "tl_grad_norm_from", "tl_partition")
+            "tl_local_sumsq", "tl_grad_norm_from", "tl_partition", "tl_plan")
 
 
 class TLError(RuntimeError):
@@ -70,6 +70,15 @@ class tl_status(ctypes.Structure):
                 ("b2p", ctypes.c_double)]
 
     def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class tl_plan_info(ctypes.Structure):
+    _fields_ = [("nchunks", ctypes.c_int64), ("nbig", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("seg", ctypes.c_int64), ("nsmall", ctypes.c_int64), ("run_big", ctypes.c_int32),
+                ("run_small", ctypes.c_int32), ("split_forms", ctypes.c_int32), ("fused_norm", ctypes.c_int32)]
+
+    def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
@@ -133,6 +142,7 @@ def load_library():
         "tl_partition": (i32, [i64, ctypes.POINTER(i64), ctypes.c_int32, ctypes.c_int32, i64,
                                ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64), i64,
                                ctypes.POINTER(i64)]),
+        "tl_plan": (i32, [i64, ctypes.POINTER(i64), ctypes.c_int32, ctypes.POINTER(tl_plan_info)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -347,6 +357,20 @@ def tl_partition(numel: Sequence[int], nranks: int, rank: int, align: int = 1):
     if rc != TL_OK:
         raise TLError("tl_partition", rc, lib.tl_status_string(rc).decode())
     return [(int(t[q]), int(s[q]), int(l[q])) for q in range(cnt.value)]
+
+
+def tl_plan(numel: Sequence[int], sm_count: int = 152) -> dict:
+    """How tl_create lays out a tensor list of these sizes on a device of sm_count SMs
+    (host only): the chunk table's counts, the segment length, the squared-norm run
+    lengths, whether the split forms run and whether the pass finishes the norm."""
+    lib = load_library()
+    n = len(numel)
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numel])
+    out = tl_plan_info()
+    rc = lib.tl_plan(n, arr, int(sm_count), ctypes.byref(out))
+    if rc != TL_OK:
+        raise TLError("tl_plan", rc, lib.tl_status_string(rc).decode())
+    return out.as_dict()
 
 
 def tl_num_params(ctx: Context) -> int:

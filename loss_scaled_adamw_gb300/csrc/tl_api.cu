@@ -40,8 +40,8 @@ constexpr int64_t kSegPerSm = TL_SEG_PER_SM;
 // Small tensors are grouped one per warp (a part of the table with its own launch)
 // only when the list holds at least this many of them; fewer small tensors become
 // whole-CTA segments of their own, so the pass is one launch.  The environment
-// variable TL_SMALL_GROUP_MIN, read by tl_create, overrides it (tests set 1 to run
-// the group kernels on short lists).
+// variable TL_SMALL_GROUP_MIN (read by make_plan, for tl_create and tl_plan)
+// overrides it (tests set 1 to run the group kernels on short lists).
 constexpr int64_t kGroupMin = 128;
 
 int elem_size(int dt) { return dt == TL_F32 ? 4 : dt == TL_E4M3B16 ? 1 : 2; }
@@ -389,6 +389,91 @@ void free_ctx(tl_ctx* ctx) {
     delete ctx;
 }
 
+// The chunk table of a tensor list, decided from the sizes and the SM count alone
+// (tl_create adds each segment's state addresses; tl_plan reports it).  A large
+// tensor becomes one segment per `seg` elements; small tensors (<= kSmall elements)
+// are grouped kGroup to a chunk, one per warp, when there are at least
+// small_group_min() of them.  Chunks are then ordered by work, largest first
+// (stable): the whole-CTA part, then the groups, so every round of a persistent
+// grid gets chunks of similar size.
+struct PlanSeg {
+    int64_t tensor, start, len;
+};
+struct PlanChunk {
+    std::vector<PlanSeg> segs;
+    int64_t work = 0;
+    bool group = false;
+};
+struct Plan {
+    int64_t seg = kChunk;           // segment length
+    std::vector<PlanChunk> chunks;  // whole-CTA chunks, then the groups
+    int64_t nbig = 0;               // whole-CTA chunks
+    int run[2] = {1, 1};            // chunks per squared-norm run, per part (whole-CTA, groups)
+    bool fuse_norm = false;         // the partial-writing pass finishes the norm (one slot per run)
+};
+
+int64_t small_group_min() {
+    if (const char* g = std::getenv("TL_SMALL_GROUP_MIN")) return std::max<int64_t>(1, std::atoll(g));
+    return kGroupMin;
+}
+
+// numel: ntensors sizes, validated by the caller (non-negative, P within range).
+Plan make_plan(int64_t ntensors, const int64_t* numel, int sm_count) {
+    Plan pl;
+    int64_t P = 0, n_small = 0, small_elems = 0;
+    for (int64_t i = 0; i < ntensors; ++i) {
+        if (numel[i] <= 0) continue;
+        P += numel[i];
+        if (numel[i] <= kSmall) { ++n_small; small_elems += numel[i]; }
+    }
+    const bool grouping = n_small >= small_group_min();
+    const int64_t whole = P - (grouping ? small_elems : 0);
+    int64_t seg = kChunk;
+    while (seg > kMinSeg && whole / seg < kSegPerSm * sm_count) seg /= 2;
+    pl.seg = seg;
+    PlanChunk group;
+    group.group = true;
+    for (int64_t i = 0; i < ntensors; ++i) {
+        if (numel[i] <= 0) continue;
+        if (grouping && numel[i] <= kSmall) {
+            group.segs.push_back(PlanSeg{i, 0, numel[i]});
+            group.work += numel[i];
+            if (int(group.segs.size()) == kGroup) {
+                pl.chunks.push_back(std::move(group));
+                group = PlanChunk();
+                group.group = true;
+            }
+            continue;
+        }
+        for (int64_t st = 0; st < numel[i]; st += seg) {
+            PlanChunk one;
+            const int64_t len = std::min<int64_t>(seg, numel[i] - st);
+            one.segs.push_back(PlanSeg{i, st, len});
+            one.work = len;
+            pl.chunks.push_back(std::move(one));
+        }
+    }
+    if (!group.segs.empty()) pl.chunks.push_back(std::move(group));
+    std::stable_sort(pl.chunks.begin(), pl.chunks.end(), [](const PlanChunk& a, const PlanChunk& b) {
+        if (a.group != b.group) return b.group;
+        return a.work > b.work;
+    });
+    int64_t big_elems = 0;
+    for (const PlanChunk& cb : pl.chunks) {
+        if (cb.group) continue;
+        ++pl.nbig;
+        big_elems += cb.work;
+    }
+    // chunks are mostly full segments: one squared-norm partial each; where they are
+    // short (one warp or a few), kRun of them per partial, which also selects the split
+    // forms of the partial-writing and AdamW passes
+    pl.run[0] = pl.nbig > 0 && big_elems < pl.nbig * (seg / 2) ? kRun : 1;
+    pl.run[1] = kRun;
+    const int64_t nchunks = int64_t(pl.chunks.size());
+    pl.fuse_norm = nchunks > 0 && nchunks <= kFuseNormSlots;
+    return pl;
+}
+
 }  // namespace
 
 extern "C" {
@@ -474,80 +559,30 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     if (const char* f = std::getenv("TL_TEST_FAIL_LAUNCH")) ctx->fail_at = std::atoll(f);
     if (e != cudaSuccess) { free_ctx(ctx); return TL_ECUDA; }
 
-    // Segments and chunks.  A large tensor becomes one chunk per `seg` elements;
-    // small tensors (<= kSmall elements) are grouped kGroup to a chunk, one per warp,
-    // when there are many of them.  Chunks are then ordered by work, largest first
-    // (stable), so every round of the persistent grid gets chunks of similar size.
-    int64_t group_min = kGroupMin;
-    if (const char* g = std::getenv("TL_SMALL_GROUP_MIN")) group_min = std::max<int64_t>(1, std::atoll(g));
-    int64_t n_small = 0, small_elems = 0;
-    for (int64_t i = 0; i < ntensors; ++i)
-        if (numel[i] > 0 && numel[i] <= kSmall) { ++n_small; small_elems += numel[i]; }
-    const bool grouping = n_small >= group_min;
-    {
-        const int64_t whole = P - (grouping ? small_elems : 0);
-        int64_t seg = kChunk;
-        while (seg > kMinSeg && whole / seg < kSegPerSm * ctx->sm_count) seg /= 2;
-        ctx->seg = seg;
-    }
-    const int64_t seg_len = ctx->seg;
-    struct ChunkBuild {
-        std::vector<Chunk> segs;
-        int64_t work = 0;
-        bool group = false;
-    };
-    std::vector<ChunkBuild> built;
-    ChunkBuild group;
-    group.group = true;
-    // the descriptor of elements [st, st + len) of tensor i, with its state addresses
-    auto seg = [&](int64_t i, int64_t st, int64_t len) {
+    // The chunk table (make_plan), with each segment's state addresses.  Whole-CTA
+    // chunk c is segment c; every group holds kGroup segments, a short group padded
+    // with empty segments (its first tensor, length 0) so that a warp finds its
+    // tensor without an index table.
+    const Plan pl = make_plan(ntensors, numel, ctx->sm_count);
+    ctx->seg = pl.seg;
+    const int64_t nbig = pl.nbig;
+    auto seg = [&](const PlanSeg& q) {
+        const int64_t i = q.tensor, st = q.start;
         return Chunk{acc[i] + st, master[i] + st, m[i] + st, v[i] + st,
-                     static_cast<char*>(param[i]) + st * pes, st, int32_t(i), int32_t(len), (numel[i] + 15) / 16 * 16};
+                     static_cast<char*>(param[i]) + st * pes, st, int32_t(i), int32_t(q.len), (numel[i] + 15) / 16 * 16};
     };
-    for (int64_t i = 0; i < ntensors; ++i) {
-        if (numel[i] == 0) continue;
-        if (grouping && numel[i] <= kSmall) {
-            group.segs.push_back(seg(i, 0, numel[i]));
-            group.work += numel[i];
-            if (int(group.segs.size()) == kGroup) {
-                built.push_back(std::move(group));
-                group = ChunkBuild();
-                group.group = true;
-            }
-            continue;
-        }
-        for (int64_t st = 0; st < numel[i]; st += seg_len) {
-            ChunkBuild one;
-            const int32_t len = int32_t(std::min<int64_t>(seg_len, numel[i] - st));
-            one.segs.push_back(seg(i, st, len));
-            one.work = len;
-            built.push_back(std::move(one));
-        }
-    }
-    if (!group.segs.empty()) built.push_back(std::move(group));
-    // whole-CTA chunks first, then the groups; each part by work, largest first
-    std::stable_sort(built.begin(), built.end(), [](const ChunkBuild& a, const ChunkBuild& b) {
-        if (a.group != b.group) return b.group;
-        return a.work > b.work;
-    });
-    int64_t nbig = 0;
-    for (const ChunkBuild& cb : built)
-        if (!cb.group) ++nbig;
-    // whole-CTA chunk c is segment c; every group holds kGroup segments, a short
-    // group padded with empty segments (its first tensor, length 0) so that a warp
-    // finds its tensor without an index table
     std::vector<Chunk> chunks;
-    chunks.reserve(size_t(nbig) + (built.size() - size_t(nbig)) * kGroup);
-    for (size_t b = 0; b < built.size(); ++b) {
-        const ChunkBuild& cb = built[b];
-        chunks.insert(chunks.end(), cb.segs.begin(), cb.segs.end());
+    chunks.reserve(size_t(nbig) + (pl.chunks.size() - size_t(nbig)) * kGroup);
+    for (size_t b = 0; b < pl.chunks.size(); ++b) {
+        const PlanChunk& cb = pl.chunks[b];
+        for (const PlanSeg& q : cb.segs) chunks.push_back(seg(q));
         if (int64_t(b) >= nbig) {
-            Chunk pad = cb.segs[0];
+            Chunk pad = seg(cb.segs[0]);
             pad.len = 0;
             for (size_t i = cb.segs.size(); i < size_t(kGroup); ++i) chunks.push_back(pad);
         }
     }
-    nchunks = int64_t(built.size());
+    nchunks = int64_t(pl.chunks.size());
     ctx->nchunks = nchunks;
     ctx->nbig = nbig;
     const size_t nc_alloc = size_t(std::max<int64_t>(nchunks, 1));
@@ -585,7 +620,7 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     ds.pass_ticket = 0;
     ds.adam_ticket = 0;
     // contexts that finish the norm in the pass write one partial slot per run
-    ctx->fuse_norm = nchunks > 0 && nchunks <= kFuseNormSlots;
+    ctx->fuse_norm = pl.fuse_norm;
     ds.run_slots = ctx->fuse_norm ? 1 : 0;
     e = cudaMemcpyAsync(ctx->d_state, &ds, sizeof(ds), cudaMemcpyHostToDevice, s);
     // partial slots not at the start of a run stay zero for good
@@ -598,10 +633,8 @@ int tl_create(tl_ctx** out, int64_t ntensors, const int64_t* numel, void* const*
     // Persistent grid sizes from the occupancy of each kernel variant the
     // context's dtypes can launch.
     const int gdt = cfg->grad_dtype, pdt = cfg->param_dtype;
-    int64_t big_elems = 0;
-    for (int64_t c = 0; c < nbig; ++c) big_elems += chunks[size_t(c)].len;
-    ctx->run[0] = nbig > 0 && big_elems < nbig * (seg_len / 2) ? kRun : 1;
-    ctx->run[1] = kRun;
+    ctx->run[0] = pl.run[0];
+    ctx->run[1] = pl.run[1];
     for (int part = 0; part < 2; ++part) {
         const bool small = part == 1;
         const int64_t n = small ? nchunks - nbig : nbig;
@@ -1093,6 +1126,29 @@ int tl_set_lr_schedule(tl_ctx* ctx, const float* lr_table, int64_t len) {
     }
     ctx->lr_sched = lr_table;
     ctx->lr_len = len;
+    return TL_OK;
+}
+
+int tl_plan(int64_t ntensors, const int64_t* numel, int32_t sm_count, tl_plan_info* out) {
+    if (out == nullptr || ntensors < 0 || ntensors > (int64_t(1) << 31) - 1 || sm_count < 1) return TL_EINVAL;
+    if (ntensors > 0 && numel == nullptr) return TL_EINVAL;
+    int64_t P = 0;
+    for (int64_t i = 0; i < ntensors; ++i) {
+        if (numel[i] < 0 || numel[i] > (int64_t(1) << 62) / 4 - P) return TL_EINVAL;
+        P += numel[i];
+    }
+    const Plan pl = make_plan(ntensors, numel, sm_count);
+    tl_plan_info r{};
+    r.nchunks = int64_t(pl.chunks.size());
+    r.nbig = pl.nbig;
+    r.ngroups = r.nchunks - r.nbig;
+    r.seg = pl.seg;
+    for (size_t b = size_t(pl.nbig); b < pl.chunks.size(); ++b) r.nsmall += int64_t(pl.chunks[b].segs.size());
+    r.run_big = pl.run[0];
+    r.run_small = pl.run[1];
+    r.split_forms = kPairSegs && pl.run[0] > 1 ? 1 : 0;
+    r.fused_norm = pl.fuse_norm ? 1 : 0;
+    *out = r;
     return TL_OK;
 }
 

@@ -54,6 +54,16 @@ int main(void) {
     FIELD(tl_norm_result, found_inf);
     FIELD(tl_norm_result, reserved);
     FIELD(tl_norm_result, sumsq);
+    printf("tl_plan_info %zu\n", sizeof(tl_plan_info));
+    FIELD(tl_plan_info, nchunks);
+    FIELD(tl_plan_info, nbig);
+    FIELD(tl_plan_info, ngroups);
+    FIELD(tl_plan_info, seg);
+    FIELD(tl_plan_info, nsmall);
+    FIELD(tl_plan_info, run_big);
+    FIELD(tl_plan_info, run_small);
+    FIELD(tl_plan_info, split_forms);
+    FIELD(tl_plan_info, fused_norm);
     /* the constants are plain integer expressions */
     printf("TL_OK %d\nTL_EINVAL %d\nTL_ECUDA %d\nTL_ESTATE %d\nTL_ENOMEM %d\n", TL_OK, TL_EINVAL, TL_ECUDA,
            TL_ESTATE, TL_ENOMEM);
@@ -62,7 +72,8 @@ int main(void) {
     any_fn fns[] = {
         (any_fn)&tl_create, (any_fn)&tl_destroy, (any_fn)&tl_accumulate, (any_fn)&tl_unscale_check,
         (any_fn)&tl_accumulate_many, (any_fn)&tl_unscale_check_many, (any_fn)&tl_grad_norm,
-        (any_fn)&tl_local_sumsq, (any_fn)&tl_grad_norm_from, (any_fn)&tl_partition, (any_fn)&tl_clip_adamw_step,
+        (any_fn)&tl_local_sumsq, (any_fn)&tl_grad_norm_from, (any_fn)&tl_partition, (any_fn)&tl_plan,
+        (any_fn)&tl_clip_adamw_step,
         (any_fn)&tl_set_lr_schedule, (any_fn)&tl_scaler_update, (any_fn)&tl_read_status, (any_fn)&tl_get_state,
         (any_fn)&tl_set_state, (any_fn)&tl_scale_ptr, (any_fn)&tl_loss_seed, (any_fn)&tl_num_params,
         (any_fn)&tl_num_chunks, (any_fn)&tl_unscale_norm_noalloc, (any_fn)&tl_launch_count,

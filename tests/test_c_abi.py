@@ -36,7 +36,7 @@ def test_c99_sees_the_binding_layout(tmp_path):
     out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
     got = dict(line.rsplit(" ", 1) for line in out.strip().splitlines())
     got = {k: int(v) for k, v in got.items()}
-    for cls in (tl.tl_config, tl.tl_adamw_hp, tl.tl_state, tl.tl_status, tl.tl_norm_result):
+    for cls in (tl.tl_config, tl.tl_adamw_hp, tl.tl_state, tl.tl_status, tl.tl_norm_result, tl.tl_plan_info):
         name = cls.__name__
         assert got[name] == ctypes.sizeof(cls), name
         for field, _ in cls._fields_:
