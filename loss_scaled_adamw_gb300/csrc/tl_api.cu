@@ -1146,7 +1146,7 @@ int tl_plan(int64_t ntensors, const int64_t* numel, int32_t sm_count, tl_plan_in
     for (size_t b = size_t(pl.nbig); b < pl.chunks.size(); ++b) r.nsmall += int64_t(pl.chunks[b].segs.size());
     r.run_big = pl.run[0];
     r.run_small = pl.run[1];
-    r.split_forms = kPairSegs && pl.run[0] > 1 ? 1 : 0;
+    r.split_forms = pl.run[0] > 1 ? 1 : 0;   // the rule of the default build (TL_PAIR_SEGS on)
     r.fused_norm = pl.fuse_norm ? 1 : 0;
     *out = r;
     return TL_OK;

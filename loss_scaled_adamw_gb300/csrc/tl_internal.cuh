@@ -36,11 +36,6 @@ constexpr int kThreads = 256;        // streaming kernels: 8 warps per CTA
 #define TL_SPLIT_THREADS 64
 #endif
 constexpr int kSplitThreads = TL_SPLIT_THREADS;
-// Lists of short segments (runs of several chunks) take the split forms (TL_PAIR_SEGS).
-#ifndef TL_PAIR_SEGS
-#define TL_PAIR_SEGS 1
-#endif
-constexpr bool kPairSegs = TL_PAIR_SEGS != 0;
 static_assert(kSplitThreads % 32 == 0 && kSplitThreads > 32 && kThreads % kSplitThreads == 0,
               "a split form works a segment with whole warps (32 is the small-tensor form)");
 constexpr int kNormThreads = 256;    // threads per CTA of the second-stage reduce

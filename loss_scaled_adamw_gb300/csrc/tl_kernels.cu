@@ -549,6 +549,12 @@ __device__ __forceinline__ void for_runs(int64_t c0, int64_t c1, int run, Work w
     }
 }
 
+// Lists of short segments take the split forms (TL_PAIR_SEGS; tl_plan reports the
+// forms by the default, on).
+#ifndef TL_PAIR_SEGS
+#define TL_PAIR_SEGS 1
+#endif
+constexpr bool kPairSegs = TL_PAIR_SEGS != 0;
 // ... and so do the AdamW passes (TL_SPLIT_ADAM)
 #ifndef TL_SPLIT_ADAM
 #define TL_SPLIT_ADAM 1
