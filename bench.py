@@ -436,6 +436,17 @@ TRAFFIC_KEYS = {"accumulate": "k_accumulate_bf16", "clip_adamw_step": "k_adamw_b
                 "accumulate_many": "k_accum_many_bf16_first_last"}
 
 
+def table_plan(tl, numel, local_rank):
+    """The chunk table the context lays this list out in on this device (tl_plan, host
+    only): chunk counts, segment length, squared-norm runs, split forms, fused norm."""
+    import torch
+    try:
+        sm = torch.cuda.get_device_properties(local_rank).multi_processor_count
+        return tl.tl_plan(list(numel), sm)
+    except Exception as exc:   # a note on the layout must never cost the measurement
+        return {"error": str(exc)[:200]}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import loss_scaled_adamw_gb300 as tl
@@ -475,7 +486,8 @@ def run_gpu(args, rank, world, local_rank):
                    "layout": args.layout,
                    "l2": (f"no flush: every launch streams >= {P * 6 / 1e9:.1f} GB, far above the 129 MB L2"
                           if P * 6 > 10 * 129e6 else "small case: the working set fits in L2 (launch-latency bound)"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "table": table_plan(tl, wl.numel, local_rank)},
         "hbm": head["hbm"],
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": peak,
                      "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_kind": peak_kind,
